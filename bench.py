@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""Benchmark of the linear-attention hot path on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one causal la_forward over one batch of the main workload
+(bf16 q, k, v [B=4, H=16, N=4096, d=64], N(0,1)/sqrt(d), seed = rank).  The
+other paths of the hot path (non-causal form on the same batch, long-context
+causal, causal with per-head decay, fp32 causal, recurrent decode) are timed
+in the same run and reported under "paths".  Rank 0 prints one JSON line.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the stream the library launches on, with a 256 MiB write between steps to
+flush L2; barrier + synchronize on both sides of the timed region; the max
+over ranks is taken.  `value` = tokens (B*N per step, summed over ranks) per
+second.  `e2e` repeats the main step through the C ABI with pinned host
+buffers, the host->device copies of q, k, v and the device->host copy of the
+output inside the timed region.
+
+--impl reference times the CPU oracle (the slow double-precision reference
+that the parity tests use) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("causal linear-attn tokens/s and % tensor roofline; "
+          "decode step % HBM peak")
+MAIN = "bf16_b4h16_n4096_d64"
+FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]),
+                "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained",
+                                                     j["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+               "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "-i",
+                 str(self.idx), "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        load = [r for r in self.rows if (num(r[3]) or 0) >= 50]
+        use = load or self.rows
+        sm = [num(r[0]) for r in use if num(r[0]) is not None]
+        smax = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        reasons = sorted({name for r in use
+                          for name, val in zip(self.REASONS, r[4:8])
+                          if val.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(self.rows),
+                "samples_under_load": len(load)}
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_steps(fn, K, W, world, flush=None):
+    """Per-step CUDA-event durations (ms) of K steps after W warm-ups."""
+    import torch
+    for _ in range(W):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for s, e in ev:
+        if flush is not None:
+            flush()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def forward_bytes(B, H, N, d, elem):
+    """Compulsory HBM bytes of one forward: q, k, v read once, out written
+    once."""
+    return 4 * B * H * N * d * elem
+
+
+def roofline_hbm(bytes_per_launch, ms, peak_gbs, traffic=None):
+    achieved = bytes_per_launch / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(achieved / peak_gbs, 4), "traffic": traffic}
+
+
+def tensor_fraction(flops_per_launch, ms, peak_tflops):
+    t = flops_per_launch / (ms * 1e-3) / 1e12
+    return {"achieved_tflops": round(t, 2), "peak_tflops": peak_tflops,
+            "frac": round(t / peak_tflops, 4)}
+
+
+def chunk_flops(B, H, N, d, C):
+    """FLOPs of the chunked causal method with full C x C blocks: per token
+    2*(2 d^2 + 2 C d)."""
+    return 2 * (2 * d * d + 2 * C * d) * B * H * N
+
+
+# ------------------------------------------------------------------ our arm
+
+
+def run_ours(args):
+    import torch
+    import linear_attention_feature_gb300 as la
+    from linear_attention_feature_gb300 import workloads as wl
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    la.build.build()
+    la.load_library()
+    peaks = load_peaks()
+    K, W = args.steps, args.warmup
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    sampler = ClockSampler(gpu_index).start()
+
+    # ---------------- main: causal forward on the main workload
+    w = wl.WORKLOADS[MAIN]
+    q, k, v = (t.to(dev) for t in wl.make_workload_qkv(w, seed=rank))
+    out = torch.empty_like(q)
+    main_fn = lambda: la.forward(q, k, v, causal=True, out=out)  # noqa: E731
+    n0 = la.kernel_launch_count()
+    steps_ms = timed_steps(main_fn, K, W, world, flush)
+    launches = (la.kernel_launch_count() - n0)
+    # launches in the timed region = total minus the W warm-ups' share
+    launches = launches * K // (K + W)
+    la.check_device_status()
+    ms = max_over_ranks(sum(steps_ms) / K, world)
+    tokens_step = w.B * w.N
+    value = tokens_step * world / (ms * 1e-3)
+    byts = forward_bytes(w.B, w.H, w.N, w.d, 2)
+    C = 64
+    roof = roofline_hbm(byts, ms, peaks["hbm_gbs"])
+    tens = tensor_fraction(chunk_flops(w.B, w.H, w.N, w.d, C), ms,
+                           peaks["bf16_tflops"])
+
+    # ---------------- e2e through the C ABI with host buffers
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qd, kd, vd, od = (torch.empty_like(q) for _ in range(4))
+
+    def e2e_fn():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        la.forward(qd, kd, vd, causal=True, out=od)
+        oh.copy_(od, non_blocking=True)
+    e2e_ms = timed_steps(e2e_fn, K, W, world)
+    e2e_t = max_over_ranks(sum(e2e_ms) / K, world)
+    e2e = {"value": round(tokens_step * world / (e2e_t * 1e-3), 1),
+           "unit": "tokens/s", "h2d_bytes_per_step": 3 * q.numel() * 2,
+           "d2h_bytes_per_step": out.numel() * 2,
+           "ms_per_step": round(e2e_t, 4)}
+    del qh, kh, vh, oh, qd, kd, vd, od
+
+    paths = {}
+    if not args.main_only:
+        paths = run_other_paths(args, la, wl, dev, flush, peaks, world, rank,
+                                q, k, v, out)
+    clocks = sampler.stop()
+
+    # ---------------- CPU baseline (oracle) on rank 0
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w, q, k, v, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{MAIN} causal", "B": w.B, "H": w.H,
+                       "N": w.N, "d": w.d, "global_batch": w.B * world,
+                       "seq_len": w.N, "parallelism": f"replicas{world}",
+                       "inputs": "N(0,1)/sqrt(d), bf16, seed=rank",
+                       "l2": "flushed between timed steps (256 MiB write)"},
+            "roofline": roof, "tensor": tens, "chunk": C,
+            "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks, "cpu_baseline": cpu, "paths": paths,
+            "peaks": peaks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
+    import torch
+    res = {}
+    Kx, Wx = max(3, args.steps // 2), max(3, args.warmup)
+
+    def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2):
+        w = wl.WORKLOADS[wkey]
+        try:
+            if inputs is None:
+                qq, kk, vv = (t.to(dev) for t in wl.make_workload_qkv(w, seed=rank))
+            else:
+                qq, kk, vv = inputs
+            oo = torch.empty_like(qq)
+            fn = lambda: la.forward(qq, kk, vv, causal=causal, decay=decay, out=oo)  # noqa
+            steps = timed_steps(fn, Kx, Wx, world, flush)
+            la.check_device_status()
+            ms = max_over_ranks(sum(steps) / Kx, world)
+            r = {"tokens_per_s": round(w.B * w.N * world / (ms * 1e-3), 1),
+                 "ms_per_step": round(ms, 4), "steps": Kx,
+                 "roofline": roofline_hbm(forward_bytes(w.B, w.H, w.N, w.d, elem),
+                                          ms, peaks["hbm_gbs"])}
+            if causal and elem == 2:
+                C = 64 if w.d == 64 else 128
+                r["tensor"] = tensor_fraction(chunk_flops(w.B, w.H, w.N, w.d, C),
+                                              ms, peaks["bf16_tflops"])
+                r["chunk"] = C
+            res[name] = r
+        except Exception as e:  # keep the main line; report the failure
+            res[name] = {"error": f"{type(e).__name__}: {e}"}
+
+    fwd_path(f"{MAIN} noncausal", MAIN, False, inputs=(q, k, v))
+    fwd_path("bf16_b2h16_n32768_d128 causal", "bf16_b2h16_n32768_d128", True)
+    wd = wl.WORKLOADS["bf16_decay_b4h8_n16384_d128"]
+    fwd_path("bf16_decay_b4h8_n16384_d128 causal", wd.name, True,
+             decay=list(wd.decay))
+    fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
+    try:
+        res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,
+                                                args)
+    except Exception as e:
+        res["decode_b256h32_d128"] = {"error": f"{type(e).__name__}: {e}"}
+    return res
+
+
+def decode_bytes(BH, d, elem):
+    """Compulsory bytes of one decode step: S and z read and written (fp32),
+    q, k, v read, out written."""
+    return BH * (2 * (d * d + d) * 4 + 4 * d * elem)
+
+
+def run_decode(la, wl, dev, peaks, world, rank, args):
+    import torch
+    w = wl.WORKLOADS["decode_b256h32_d128"]
+    B, H, d = w.B, w.H, w.d
+    P, T = w.extra["prefill"], w.extra["steps"]
+    if args.decode_steps:
+        T = args.decode_steps
+    q, k, v = wl.make_decode_tokens(B, H, d, P + T, "bf16", seed=100 + rank,
+                                    device=dev)
+    S = torch.zeros(B, H, d, d, device=dev)
+    z = torch.zeros(B, H, d, device=dev)
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    for t in range(P):  # prefill from the 1024 seeded tokens (untimed)
+        la.decode_step(S, z, q[t], k[t], v[t], out=o)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for t in range(P, P + T):
+        la.decode_step(S, z, q[t], k[t], v[t], out=o)
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    la.check_device_status()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world)
+    ms = ms_total / T
+    return {"tokens_per_s": round(B * T * world / (ms_total * 1e-3), 1),
+            "ms_per_step": round(ms, 5), "steps": T, "prefill": P,
+            "state_bytes": S.numel() * 4,
+            "l2": "state (512 MiB) larger than L2; steps back to back",
+            "roofline": roofline_hbm(decode_bytes(B * H, d, 2), ms,
+                                     peaks["hbm_gbs"])}
+
+
+# ------------------------------------------------------------------ oracle
+
+
+def cpu_baseline(w, q, k, v, seconds):
+    """Time the oracle (as it stands) on a bounded sample of the main
+    workload: whole heads of the causal form, on all host cores."""
+    import oracle
+    cores = os.cpu_count() or 1
+    qs, ks, vs = (t.cpu() for t in (q, k, v))
+    BH = w.B * w.H
+    # calibrate on one head, then take as many heads as fit the budget
+    t0 = time.perf_counter()
+    oracle.causal(qs[0, :1], ks[0, :1], vs[0, :1], nthreads=1)
+    per_head = time.perf_counter() - t0
+    heads = int(max(1, min(BH, seconds * cores / max(per_head, 1e-6))))
+    heads = max(cores, heads) if BH >= cores else BH
+    heads = min(heads, BH)
+    qf = qs.reshape(BH, w.N, w.d)[:heads]
+    kf = ks.reshape(BH, w.N, w.d)[:heads]
+    vf = vs.reshape(BH, w.N, w.d)[:heads]
+    t0 = time.perf_counter()
+    oracle.causal(qf, kf, vf, nthreads=cores)
+    dt = time.perf_counter() - t0
+    frac = heads / BH
+    return {"value": round(frac * w.B * w.N / dt, 1), "unit": "tokens/s",
+            "cores": min(cores, heads), "kind": "oracle",
+            "sample": f"causal form, {heads} of {BH} heads of {MAIN} "
+                      f"(N={w.N}, d={w.d}), fp64, {dt:.2f} s; tokens/s "
+                      f"scaled by the head fraction"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    from linear_attention_feature_gb300 import workloads as wl
+    w = wl.WORKLOADS[MAIN]
+    q, k, v = wl.make_workload_qkv(w, seed=0)
+    cores = os.cpu_count() or 1
+    BH = w.B * w.H
+    heads = min(BH, cores)  # one head per core per step
+    qf = q.reshape(BH, w.N, w.d)[:heads]
+    kf = k.reshape(BH, w.N, w.d)[:heads]
+    vf = v.reshape(BH, w.N, w.d)[:heads]
+    for _ in range(args.warmup):
+        oracle.causal(qf, kf, vf, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.causal(qf, kf, vf, nthreads=cores)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = (heads / BH) * w.B * w.N / dt
+    sample = (f"each step: causal form on {heads} of {BH} heads of {MAIN} "
+              f"(N={w.N}, d={w.d}), fp64; tokens/s scaled by the head fraction")
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "impl": "reference", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{MAIN} causal", "B": w.B, "H": w.H,
+                       "N": w.N, "d": w.d, "global_batch": w.B,
+                       "seq_len": w.N},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s",
+                             "cores": heads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--main-only", action="store_true",
+                    help="time only the main causal step")
+    ap.add_argument("--no-cpu", action="store_true",
+                    help="skip the CPU-baseline timing of the oracle")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="timed decode steps (default: the workload's 1024)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,149 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) kernelised linear-attention
+ * library (liblinattn.so).
+ *
+ * The operation ("Linear Attention", generalised-kernel equations and the
+ * causal running statistics; "Story of Attention - Part 5: Linear Attention:
+ * Kernels, Decay, and Gating", section 1a):
+ *
+ *   phi(x)  = elu(x) + 1   (alpha = 1), applied elementwise to q and k only
+ *   non-causal   y_i = phi(q_i)^T [sum_j phi(k_j) v_j^T] / phi(q_i)^T [sum_j phi(k_j)]
+ *   causal       S_t = g S_{t-1} + phi(k_t) v_t^T,  z_t = g z_{t-1} + phi(k_t),
+ *                y_t = phi(q_t)^T S_t / phi(q_t)^T z_t      (update, then read)
+ *
+ * with an optional per-head scalar decay g ("Linear Attention: Removing the
+ * Softmax Buys Associativity", the forget-gate passage; Part 5, section 4
+ * recurrent form), g = 1 when no decay is given.  There is no 1/sqrt(d)
+ * scaling and no epsilon in the denominator (phi > 0 makes it positive).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never frees or retains them after the call is enqueued.
+ *   - Sequences are row-major contiguous [B][H][N][d] (d fastest); decode
+ *     inputs are [B][H][d]; states S are [B][H][d][d] with S[a][c],
+ *     a = key-feature index, c = value index; normalisers z are [B][H][d].
+ *   - q, k, v and out share one dtype (`dtype`); outputs are rounded to it
+ *     with round-to-nearest-even.  Accumulation is always fp32.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and performs no implicit synchronisation.
+ *     Arguments are validated on the host before anything is enqueued; a
+ *     rejected call enqueues nothing.
+ *   - Calls are thread-safe.  The library's only global mutable state is a
+ *     per-device status word written by kernels that detect a device-side
+ *     problem (a bounded wait that ran out); read it with
+ *     la_check_device_status().
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t, so that a cudaStream_t (or
+ * torch.cuda.Stream.cuda_stream) can be passed directly. */
+typedef struct CUstream_st *la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad decay, ...      */
+    LA_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run          */
+    LA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed         */
+    LA_ERR_NO_MEMORY = 4,    /* workspace allocation failed                  */
+    LA_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up           */
+} la_status;
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+/* Largest head dimension accepted by any entry point. */
+#define LA_MAX_D 256
+/* Largest number of heads for which a per-head decay can be given. */
+#define LA_MAX_DECAY_HEADS 1024
+
+/*
+ * la_forward -- full-sequence linear attention.
+ *
+ * Defined by the non-causal form phi(Q)[phi(K)^T V] / phi(Q)[phi(K)^T 1]
+ * ("Story of Attention - Part 5", section 1a, matrix form) when causal == 0,
+ * and by the causal running-state recurrence (same section, causal form;
+ * "Linear Attention", cumulative running statistics) when causal == 1.
+ *
+ *   q, k, v  [B][H][N][d] device, dtype `dtype`, read only.
+ *   out      [B][H][N][d] device, dtype `dtype`, written; may not alias
+ *            q, k or v.
+ *   B, H, N  >= 0 (B*H*N == 0 is a no-op returning LA_OK); d in 1..LA_MAX_D.
+ *   causal   0 or 1.
+ *   decay    HOST array of H floats g_h in [0, 1] (read during the call, not
+ *            retained), or NULL for g = 1.  Only valid with causal == 1:
+ *            the pages define decay for the recurrence only, so a decay with
+ *            causal == 0 is LA_ERR_INVALID_ARG.
+ *   dtype    LA_F32 or LA_BF16.  fp32 inputs run on the fp32 CUDA-core path
+ *            (no TF32); bf16 inputs with d in {64, 128} run on the tcgen05
+ *            tensor-core kernels, other d on the CUDA-core path.
+ *
+ * Workspace: the tensor-core kernels need a small stream-ordered scratch
+ * (per-segment states and flags), allocated with cudaMallocAsync on `stream`
+ * and freed with cudaFreeAsync on the same stream; LA_ERR_NO_MEMORY if that
+ * fails.
+ */
+la_status la_forward(const void *q, const void *k, const void *v, void *out,
+                     int B, int H, int N, int d, int causal,
+                     const float *decay, la_dtype dtype, la_stream_t stream);
+
+/*
+ * la_forward_ex -- la_forward with explicit kernel selection, for tests and
+ * measurement.  `path`: 0 = automatic (what la_forward does), 1 = force the
+ * fp32 CUDA-core kernels (any dtype), 2 = force the tensor-core kernels
+ * (LA_ERR_UNSUPPORTED where they do not apply).  `segment_chunks`: 0 =
+ * automatic, else the number of chunks per sequence segment that the
+ * tensor-core kernels hand to one CTA (sequence parallelism inside a head).
+ */
+la_status la_forward_ex(const void *q, const void *k, const void *v,
+                        void *out, int B, int H, int N, int d, int causal,
+                        const float *decay, la_dtype dtype, int path,
+                        int segment_chunks, la_stream_t stream);
+
+/*
+ * la_decode_step -- one recurrent decode step per head: with
+ * phi_k = phi(k), S <- S + phi_k v^T, z <- z + phi_k, then
+ * out = phi(q)^T S / phi(q)^T z  (update, then read; "Linear Attention",
+ * running statistics and per-token inference cost O(d^2) arithmetic and
+ * O(d^2) memory, independent of history).
+ *
+ *   S        [B][H][d][d] fp32 device, read and written in place.
+ *   z        [B][H][d]    fp32 device, read and written in place.
+ *   q, k, v  [B][H][d] device, dtype `dtype`, read only.
+ *   out      [B][H][d] device, dtype `dtype`, written.
+ *   B, H >= 0 (B*H == 0 is a no-op), d in 1..LA_MAX_D.
+ * The caller owns the recurrent state; saving and restoring S and z is how
+ * a decode is checkpointed and resumed.
+ */
+la_status la_decode_step(float *S, float *z, const void *q, const void *k,
+                         const void *v, void *out, int B, int H, int d,
+                         la_dtype dtype, la_stream_t stream);
+
+/*
+ * la_check_device_status -- synchronises `stream`, then reads and clears the
+ * current device's status word.  Returns LA_ERR_TIMEOUT if a kernel gave up
+ * on a bounded wait since the last check (its outputs are then not valid),
+ * LA_ERR_CUDA if the synchronisation itself failed, else LA_OK.
+ */
+la_status la_check_device_status(la_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *la_status_string(la_status s);
+
+/* Detail of the last failed call on the calling thread ("" if none). */
+const char *la_last_error(void);
+
+/* ABI version of this header: 1. */
+int la_abi_version(void);
+
+/* Number of kernels this library has enqueued in this process (all devices,
+ * all streams) since it was loaded; for measurement and launch accounting. */
+unsigned long long la_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LINATTN_H */

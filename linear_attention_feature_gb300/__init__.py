@@ -1,0 +1,180 @@
+"""GB300-native kernelised (elu+1) linear attention.
+
+Thin Python binding over the C ABI of ``liblinattn.so`` (declared in
+``include/linattn.h``): argument marshalling only.  Every step of the
+computation runs in the library's CUDA kernels; PyTorch is used for device
+memory and streams.  There is no CPU fallback: if the library has not been
+built (``python -m linear_attention_feature_gb300.build``) or a tensor is not
+on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = ["forward", "decode_step", "check_device_status",
+           "kernel_launch_count", "LinAttnError",
+           "load_library", "LA_F32", "LA_BF16", "STATUS", "EXPORTED"]
+
+LA_F32 = 0
+LA_BF16 = 1
+STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED",
+          3: "LA_ERR_CUDA", 4: "LA_ERR_NO_MEMORY", 5: "LA_ERR_TIMEOUT"}
+EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
+            "la_check_device_status", "la_status_string", "la_last_error",
+            "la_abi_version", "la_kernel_launch_count")
+
+_lib = None
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load liblinattn.so (built in-tree).  Raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build the CUDA library first "
+            "(python -m linear_attention_feature_gb300.build)")
+    lib = ctypes.CDLL(p)
+    V, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_float)
+    lib.la_forward.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V]
+    lib.la_forward_ex.argtypes = [V, V, V, V, I, I, I, I, I, F, I, I, I, V]
+    lib.la_decode_step.argtypes = [V, V, V, V, V, V, I, I, I, I, V]
+    lib.la_check_device_status.argtypes = [V]
+    lib.la_status_string.argtypes = [I]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_last_error.argtypes = []
+    lib.la_last_error.restype = ctypes.c_char_p
+    lib.la_abi_version.argtypes = []
+    lib.la_kernel_launch_count.argtypes = []
+    lib.la_kernel_launch_count.restype = ctypes.c_ulonglong
+    for n in ("la_forward", "la_forward_ex", "la_decode_step",
+              "la_check_device_status", "la_abi_version"):
+        getattr(lib, n).restype = I
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _raise_if(status: int):
+    if status != 0:
+        detail = load_library().la_last_error().decode(errors="replace")
+        raise LinAttnError(status, detail)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def _stream_ptr(stream, device):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _decay_arg(decay, H):
+    if decay is None:
+        return None
+    vals = [float(x) for x in (decay.tolist() if hasattr(decay, "tolist") else decay)]
+    if len(vals) != H:
+        raise ValueError(f"decay must have H={H} entries")
+    return (ctypes.c_float * H)(*vals)
+
+
+def forward(q, k, v, causal: bool = True, decay=None, out=None, *,
+            path: int = 0, segment_chunks: int = 0, stream=None):
+    """Linear attention over full sequences; q, k, v [B, H, N, d] on CUDA.
+
+    causal=False: phi(Q)[phi(K)^T V] / phi(Q)[phi(K)^T 1].
+    causal=True : running-state recurrence with optional per-head decay
+    (`decay`: H floats in [0, 1]).  Returns `out` ([B, H, N, d], q's dtype).
+    """
+    torch = _torch()
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda(q, k, v, out)
+    B, H, N, d = q.shape
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_forward_ex(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            B, H, N, d, int(bool(causal)), _decay_arg(decay, H),
+            _dtype_code(q), int(path), int(segment_chunks),
+            _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out
+
+
+def decode_step(S, z, q, k, v, out=None, *, stream=None):
+    """One decode step per head: S, z (fp32, [B, H, d, d] / [B, H, d]) are
+    updated in place; q, k, v [B, H, d]; returns out [B, H, d]."""
+    torch = _torch()
+    if q.dim() != 3 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, d] shape")
+    B, H, d = q.shape
+    if tuple(S.shape) != (B, H, d, d) or tuple(z.shape) != (B, H, d):
+        raise ValueError("S must be [B, H, d, d] and z [B, H, d]")
+    if S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("S and z must be float32")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda(S, z, q, k, v, out)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_decode_step(
+            ctypes.c_void_p(S.data_ptr()), ctypes.c_void_p(z.data_ptr()),
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            B, H, d, _dtype_code(q), _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out
+
+
+def kernel_launch_count() -> int:
+    """Kernels enqueued by the library in this process so far."""
+    return int(load_library().la_kernel_launch_count())
+
+
+def check_device_status(stream=None, device=None):
+    """Synchronise the stream and raise if a kernel reported a device-side
+    failure (a bounded wait that ran out)."""
+    torch = _torch()
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        st = load_library().la_check_device_status(_stream_ptr(stream, dev))
+    _raise_if(st)

@@ -1,0 +1,219 @@
+// C ABI of liblinattn.so: argument validation, kernel selection and launch.
+// The declarations and their contracts are in include/linattn.h.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "la_internal.h"
+#include "la_tc.h"
+
+namespace la {
+
+// Per-device status word.  A kernel that gives up on a bounded wait stores a
+// non-zero la_status here; la_check_device_status reads and clears it.
+__device__ int g_status_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_status_ptr[kMaxDevices] = {};
+thread_local char g_last_error[512] = "";
+std::atomic<unsigned long long> g_launches{0};
+
+la_status fail(la_status s, const char *msg) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+    return s;
+}
+
+la_status cuda_fail(cudaError_t e, const char *where) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where,
+                  cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+}
+
+bool valid_dtype(la_dtype t) { return t == LA_F32 || t == LA_BF16; }
+}  // namespace
+
+int *device_status_word(cudaError_t *err) {
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_status_word);
+        if (*err != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
+
+}  // namespace la
+
+using namespace la;
+
+namespace {
+
+la_status validate_forward(const void *q, const void *k, const void *v,
+                           const void *out, int B, int H, int N, int d,
+                           int causal, const float *decay, la_dtype dtype,
+                           DecayArgs *dk) {
+    if (!q || !k || !v || !out)
+        return fail(LA_ERR_INVALID_ARG, "la_forward: null tensor pointer");
+    if (B < 0 || H < 0 || N < 0)
+        return fail(LA_ERR_INVALID_ARG, "la_forward: negative B, H or N");
+    if (d < 1 || d > LA_MAX_D)
+        return fail(LA_ERR_INVALID_ARG, "la_forward: d must be in 1..256");
+    if (causal != 0 && causal != 1)
+        return fail(LA_ERR_INVALID_ARG, "la_forward: causal must be 0 or 1");
+    if (!valid_dtype(dtype))
+        return fail(LA_ERR_INVALID_ARG, "la_forward: unknown dtype");
+    if (out == q || out == k || out == v)
+        return fail(LA_ERR_INVALID_ARG, "la_forward: out aliases an input");
+    dk->has = 0;
+    dk->H = H > 0 ? H : 1;
+    if (decay) {
+        if (!causal)
+            return fail(LA_ERR_INVALID_ARG,
+                        "la_forward: decay is defined for the causal form only");
+        if (H > LA_MAX_DECAY_HEADS)
+            return fail(LA_ERR_UNSUPPORTED,
+                        "la_forward: decay given for more than 1024 heads");
+        for (int h = 0; h < H; ++h) {
+            float g = decay[h];
+            if (!(g >= 0.f && g <= 1.f))  // also rejects NaN
+                return fail(LA_ERR_INVALID_ARG,
+                            "la_forward: decay values must lie in [0, 1]");
+            dk->g[h] = g;
+        }
+        dk->has = 1;
+    }
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+__attribute__((visibility("default")))
+la_status la_forward_ex(const void *q, const void *k, const void *v,
+                        void *out, int B, int H, int N, int d, int causal,
+                        const float *decay, la_dtype dtype, int path,
+                        int segment_chunks, la_stream_t stream) {
+    DecayArgs dk;
+    la_status st = validate_forward(q, k, v, out, B, H, N, d, causal, decay,
+                                    dtype, &dk);
+    if (st != LA_OK) return st;
+    if (path < 0 || path > 2)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_ex: path must be 0, 1 or 2");
+    if (segment_chunks < 0)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_ex: segment_chunks < 0");
+    FwdShape sh{B, H, N, d};
+    if (sh.BH() == 0 || N == 0) return LA_OK;
+    if (sh.BH() > 2147483647LL || (long long)N * d > (1LL << 40))
+        return fail(LA_ERR_UNSUPPORTED, "la_forward: problem too large");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    const bool tc_ok = tc_supported(sh, dtype);
+    if (path == 2 && !tc_ok)
+        return fail(LA_ERR_UNSUPPORTED,
+                    "la_forward_ex: tensor-core path needs bf16 and d in {64,128}");
+    if (tc_ok && path != 1) {
+        cudaError_t ce;
+        int *status = device_status_word(&ce);
+        if (!status) return cuda_fail(ce, "la_forward: status word");
+        TcResult r = tc_forward(q, k, v, out, sh, causal, dk, segment_chunks,
+                                status, s);
+        if (r.status != LA_OK) {
+            if (r.status == LA_ERR_CUDA) return cuda_fail(r.cuda, r.where);
+            return fail(r.status, r.where);
+        }
+        return LA_OK;
+    }
+    cudaError_t e = launch_simt_forward(q, k, v, out, sh, causal, dk, dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward (CUDA-core kernel)");
+    note_launches(1);
+    return LA_OK;
+}
+
+__attribute__((visibility("default")))
+la_status la_forward(const void *q, const void *k, const void *v, void *out,
+                     int B, int H, int N, int d, int causal,
+                     const float *decay, la_dtype dtype, la_stream_t stream) {
+    return la_forward_ex(q, k, v, out, B, H, N, d, causal, decay, dtype, 0, 0,
+                         stream);
+}
+
+__attribute__((visibility("default")))
+la_status la_decode_step(float *S, float *z, const void *q, const void *k,
+                         const void *v, void *out, int B, int H, int d,
+                         la_dtype dtype, la_stream_t stream) {
+    if (!S || !z || !q || !k || !v || !out)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step: null pointer");
+    if (B < 0 || H < 0)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step: negative B or H");
+    if (d < 1 || d > LA_MAX_D)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step: d must be in 1..256");
+    if (!valid_dtype(dtype))
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step: unknown dtype");
+    long long BH = (long long)B * H;
+    if (BH == 0) return LA_OK;
+    if (BH > 2147483647LL)
+        return fail(LA_ERR_UNSUPPORTED, "la_decode_step: too many heads");
+    cudaError_t e = launch_decode_step(S, z, q, k, v, out, BH, d, dtype,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
+    note_launches(1);
+    return LA_OK;
+}
+
+__attribute__((visibility("default")))
+la_status la_check_device_status(la_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status: sync");
+    int *p = device_status_word(&e);
+    if (!p) return cuda_fail(e, "la_check_device_status: status word");
+    int word = 0;
+    e = cudaMemcpy(&word, p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status: read");
+    if (word != 0) {
+        int zero = 0;
+        e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status: clear");
+        return fail(static_cast<la_status>(word),
+                    "a kernel reported a device-side failure");
+    }
+    return LA_OK;
+}
+
+__attribute__((visibility("default")))
+const char *la_status_string(la_status s) {
+    switch (s) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA";
+        case LA_ERR_NO_MEMORY: return "LA_ERR_NO_MEMORY";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+    }
+    return "LA_ERR_UNKNOWN";
+}
+
+__attribute__((visibility("default")))
+const char *la_last_error(void) { return g_last_error; }
+
+__attribute__((visibility("default")))
+int la_abi_version(void) { return 1; }
+
+__attribute__((visibility("default")))
+unsigned long long la_kernel_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// Recurrent decode step: S <- S + phi(k) v^T, z <- z + phi(k),
+// out = phi(q)^T S / phi(q)^T z  ("Linear Attention", running statistics and
+// the O(d^2)-per-token inference cost).
+//
+// The step is a pure stream over the fp32 d x d state (read once, written
+// once): 2 * 4 * d^2 bytes per head against ~4 d^2 flops, so it is bound by
+// HBM bandwidth.  One CTA owns one head.  In the vector kernel a thread owns
+// 4 adjacent value columns c (one 128-bit load per state row) for a fixed
+// subset of key-feature rows a; a warp therefore reads whole 512-byte rows
+// (d = 128) perfectly coalesced.  All of a thread's rows are loaded before
+// any is used so that its loads are in flight together.  The per-column
+// partial sums of phi(q)^T S are reduced across row groups through shared
+// memory; the denominator phi(q)^T z is reduced with warp shuffles.
+#include <cuda_bf16.h>
+
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float ld_in(const float *p) { return *p; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+}
+__device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) {
+    *p = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ float phi(float x) {
+    return x > 0.f ? x + 1.f : expf(x);
+}
+
+// Shared prologue: phi(k), phi(q) into shared memory; z <- z + phi(k) and
+// den = phi(q)^T z (after the update) reduced into *sden.
+template <typename T>
+__device__ __forceinline__ void decode_prologue(float *__restrict__ zh,
+                                                const T *__restrict__ qh,
+                                                const T *__restrict__ kh,
+                                                int d, float *sk, float *sq,
+                                                float *swarp, float *sden) {
+    const int tid = threadIdx.x;
+    float part = 0.f;
+    for (int a = tid; a < d; a += kThreads) {
+        float pk = phi(ld_in(kh + a));
+        float pq = phi(ld_in(qh + a));
+        sk[a] = pk;
+        sq[a] = pq;
+        float zn = zh[a] + pk;
+        zh[a] = zn;
+        part = fmaf(pq, zn, part);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if ((tid & 31) == 0) swarp[tid >> 5] = part;
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) s += swarp[w];
+        *sden = s;
+    }
+}
+
+// d == D, D % 4 == 0, S 16-byte aligned.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads)
+decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
+                  const T *__restrict__ q, const T *__restrict__ k,
+                  const T *__restrict__ v, T *__restrict__ out) {
+    constexpr int NCG = D / 4;                 // column groups (float4 each)
+    constexpr int NRG = kThreads / NCG;        // row groups
+    constexpr int RPT = D / NRG;               // rows per thread
+    constexpr int BATCH = RPT < 16 ? RPT : 16; // loads in flight per thread
+    static_assert(NCG <= kThreads && kThreads % NCG == 0, "bad D");
+    static_assert(D % NRG == 0 && RPT % BATCH == 0, "bad D");
+    __shared__ float sk[D], sq[D];
+    __shared__ float4 red[NRG][NCG];
+    __shared__ float swarp[kThreads / 32], sden;
+
+    const long long bh = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int cg = tid % NCG, rg = tid / NCG;
+    float4 *__restrict__ Sh = reinterpret_cast<float4 *>(S + (size_t)bh * D * D);
+    decode_prologue<T>(z + (size_t)bh * D, q + (size_t)bh * D,
+                       k + (size_t)bh * D, D, sk, sq, swarp, &sden);
+    const T *vh = v + (size_t)bh * D + 4 * cg;
+    const float v0 = ld_in(vh), v1 = ld_in(vh + 1), v2 = ld_in(vh + 2),
+                v3 = ld_in(vh + 3);
+    __syncthreads();
+
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r0 = 0; r0 < RPT; r0 += BATCH) {
+        float4 s[BATCH];
+#pragma unroll
+        for (int r = 0; r < BATCH; ++r)
+            s[r] = __ldcs(Sh + (size_t)(rg + (r0 + r) * NRG) * NCG + cg);
+#pragma unroll
+        for (int r = 0; r < BATCH; ++r) {
+            const int a = rg + (r0 + r) * NRG;
+            const float pk = sk[a], pq = sq[a];
+            s[r].x = fmaf(pk, v0, s[r].x);
+            s[r].y = fmaf(pk, v1, s[r].y);
+            s[r].z = fmaf(pk, v2, s[r].z);
+            s[r].w = fmaf(pk, v3, s[r].w);
+            __stcs(Sh + (size_t)a * NCG + cg, s[r]);
+            acc.x = fmaf(pq, s[r].x, acc.x);
+            acc.y = fmaf(pq, s[r].y, acc.y);
+            acc.z = fmaf(pq, s[r].z, acc.z);
+            acc.w = fmaf(pq, s[r].w, acc.w);
+        }
+    }
+    red[rg][cg] = acc;
+    __syncthreads();
+    if (tid < NCG) {
+        float4 t = red[0][tid];
+#pragma unroll
+        for (int r = 1; r < NRG; ++r) {
+            float4 u = red[r][tid];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        const float inv = 1.f / sden;
+        T *o = out + (size_t)bh * D + 4 * tid;
+        st_out(o, t.x * inv);
+        st_out(o + 1, t.y * inv);
+        st_out(o + 2, t.z * inv);
+        st_out(o + 3, t.w * inv);
+    }
+}
+
+// Any d (1..LA_MAX_D) and any alignment: a thread per value column, rows in
+// sequence (each row read coalesced across the CTA).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+decode_generic_kernel(float *__restrict__ S, float *__restrict__ z,
+                      const T *__restrict__ q, const T *__restrict__ k,
+                      const T *__restrict__ v, T *__restrict__ out, int d) {
+    __shared__ float sk[LA_MAX_D], sq[LA_MAX_D];
+    __shared__ float swarp[kThreads / 32], sden;
+    const long long bh = blockIdx.x;
+    float *Sh = S + (size_t)bh * d * d;
+    decode_prologue<T>(z + (size_t)bh * d, q + (size_t)bh * d,
+                       k + (size_t)bh * d, d, sk, sq, swarp, &sden);
+    __syncthreads();
+    for (int c = threadIdx.x; c < d; c += kThreads) {
+        const float vc = ld_in(v + (size_t)bh * d + c);
+        float acc = 0.f;
+        for (int a = 0; a < d; ++a) {
+            float s = fmaf(sk[a], vc, Sh[(size_t)a * d + c]);
+            Sh[(size_t)a * d + c] = s;
+            acc = fmaf(sq[a], s, acc);
+        }
+        st_out(out + (size_t)bh * d + c, acc / sden);
+    }
+}
+
+template <typename T>
+cudaError_t launch_t(float *S, float *z, const void *q, const void *k,
+                     const void *v, void *out, long long BH, int d,
+                     cudaStream_t stream) {
+    const T *qq = static_cast<const T *>(q), *kk = static_cast<const T *>(k),
+            *vv = static_cast<const T *>(v);
+    T *oo = static_cast<T *>(out);
+    const bool aligned = (reinterpret_cast<uintptr_t>(S) & 15u) == 0;
+    dim3 grid((unsigned)BH);
+    if (aligned && d == 128)
+        decode_vec_kernel<T, 128><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo);
+    else if (aligned && d == 64)
+        decode_vec_kernel<T, 64><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo);
+    else if (aligned && d == 256)
+        decode_vec_kernel<T, 256><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo);
+    else
+        decode_generic_kernel<T><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, d);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_step(float *S, float *z, const void *q,
+                               const void *k, const void *v, void *out,
+                               long long BH, int d, la_dtype dtype,
+                               cudaStream_t stream) {
+    if (dtype == LA_F32) return launch_t<float>(S, z, q, k, v, out, BH, d, stream);
+    return launch_t<__nv_bfloat16>(S, z, q, k, v, out, BH, d, stream);
+}
+
+}  // namespace la

@@ -1,0 +1,49 @@
+// Internal declarations shared by the translation units of liblinattn.so.
+// Nothing here is part of the public ABI (include/linattn.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "linattn.h"
+
+namespace la {
+
+// Per-head decay, passed to kernels by value (kernel parameter space).
+// has == 0 means g = 1 for every head.
+struct DecayArgs {
+    int has;
+    int H;
+    float g[LA_MAX_DECAY_HEADS];
+};
+
+__host__ __device__ inline float decay_of(const DecayArgs &dk, int bh) {
+    return dk.has ? dk.g[bh % dk.H] : 1.0f;
+}
+
+// Common shape of a full-sequence call.
+struct FwdShape {
+    int B, H, N, d;
+    long long BH() const { return (long long)B * H; }
+};
+
+// ---- CUDA-core (fp32 FMA) forward: any d in 1..LA_MAX_D, fp32 or bf16 ----
+cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
+                                void *out, const FwdShape &sh, int causal,
+                                const DecayArgs &decay, la_dtype dtype,
+                                cudaStream_t stream);
+
+// ---- recurrent decode step ----
+cudaError_t launch_decode_step(float *S, float *z, const void *q,
+                               const void *k, const void *v, void *out,
+                               long long BH, int d, la_dtype dtype,
+                               cudaStream_t stream);
+
+// Address of the current device's status word (kernels set it to a non-zero
+// la_status when a bounded wait gives up).  Looked up once per device.
+int *device_status_word(cudaError_t *err);
+
+// Counts every kernel enqueued by the library (la_kernel_launch_count).
+void note_launches(int n);
+
+}  // namespace la

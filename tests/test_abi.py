@@ -1,0 +1,130 @@
+"""The C-ABI library builds, loads and exports what include/linattn.h
+declares, and its host-side argument checks reject bad calls before anything
+touches a GPU (these tests need no GPU: every call here returns during
+validation, so no CUDA call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_feature_gb300 as la
+from linear_attention_feature_gb300 import build as labuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "linattn.h")
+
+INVALID, UNSUPPORTED, OK = 1, 2, 0
+
+
+@pytest.fixture(scope="module")
+def lib():
+    labuild.build()
+    return la.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("la_forward", "la_decode_step", "la_check_device_status",
+              "la_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert set(declared_functions()) <= set(la.EXPORTED) | {"la_forward_ex"}
+
+
+def test_status_strings_and_version(lib):
+    for code, name in la.STATUS.items():
+        assert lib.la_status_string(code).decode() == name
+    assert lib.la_status_string(99).decode() == "LA_ERR_UNKNOWN"
+    assert lib.la_abi_version() == 1
+
+
+P = ctypes.c_void_p(0x1000)   # never dereferenced: validation fails first
+P2 = ctypes.c_void_p(0x2000)
+P3 = ctypes.c_void_p(0x3000)
+OUT = ctypes.c_void_p(0x4000)
+
+
+def fwd(lib, q=P, k=P2, v=P3, out=OUT, B=1, H=2, N=8, d=64, causal=1,
+        decay=None, dtype=1, path=0, seg=0):
+    return lib.la_forward_ex(q, k, v, out, B, H, N, d, causal, decay, dtype,
+                             path, seg, None)
+
+
+def floats(*xs):
+    return (ctypes.c_float * len(xs))(*xs)
+
+
+@pytest.mark.parametrize("kw, code, msg", [
+    (dict(q=None), INVALID, "null"),
+    (dict(out=None), INVALID, "null"),
+    (dict(B=-1), INVALID, "negative"),
+    (dict(N=-3), INVALID, "negative"),
+    (dict(d=0), INVALID, "d must"),
+    (dict(d=257), INVALID, "d must"),
+    (dict(causal=2), INVALID, "causal"),
+    (dict(dtype=7), INVALID, "dtype"),
+    (dict(out=P), INVALID, "alias"),
+    (dict(causal=0, decay=floats(0.5, 0.5)), INVALID, "causal form only"),
+    (dict(decay=floats(0.5, 1.5)), INVALID, "[0, 1]"),
+    (dict(decay=floats(float("nan"), 0.5)), INVALID, "[0, 1]"),
+    (dict(decay=floats(-0.1, 0.5)), INVALID, "[0, 1]"),
+    (dict(path=3), INVALID, "path"),
+    (dict(seg=-1), INVALID, "segment_chunks"),
+    (dict(dtype=0, path=2), UNSUPPORTED, "tensor-core"),
+    (dict(d=96, path=2), UNSUPPORTED, "tensor-core"),
+])
+def test_forward_rejects_bad_arguments(lib, kw, code, msg):
+    assert fwd(lib, **kw) == code
+    assert msg in lib.la_last_error().decode()
+
+
+def test_forward_empty_problems_are_noops(lib):
+    # nothing is enqueued, so no GPU is needed
+    assert fwd(lib, B=0) == OK
+    assert fwd(lib, H=0) == OK
+    assert fwd(lib, N=0) == OK
+
+
+def test_forward_rejects_decay_for_too_many_heads(lib):
+    H = 1025
+    dec = (ctypes.c_float * H)(*([0.5] * H))
+    assert fwd(lib, H=H, decay=dec) == UNSUPPORTED
+
+
+def test_decode_rejects_bad_arguments(lib):
+    f = lib.la_decode_step
+    assert f(None, P, P, P, P, OUT, 1, 1, 64, 1, None) == INVALID
+    assert f(P, P, P, P, P, None, 1, 1, 64, 1, None) == INVALID
+    assert f(P, P, P, P, P, OUT, -1, 1, 64, 1, None) == INVALID
+    assert f(P, P, P, P, P, OUT, 1, 1, 0, 1, None) == INVALID
+    assert f(P, P, P, P, P, OUT, 1, 1, 300, 1, None) == INVALID
+    assert f(P, P, P, P, P, OUT, 1, 1, 64, 5, None) == INVALID
+    assert f(P, P, P, P, P, OUT, 0, 4, 64, 1, None) == OK
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        la.forward(q, q.clone(), q.clone())
+    S = torch.zeros(1, 1, 4, 4)
+    z = torch.zeros(1, 1, 4)
+    t = torch.zeros(1, 1, 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        la.decode_step(S, z, t, t.clone(), t.clone())
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        la.load_library(str(tmp_path / "nope.so"))
