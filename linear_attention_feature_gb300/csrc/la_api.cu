@@ -122,10 +122,10 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
         return fail(LA_ERR_UNSUPPORTED, "la_forward: problem too large");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    const bool tc_ok = tc_supported(sh, dtype);
+    const bool tc_ok = tc_supported(sh, dtype, causal, q, k, v, out);
     if (path == 2 && !tc_ok)
         return fail(LA_ERR_UNSUPPORTED,
-                    "la_forward_ex: tensor-core path needs bf16 and d in {64,128}");
+                    "la_forward_ex: tensor-core path needs bf16, d in {64,128} and 16-byte aligned tensors");
     if (tc_ok && path != 1) {
         cudaError_t ce;
         int *status = device_status_word(&ce);

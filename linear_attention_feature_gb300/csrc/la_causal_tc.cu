@@ -1,0 +1,950 @@
+// Chunkwise causal linear attention on tcgen05 tensor cores (bf16 in, fp32
+// accumulate), with optional per-head decay g.
+//
+// The method ("Linear Attention", chunkwise parallel form; "Story of
+// Attention - Part 5", section 6 block formulas, with the normaliser carried
+// like the numerator): the sequence is cut into chunks of C = 128 tokens.
+// For a chunk with local rows i, j (0-based) and S, z the state before it:
+//   P      = phi(Q) phi(K)^T                       (tcgen05, TMEM fp32)
+//   Pt_ij  = P_ij g^(i-j) for j <= i, else 0       (epilogue, rounded bf16)
+//   O      = Pt V + diag(g^(i+1)) phi(Q) S         (tcgen05; Pt read from TMEM)
+//   den_i  = rowsum(Pt_i) + g^(i+1) phi(q_i).z
+//   out_i  = O_i / den_i
+//   S     <- g^n S + Khat^T V,  Khat_t = g^(n-1-t) phi(k_t)   (n = chunk length)
+//   z     <- g^n z + sum_t Khat_t
+// S is carried in TMEM in fp32 and copied to shared memory in bf16 as the B
+// operand of the next chunk's phi(Q) S.
+//
+// Sequence parallelism inside a head: a head's chunks are cut into segments
+// of `seg_chunks` chunks, and the value dimension into halves of 64 columns
+// (d = 128 gives two halves, each with all 128 key features).  A work item
+// is (head, segment, half); persistent CTAs take items from a ticket counter
+// (so a CTA only ever waits on items held by running CTAs).  A segment that
+// has successors first reduces its local decayed state (phase A: phi(K)^T V
+// only) and publishes it; it then looks back over its predecessors' published
+// states (inclusive prefixes end the walk) to get its start state, publishes
+// its own inclusive prefix, and runs the chunk loop (phase B).  The phase-B
+// re-read of K and V normally hits L2 (phase A loads them with evict-last).
+//
+// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-5 feature-map transform (T), warps 6-9 score and output
+// epilogues (E), warps 10-13 state epilogue and look-back (S).  All waits are
+// bounded; a wait that runs out sets the device status word to
+// LA_ERR_TIMEOUT and an abort flag, after which every wait passes through so
+// that the kernel finishes (with invalid output) instead of hanging.
+#include "la_tc.h"
+#include "la_tc_host.h"
+#include "la_tc_ptx.cuh"
+
+namespace la {
+namespace causal_tc {
+
+using namespace la::tc;
+
+constexpr int C = 128;           // chunk length (tokens) = MMA M
+constexpr int DV = 64;           // value columns per work item
+constexpr int kThreads = 448;
+constexpr int kWarpT = 2, kWarpE = 6, kWarpS = 10;
+constexpr int BAR_T = 1, BAR_E = 2, BAR_S = 3;
+constexpr uint32_t TM_P = 0, TM_O = 128, TM_OQS = 192, TM_S = 256;
+constexpr uint32_t TM_COLS = 512;
+constexpr int FLAG_AGG = 1, FLAG_INCL = 2;
+
+struct Params {
+    int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
+    float *agg, *incl;  // [items][DK * DV + DK]: S rows (a-major), then z
+    int *flags;         // [items]
+    int *ctrl;          // [0] ticket counter, [1] abort flag
+    int *status;        // device status word
+    long long timeout;  // clock cycles per bounded wait
+};
+
+template <int DK, bool kDecay>
+struct Layout {
+    static constexpr int KB = DK / 64;
+    static constexpr int STAGES = DK == 128 ? 2 : 3;
+    static constexpr int TILE = DK * C * 2;   // a Q or K tile (bf16)
+    static constexpr int VTILE = C * DV * 2;  // a V (or O) tile half
+    static constexpr int STAGE = 2 * TILE + VTILE;
+    static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 2 * TILE;
+    static constexpr int OFF_SB = STAGES * STAGE;
+    static constexpr int SB = DK * DV * 2;
+    static constexpr int OFF_KHAT = OFF_SB + SB;
+    static constexpr int KHAT = kDecay ? TILE : 0;
+    static constexpr int OFF_SMALL = OFF_KHAT + KHAT;
+    static constexpr int STATE = DK * DV + DK;
+};
+
+struct Small {
+    float zbuf[128];        // T: running z (state before the chunk)
+    float zstart[128];      // S -> T: z at the start of the segment
+    float dzbuf[128];       // T -> S: phase-A local z
+    float colsum[128];      // T scratch
+    float den_inter[3][128];
+    float gtab[128];        // E: g^0 .. g^127 of the current head
+    uint64_t full[3], empty[3], xf[3];
+    uint64_t pfull, pt_ready, o_full, o_empty, pv_done, s_full, sb_ready,
+        zready, dz_ready;
+    uint64_t item_full[2], item_empty[2];
+    int ring[2];
+    uint32_t tmem_base;
+};
+
+struct Ctx {
+    volatile int *abort;
+    int *status;
+    long long timeout;
+};
+
+struct Item {
+    int bh, seg, half, c0, c1;
+    bool hasA;
+};
+
+__device__ __forceinline__ Item decode_item(int t, const Params &p) {
+    Item it;
+    it.half = t % p.nhalf;
+    const int u = t / p.nhalf;
+    it.bh = u % p.BH;
+    it.seg = u / p.BH;
+    it.c0 = it.seg * p.seg_chunks;
+    it.c1 = min(it.c0 + p.seg_chunks, p.nchunks);
+    it.hasA = it.seg < p.nseg - 1;
+    return it;
+}
+
+__device__ __forceinline__ int item_index(int bh, int seg, int half,
+                                          const Params &p) {
+    return (seg * p.BH + bh) * p.nhalf + half;
+}
+
+__device__ __forceinline__ void raise_timeout(const Ctx &cx) {
+    atomicExch(cx.status, (int)LA_ERR_TIMEOUT);
+    *cx.abort = 1;
+}
+
+// Bounded mbarrier wait; passes through (returns false) once aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
+                                         const Ctx &cx) {
+    if (*cx.abort) return false;
+    const long long dl = clock64() + cx.timeout;
+    for (int n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*cx.abort) return false;
+            if (clock64() > dl) {
+                raise_timeout(cx);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded poll of a published-state flag; returns FLAG_AGG or FLAG_INCL
+// (FLAG_INCL with garbage data once aborted, which ends the look-back).
+__device__ __forceinline__ int poll_flag(const int *f, const Ctx &cx) {
+    const long long dl = clock64() + cx.timeout;
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
+                     : "=r"(v)
+                     : "l"(f)
+                     : "memory");
+        if (v >= FLAG_AGG) return v;
+        if (*cx.abort) return FLAG_INCL;
+        if (clock64() > dl) {
+            raise_timeout(cx);
+            return FLAG_INCL;
+        }
+        __nanosleep(100);
+    }
+}
+
+__device__ __forceinline__ void publish_flag(int *f, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v)
+                 : "memory");
+}
+
+// g^k from log2(g) (log2(0) = -inf gives 0 for k > 0); k = 0 gives 1.
+__device__ __forceinline__ float gpow(float lg, int k) {
+    return k == 0 ? 1.f : exp2f(lg * (float)k);
+}
+
+__device__ __forceinline__ float head_log2g(const DecayArgs &dk, int bh) {
+    if (!dk.has) return 0.f;
+    return log2f(dk.g[bh % dk.H]);
+}
+
+// elu(x) + 1 (alpha = 1)
+__device__ __forceinline__ float phi(float x) {
+    return x > 0.f ? x + 1.f : __expf(x);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) {
+    return __uint_as_float(w << 16);
+}
+__device__ __forceinline__ float bf_hi(uint32_t w) {
+    return __uint_as_float(w & 0xFFFF0000u);
+}
+
+// Pop the next item id from the CTA's item ring (every thread of a role
+// calls; `nthreads` threads share the named barrier `bar_id`, or 0 for a
+// single-thread role).
+__device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
+                                        int bar_id, int nthreads, bool leader) {
+    const int r = tl & 1;
+    wait_bar(&sm.item_full[r], (tl >> 1) & 1, cx);
+    const int t = (*cx.abort) ? -1 : ((volatile int *)sm.ring)[r];
+    if (bar_id) named_bar_sync(bar_id, nthreads);
+    if (leader) mbar_arrive(&sm.item_empty[r]);
+    ++tl;
+    return t;
+}
+
+// ---------------------------------------------------------------- producer
+
+template <int DK, bool kDecay>
+__device__ void producer(uint8_t *smem, Small &sm, const Params &p,
+                         const Ctx &cx, const CUtensorMap *tq,
+                         const CUtensorMap *tk, const CUtensorMap *tv) {
+    using L = Layout<DK, kDecay>;
+    const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
+    int j = 0, tl = 0;
+    for (;;) {
+        int t = atomicAdd(p.ctrl, 1);
+        if (t >= p.items || *cx.abort) t = -1;
+        const int r = tl & 1;
+        wait_bar(&sm.item_empty[r], ((tl >> 1) & 1) ^ 1, cx);
+        ((volatile int *)sm.ring)[r] = t;
+        mbar_arrive(&sm.item_full[r]);
+        ++tl;
+        if (t < 0) break;
+        const Item it = decode_item(t, p);
+        for (int pass = it.hasA ? 0 : 1; pass < 2; ++pass) {
+            for (int c = it.c0; c < it.c1; ++c, ++j) {
+                const int st = j % L::STAGES;
+                wait_bar(&sm.empty[st], ((j / L::STAGES) & 1) ^ 1, cx);
+                uint8_t *base = smem + st * L::STAGE;
+                const uint64_t pol = pass == 0 ? keep : stream;
+                mbar_arrive_expect_tx(&sm.full[st], pass == 0
+                                                        ? L::TILE + L::VTILE
+                                                        : 2 * L::TILE + L::VTILE);
+                if (pass == 1)
+                    for (int kb = 0; kb < L::KB; ++kb)
+                        tma_load_3d(base + L::OFF_Q + kb * 16384, tq, &sm.full[st],
+                                    64 * kb, c * C, it.bh, stream);
+                for (int kb = 0; kb < L::KB; ++kb)
+                    tma_load_3d(base + L::OFF_K + kb * 16384, tk, &sm.full[st],
+                                64 * kb, c * C, it.bh, pol);
+                tma_load_3d(base + L::OFF_V, tv, &sm.full[st], 64 * it.half,
+                            c * C, it.bh, pol);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+
+template <int DK, bool kDecay>
+__device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
+                           const Ctx &cx, uint32_t tmem) {
+    using L = Layout<DK, kDecay>;
+    constexpr uint32_t idP = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idPV = idesc_bf16(128, DV, 0, 1);
+    constexpr uint32_t idQS = idesc_bf16(128, DV, 0, 1);
+    constexpr uint32_t idSU = idesc_bf16(128, DV, 1, 1);
+    constexpr uint32_t lboA = DK == 128 ? 16384 : 0;  // d=64: rows 64..127 alias
+    const uint32_t sb = smem_u32(smem + L::OFF_SB);
+    const uint32_t khat = smem_u32(smem + L::OFF_KHAT);
+    int j = 0, nb = 0, nsb = 0, tl = 0;
+    for (;;) {
+        const int t = pop_item(sm, tl, cx, 0, 0, true);
+        if (t < 0) break;
+        const Item it = decode_item(t, p);
+        if (it.hasA) {
+            wait_bar(&sm.sb_ready, nsb & 1, cx);
+            ++nsb;
+            for (int c = it.c0; c < it.c1; ++c, ++j) {
+                const int st = j % L::STAGES;
+                wait_bar(&sm.xf[st], (j / L::STAGES) & 1, cx);
+                tc_fence_after();
+                const uint32_t kb = smem_u32(smem + st * L::STAGE + L::OFF_K);
+                const uint32_t vb = smem_u32(smem + st * L::STAGE + L::OFF_V);
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
+                           sdesc_sw128(vb + ks * 2048, 16384, 1024), idSU,
+                           (c > it.c0 || ks > 0) ? 1u : 0u);
+                if (c == it.c1 - 1) mma_commit(&sm.s_full);
+                mma_commit(&sm.empty[st]);
+            }
+        }
+        for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
+            const int st = j % L::STAGES;
+            wait_bar(&sm.xf[st], (j / L::STAGES) & 1, cx);
+            wait_bar(&sm.pv_done, (nb & 1) ^ 1, cx);
+            tc_fence_after();
+            const uint32_t qb = smem_u32(smem + st * L::STAGE + L::OFF_Q);
+            const uint32_t kb = smem_u32(smem + st * L::STAGE + L::OFF_K);
+            const uint32_t vb = smem_u32(smem + st * L::STAGE + L::OFF_V);
+            // P = phi(Q) phi(K)^T
+            for (int ks = 0; ks < DK / 16; ++ks) {
+                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_ss(tmem + TM_P, sdesc_sw128(qb + off, 16, 1024),
+                       sdesc_sw128(kb + off, 16, 1024), idP, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&sm.pfull);
+            wait_bar(&sm.sb_ready, nsb & 1, cx);
+            ++nsb;
+            wait_bar(&sm.o_empty, (nb & 1) ^ 1, cx);
+            tc_fence_after();
+            // phi(Q) S (into O, or into the separate inter-chunk accumulator
+            // when a decay weight must be applied per row)
+            for (int ks = 0; ks < DK / 16; ++ks) {
+                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_ss(tmem + (kDecay ? TM_OQS : TM_O),
+                       sdesc_sw128(qb + off, 16, 1024),
+                       sdesc_sw128(sb + ks * 2048, 16384, 1024), idQS,
+                       ks > 0 ? 1u : 0u);
+            }
+            // S += Khat^T V
+            const uint32_t ka = kDecay ? khat : kb;
+            for (int ks = 0; ks < C / 16; ++ks)
+                mma_ss(tmem + TM_S, sdesc_sw128(ka + ks * 2048, lboA, 1024),
+                       sdesc_sw128(vb + ks * 2048, 16384, 1024), idSU, 1u);
+            mma_commit(&sm.s_full);
+            wait_bar(&sm.pt_ready, nb & 1, cx);
+            tc_fence_after();
+            // O += Pt V, Pt (bf16) read from TMEM
+            for (int ks = 0; ks < C / 16; ++ks)
+                mma_ts(tmem + TM_O, tmem + TM_P + ks * 8,
+                       sdesc_sw128(vb + ks * 2048, 16384, 1024), idPV,
+                       (kDecay && ks == 0) ? 0u : 1u);
+            mma_commit(&sm.o_full);
+            mma_commit(&sm.pv_done);
+            mma_commit(&sm.empty[st]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- transform
+
+// Sum over the rows of column `col` (bf16) of a [128][DK] swizzled tile,
+// rows [r0, r0 + nr).
+template <int DK>
+__device__ __forceinline__ float column_sum(const uint8_t *tile, int col,
+                                            int r0, int nr) {
+    const uint8_t *blk = tile + (col >> 6) * 16384;
+    const int c = col & 63;
+    float s = 0.f;
+#pragma unroll 8
+    for (int r = r0; r < r0 + nr; ++r) {
+        const uint16_t h = *reinterpret_cast<const uint16_t *>(blk + sw128_offset(r, c));
+        s += __uint_as_float((uint32_t)h << 16);
+    }
+    return s;
+}
+
+// Column sums of a [128][DK] tile into `out` (thread a of 128 owns column a
+// for DK = 128; for DK = 64 two threads split the rows and combine).
+template <int DK>
+__device__ __forceinline__ float tile_colsum(const uint8_t *tile, int et,
+                                             Small &sm) {
+    if (DK == 128) return column_sum<DK>(tile, et, 0, 128);
+    const float part = column_sum<DK>(tile, et & 63, (et >> 6) * 64, 64);
+    sm.colsum[et] = part;
+    named_bar_sync(BAR_T, 128);
+    const float s = (et < 64) ? sm.colsum[et] + sm.colsum[et + 64] : 0.f;
+    return s;
+}
+
+template <int DK, bool kDecay>
+__device__ void transform(uint8_t *smem, Small &sm, const Params &p,
+                          const Ctx &cx, const DecayArgs &dk) {
+    using L = Layout<DK, kDecay>;
+    const int et = threadIdx.x - kWarpT * 32;  // 0..127: row / column owned
+    uint8_t *khat = smem + L::OFF_KHAT;
+    int j = 0, tl = 0, ns = 0, nzr = 0;
+    for (;;) {
+        const int t = pop_item(sm, tl, cx, BAR_T, 128, et == 0);
+        if (t < 0) break;
+        const Item it = decode_item(t, p);
+        const float lg = head_log2g(dk, it.bh);
+        if (it.hasA) {
+            // phase A: Khat_t = g^(L-1-t) phi(k_t), t relative to the segment
+            const int seg_end = min(it.c1 * C, p.N);
+            float dz = 0.f;
+            for (int c = it.c0; c < it.c1; ++c, ++j) {
+                const int st = j % L::STAGES;
+                wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
+                uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
+                const int tok = c * C + et;
+                const float w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
+#pragma unroll
+                for (int kb = 0; kb < L::KB; ++kb)
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint4 *ptr = reinterpret_cast<uint4 *>(
+                            kt + kb * 16384 + sw128_offset(et, ch * 8));
+                        uint4 x = *ptr;
+                        uint32_t *xw = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            xw[e] = pack_bf16x2(w * phi(bf_lo(xw[e])),
+                                                w * phi(bf_hi(xw[e])));
+                        *ptr = x;
+                    }
+                fence_async_shared();
+                named_bar_sync(BAR_T, 128);
+                if (et == 0) mbar_arrive(&sm.xf[st]);
+                dz += tile_colsum<DK>(kt, et, sm);
+                named_bar_sync(BAR_T, 128);
+                if (et == 0) mbar_arrive(&sm.empty[st]);
+            }
+            if (et < DK) sm.dzbuf[et] = dz;
+            named_bar_sync(BAR_T, 128);
+            if (et == 0) mbar_arrive(&sm.dz_ready);
+            ++ns;
+        }
+        // phase B: start state from the look-back
+        wait_bar(&sm.zready, nzr & 1, cx);
+        ++nzr;
+        if (et < DK) sm.zbuf[et] = sm.zstart[et];
+        named_bar_sync(BAR_T, 128);
+        for (int c = it.c0; c < it.c1; ++c, ++j) {
+            const int st = j % L::STAGES;
+            wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
+            uint8_t *qt = smem + st * L::STAGE + L::OFF_Q;
+            uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
+            const int n = min(C, p.N - c * C);
+            // phi(Q) in place; den_inter_i = g^(i+1) phi(q_i) . z
+            float dot = 0.f;
+#pragma unroll
+            for (int kb = 0; kb < L::KB; ++kb)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 *ptr = reinterpret_cast<uint4 *>(
+                        qt + kb * 16384 + sw128_offset(et, ch * 8));
+                    uint4 x = *ptr;
+                    uint32_t *xw = reinterpret_cast<uint32_t *>(&x);
+                    const float *zz = sm.zbuf + kb * 64 + ch * 8;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        xw[e] = pack_bf16x2(phi(bf_lo(xw[e])), phi(bf_hi(xw[e])));
+                        dot = fmaf(bf_lo(xw[e]), zz[2 * e], dot);
+                        dot = fmaf(bf_hi(xw[e]), zz[2 * e + 1], dot);
+                    }
+                    *ptr = x;
+                }
+            sm.den_inter[st][et] = kDecay ? gpow(lg, et + 1) * dot : dot;
+            // phi(K) in place (rows past the sequence end masked to 0);
+            // with decay also Khat = g^(n-1-t) phi(K) for the state update
+            const bool valid = et < n;
+            float w = 1.f;
+            if (kDecay) {
+                if (ns > 0) wait_bar(&sm.s_full, (ns - 1) & 1, cx);
+                w = valid ? gpow(lg, n - 1 - et) : 0.f;
+            }
+#pragma unroll
+            for (int kb = 0; kb < L::KB; ++kb)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t off = kb * 16384 + sw128_offset(et, ch * 8);
+                    uint4 *ptr = reinterpret_cast<uint4 *>(kt + off);
+                    uint4 x = *ptr, xh;
+                    uint32_t *xw = reinterpret_cast<uint32_t *>(&x);
+                    uint32_t *hw = reinterpret_cast<uint32_t *>(&xh);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a0 = valid ? phi(bf_lo(xw[e])) : 0.f;
+                        const float a1 = valid ? phi(bf_hi(xw[e])) : 0.f;
+                        xw[e] = pack_bf16x2(a0, a1);
+                        if (kDecay) hw[e] = pack_bf16x2(w * a0, w * a1);
+                    }
+                    *ptr = x;
+                    if (kDecay) *reinterpret_cast<uint4 *>(khat + off) = xh;
+                }
+            fence_async_shared();
+            named_bar_sync(BAR_T, 128);
+            if (et == 0) mbar_arrive(&sm.xf[st]);
+            // z <- g^n z + sum_t Khat_t
+            const float cs = tile_colsum<DK>(kDecay ? khat : kt, et, sm);
+            named_bar_sync(BAR_T, 128);
+            if (et == 0) mbar_arrive(&sm.empty[st]);
+            if (et < DK) sm.zbuf[et] = gpow(lg, n) * sm.zbuf[et] + cs;
+            named_bar_sync(BAR_T, 128);
+            ++ns;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- epilogue E
+
+template <int DK, bool kDecay>
+__device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
+                         const Ctx &cx, const DecayArgs &dk, uint32_t tmem,
+                         const CUtensorMap *to) {
+    using L = Layout<DK, kDecay>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int et = threadIdx.x - kWarpE * 32;
+    const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);
+    int j = 0, nb = 0, tl = 0;
+    for (;;) {
+        const int t = pop_item(sm, tl, cx, BAR_E, 128, et == 0);
+        if (t < 0) break;
+        const Item it = decode_item(t, p);
+        const float lg = head_log2g(dk, it.bh);
+        if (kDecay) {
+            sm.gtab[et] = gpow(lg, et);
+            named_bar_sync(BAR_E, 128);
+        }
+        const float wq = kDecay ? gpow(lg, row + 1) : 1.f;
+        if (it.hasA)
+            for (int c = it.c0; c < it.c1; ++c, ++j) {
+                const int st = j % L::STAGES;
+                wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
+                if (et == 0) mbar_arrive(&sm.empty[st]);
+            }
+        for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
+            const int st = j % L::STAGES;
+            // ---- scores: mask, decay, bf16 into TMEM (in place), row sums
+            wait_bar(&sm.pfull, nb & 1, cx);
+            tc_fence_after();
+            float rowsum = 0.f;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                uint32_t pk[16];
+                if (b > q) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                } else {
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_P + 32 * b, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int j0 = 32 * b + e;
+                        float x0 = __uint_as_float(v[e]);
+                        float x1 = __uint_as_float(v[e + 1]);
+                        if (kDecay) {
+                            x0 = j0 <= row ? x0 * sm.gtab[row - j0] : 0.f;
+                            x1 = j0 + 1 <= row ? x1 * sm.gtab[row - j0 - 1] : 0.f;
+                        } else if (b == q) {
+                            x0 = j0 <= row ? x0 : 0.f;
+                            x1 = j0 + 1 <= row ? x1 : 0.f;
+                        }
+                        const uint32_t w2 = pack_bf16x2(x0, x1);
+                        rowsum += bf_lo(w2) + bf_hi(w2);
+                        pk[e >> 1] = w2;
+                    }
+                }
+                tmem_st16(lb + TM_P + 16 * b, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_sync(BAR_E, 128);
+            if (et == 0) mbar_arrive(&sm.pt_ready);
+
+            // ---- output: (O + g^(i+1) O_inter) / den
+            wait_bar(&sm.o_full, nb & 1, cx);
+            tc_fence_after();
+            uint32_t o0[32], o1[32];
+            tmem_ld32(lb + TM_O, o0);
+            tmem_ld32(lb + TM_O + 32, o1);
+            tmem_wait_ld();
+            float y[64];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                y[e] = __uint_as_float(o0[e]);
+                y[32 + e] = __uint_as_float(o1[e]);
+            }
+            if (kDecay) {
+                tmem_ld32(lb + TM_OQS, o0);
+                tmem_ld32(lb + TM_OQS + 32, o1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    y[e] = fmaf(wq, __uint_as_float(o0[e]), y[e]);
+                    y[32 + e] = fmaf(wq, __uint_as_float(o1[e]), y[32 + e]);
+                }
+            }
+            tc_fence_before();
+            named_bar_sync(BAR_E, 128);
+            if (et == 0) mbar_arrive(&sm.o_empty);
+            const float inv = 1.f / (rowsum + sm.den_inter[st][row]);
+            uint8_t *stage_o = smem + st * L::STAGE + L::OFF_Q;  // phi(Q) is dead
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint4 v;
+                v.x = pack_bf16x2(y[8 * ch + 0] * inv, y[8 * ch + 1] * inv);
+                v.y = pack_bf16x2(y[8 * ch + 2] * inv, y[8 * ch + 3] * inv);
+                v.z = pack_bf16x2(y[8 * ch + 4] * inv, y[8 * ch + 5] * inv);
+                v.w = pack_bf16x2(y[8 * ch + 6] * inv, y[8 * ch + 7] * inv);
+                *reinterpret_cast<uint4 *>(stage_o + sw128_offset(row, ch * 8)) = v;
+            }
+            fence_async_shared();
+            named_bar_sync(BAR_E, 128);
+            if (et == 0) {
+                tma_store_3d(to, stage_o, 64 * it.half, c * C, it.bh);
+                tma_store_commit();
+                tma_store_wait_read<0>();
+                mbar_arrive(&sm.empty[st]);
+            }
+        }
+    }
+    if (et == 0) tma_store_wait_all<0>();
+}
+
+// ---------------------------------------------------------------- state S
+
+template <int DK, bool kDecay>
+__device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
+                           const Ctx &cx, const DecayArgs &dk, uint32_t tmem) {
+    using L = Layout<DK, kDecay>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;
+    const int a = q * 32 + lane;  // key-feature row of S (= TMEM lane)
+    const int et = threadIdx.x - kWarpS * 32;
+    const bool act = a < DK;      // warp-uniform
+    const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);
+    uint8_t *sb = smem + L::OFF_SB;
+    int tl = 0, ns = 0, ndz = 0;
+    bool pending = false;
+    for (;;) {
+        const int t = pop_item(sm, tl, cx, BAR_S, 128, et == 0);
+        if (t < 0) break;
+        const Item it = decode_item(t, p);
+        const float lg = head_log2g(dk, it.bh);
+        const float gL = gpow(lg, p.seg_chunks * C);
+        if (pending) {
+            wait_bar(&sm.s_full, ns & 1, cx);
+            ++ns;
+            pending = false;
+        }
+        tc_fence_after();
+        float *agg = p.agg + (size_t)t * L::STATE;
+        float *incl = p.incl + (size_t)t * L::STATE;
+        if (it.hasA) {
+            // S's TMEM columns are free for this item's phase A
+            tc_fence_before();
+            named_bar_sync(BAR_S, 128);
+            if (et == 0) mbar_arrive(&sm.sb_ready);
+            wait_bar(&sm.s_full, ns & 1, cx);
+            ++ns;
+            wait_bar(&sm.dz_ready, ndz & 1, cx);
+            ++ndz;
+            tc_fence_after();
+            if (act) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lb + TM_S, v0);
+                tmem_ld32(lb + TM_S + 32, v1);
+                tmem_wait_ld();
+                float4 *dst = reinterpret_cast<float4 *>(agg + a * DV);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    dst[e] = make_float4(__uint_as_float(v0[4 * e]), __uint_as_float(v0[4 * e + 1]),
+                                         __uint_as_float(v0[4 * e + 2]), __uint_as_float(v0[4 * e + 3]));
+                    dst[8 + e] = make_float4(__uint_as_float(v1[4 * e]), __uint_as_float(v1[4 * e + 1]),
+                                             __uint_as_float(v1[4 * e + 2]), __uint_as_float(v1[4 * e + 3]));
+                }
+                agg[DK * DV + a] = sm.dzbuf[a];
+            }
+            __threadfence();
+            named_bar_sync(BAR_S, 128);
+            if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
+        }
+        // look-back over the predecessors of this segment
+        float acc[DV];
+#pragma unroll
+        for (int e = 0; e < DV; ++e) acc[e] = 0.f;
+        float accz = 0.f;
+        {
+            float w = 1.f;
+            for (int s2 = it.seg - 1; s2 >= 0; --s2) {
+                const int pi = item_index(it.bh, s2, it.half, p);
+                const int f = poll_flag(p.flags + pi, cx);
+                const float *src = (f == FLAG_INCL ? p.incl : p.agg) + (size_t)pi * L::STATE;
+                if (act) {
+                    const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV);
+#pragma unroll
+                    for (int e = 0; e < DV / 4; ++e) {
+                        const float4 u = __ldcg(s4 + e);
+                        acc[4 * e] = fmaf(w, u.x, acc[4 * e]);
+                        acc[4 * e + 1] = fmaf(w, u.y, acc[4 * e + 1]);
+                        acc[4 * e + 2] = fmaf(w, u.z, acc[4 * e + 2]);
+                        acc[4 * e + 3] = fmaf(w, u.w, acc[4 * e + 3]);
+                    }
+                    accz = fmaf(w, __ldcg(src + DK * DV + a), accz);
+                }
+                if (f == FLAG_INCL) break;
+                w *= gL;
+            }
+        }
+        if (it.hasA) {
+            // inclusive prefix = g^L S_start + local state
+            if (act) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(lb + TM_S, v0);
+                tmem_ld32(lb + TM_S + 32, v1);
+                tmem_wait_ld();
+                float4 *dst = reinterpret_cast<float4 *>(incl + a * DV);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    dst[e] = make_float4(fmaf(gL, acc[4 * e], __uint_as_float(v0[4 * e])),
+                                         fmaf(gL, acc[4 * e + 1], __uint_as_float(v0[4 * e + 1])),
+                                         fmaf(gL, acc[4 * e + 2], __uint_as_float(v0[4 * e + 2])),
+                                         fmaf(gL, acc[4 * e + 3], __uint_as_float(v0[4 * e + 3])));
+                    dst[8 + e] = make_float4(fmaf(gL, acc[32 + 4 * e], __uint_as_float(v1[4 * e])),
+                                             fmaf(gL, acc[32 + 4 * e + 1], __uint_as_float(v1[4 * e + 1])),
+                                             fmaf(gL, acc[32 + 4 * e + 2], __uint_as_float(v1[4 * e + 2])),
+                                             fmaf(gL, acc[32 + 4 * e + 3], __uint_as_float(v1[4 * e + 3])));
+                }
+                incl[DK * DV + a] = fmaf(gL, accz, sm.dzbuf[a]);
+            }
+            __threadfence();
+            named_bar_sync(BAR_S, 128);
+            if (et == 0) publish_flag(p.flags + t, FLAG_INCL);
+        }
+        // phase-B start: TMEM S = g^n0 S_start, bf16 S_start as MMA operand
+        {
+            const int n0 = min(C, p.N - it.c0 * C);
+            const float f0 = gpow(lg, n0);
+            if (act) {
+                uint32_t v[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f0 * acc[32 * h + e]);
+                    tmem_st32(lb + TM_S + 32 * h, v);
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 u;
+                    u.x = pack_bf16x2(acc[8 * ch + 0], acc[8 * ch + 1]);
+                    u.y = pack_bf16x2(acc[8 * ch + 2], acc[8 * ch + 3]);
+                    u.z = pack_bf16x2(acc[8 * ch + 4], acc[8 * ch + 5]);
+                    u.w = pack_bf16x2(acc[8 * ch + 6], acc[8 * ch + 7]);
+                    *reinterpret_cast<uint4 *>(sb + sw128_offset(a, ch * 8)) = u;
+                }
+                sm.zstart[a] = accz;
+                tmem_wait_st();
+            }
+            fence_async_shared();
+            tc_fence_before();
+            named_bar_sync(BAR_S, 128);
+            if (et == 0) {
+                mbar_arrive(&sm.sb_ready);
+                mbar_arrive(&sm.zready);
+            }
+            pending = true;
+        }
+        for (int c = it.c0 + 1; c < it.c1; ++c) {
+            wait_bar(&sm.s_full, ns & 1, cx);
+            ++ns;
+            tc_fence_after();
+            const int n = min(C, p.N - c * C);
+            const float f = gpow(lg, n);
+            if (act) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_S + 32 * h, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(v[8 * ch + 0]), __uint_as_float(v[8 * ch + 1]));
+                        u.y = pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3]));
+                        u.z = pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5]));
+                        u.w = pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7]));
+                        *reinterpret_cast<uint4 *>(sb + sw128_offset(a, 32 * h + ch * 8)) = u;
+                    }
+                    if (kDecay) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f * __uint_as_float(v[e]));
+                        tmem_st32(lb + TM_S + 32 * h, v);
+                    }
+                }
+                if (kDecay) tmem_wait_st();
+            }
+            fence_async_shared();
+            tc_fence_before();
+            named_bar_sync(BAR_S, 128);
+            if (et == 0) mbar_arrive(&sm.sb_ready);
+        }
+    }
+    if (pending) wait_bar(&sm.s_full, ns & 1, cx);
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int DK, bool kDecay>
+__global__ void __launch_bounds__(kThreads, 1)
+causal_kernel(const __grid_constant__ CUtensorMap tq,
+              const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv,
+              const __grid_constant__ CUtensorMap to, const Params p,
+              const DecayArgs dk) {
+    using L = Layout<DK, kDecay>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Small &sm = *reinterpret_cast<Small *>(smem + L::OFF_SMALL);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Ctx cx{reinterpret_cast<volatile int *>(p.ctrl + 1), p.status,
+                 p.timeout};
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::STAGES; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 3);
+            mbar_init(&sm.xf[s], 1);
+        }
+        mbar_init(&sm.pfull, 1);
+        mbar_init(&sm.pt_ready, 1);
+        mbar_init(&sm.o_full, 1);
+        mbar_init(&sm.o_empty, 1);
+        mbar_init(&sm.pv_done, 1);
+        mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.sb_ready, 1);
+        mbar_init(&sm.zready, 1);
+        mbar_init(&sm.dz_ready, 1);
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(&sm.item_full[r], 1);
+            mbar_init(&sm.item_empty[r], 4);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, TM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&to);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) producer<DK, kDecay>(smem, sm, p, cx, &tq, &tk, &tv);
+    } else if (warp == 1) {
+        if (lane == 0) mma_issuer<DK, kDecay>(smem, sm, p, cx, tmem);
+    } else if (warp < kWarpE) {
+        transform<DK, kDecay>(smem, sm, p, cx, dk);
+    } else if (warp < kWarpS) {
+        epilogue<DK, kDecay>(smem, sm, p, cx, dk, tmem, &to);
+    } else {
+        state_role<DK, kDecay>(smem, sm, p, cx, dk, tmem);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TM_COLS);
+}
+
+template <int DK, bool kDecay>
+constexpr size_t smem_bytes() {
+    return (size_t)Layout<DK, kDecay>::OFF_SMALL + sizeof(Small) + 1024;
+}
+
+static_assert(smem_bytes<128, true>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<64, true>() <= 232448, "shared memory budget");
+
+}  // namespace causal_tc
+
+namespace {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <int DK, bool kDecay>
+TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
+                         const FwdShape &sh, const DecayArgs &dk, int seg_chunks,
+                         int *status, cudaStream_t stream) {
+    using namespace causal_tc;
+    using L = Layout<DK, kDecay>;
+    const int BH = (int)sh.BH(), N = sh.N;
+    CUtensorMap tq, tk, tv, to;
+    cudaError_t e;
+    if ((e = tchost::make_seq_map(&tq, q, BH, N, DK, C)) != cudaSuccess ||
+        (e = tchost::make_seq_map(&tk, k, BH, N, DK, C)) != cudaSuccess ||
+        (e = tchost::make_seq_map(&tv, v, BH, N, DK, C)) != cudaSuccess ||
+        (e = tchost::make_seq_map(&to, out, BH, N, DK, C)) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward: TMA descriptor"};
+    int sms = 0;
+    if ((e = tchost::sm_count(&sms)) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward: device query"};
+
+    Params p{};
+    p.BH = BH;
+    p.H = sh.H;
+    p.N = N;
+    p.nchunks = (N + C - 1) / C;
+    p.nhalf = DK / DV;
+    if (seg_chunks <= 0) {
+        // ~3 items per SM, segments of 2..8 chunks (the phase-A loads of K
+        // and V then stay in L2 until phase B re-reads them)
+        long long units = (long long)BH * p.nchunks * p.nhalf;
+        long long want = (units + 3LL * sms - 1) / (3LL * sms);
+        seg_chunks = (int)(want < 2 ? 2 : (want > 8 ? 8 : want));
+    }
+    p.seg_chunks = seg_chunks;
+    p.nseg = (p.nchunks + seg_chunks - 1) / seg_chunks;
+    long long items = (long long)BH * p.nseg * p.nhalf;
+    if (items > (1LL << 30))
+        return {LA_ERR_UNSUPPORTED, cudaSuccess, "la_forward: too many work items"};
+    p.items = (int)items;
+    p.timeout = 1LL << 32;
+
+    // workspace: control words, flags, published states
+    const size_t off_flags = 256;
+    const size_t off_agg = align_up(off_flags + sizeof(int) * items, 256);
+    const size_t state_bytes = (p.nseg > 1) ? sizeof(float) * L::STATE * items : 0;
+    const size_t off_incl = align_up(off_agg + state_bytes, 256);
+    const size_t total = off_incl + state_bytes;
+    void *ws = nullptr;
+    if ((e = cudaMallocAsync(&ws, total, stream)) != cudaSuccess)
+        return {LA_ERR_NO_MEMORY, e, "la_forward: workspace allocation"};
+    char *w8 = static_cast<char *>(ws);
+    p.ctrl = reinterpret_cast<int *>(w8);
+    p.flags = reinterpret_cast<int *>(w8 + off_flags);
+    p.agg = reinterpret_cast<float *>(w8 + off_agg);
+    p.incl = reinterpret_cast<float *>(w8 + off_incl);
+    p.status = status;
+    e = cudaMemsetAsync(ws, 0, off_agg, stream);
+    if (e == cudaSuccess) {
+        const size_t smem = smem_bytes<DK, kDecay>();
+        auto kern = causal_kernel<DK, kDecay>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e == cudaSuccess) {
+            const int grid = (int)(items < sms ? items : sms);
+            kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p, dk);
+            e = cudaGetLastError();
+        }
+    }
+    cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e != cudaSuccess) return {LA_ERR_CUDA, e, "la_forward: causal kernel launch"};
+    if (ef != cudaSuccess) return {LA_ERR_CUDA, ef, "la_forward: workspace free"};
+    note_launches(1);
+    return {LA_OK, cudaSuccess, ""};
+}
+
+}  // namespace
+
+TcResult launch_causal_tc(const void *q, const void *k, const void *v,
+                          void *out, const FwdShape &sh, const DecayArgs &dk,
+                          int seg_chunks, int *status, cudaStream_t stream) {
+    if (sh.d == 128)
+        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, stream)
+                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, stream);
+    return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, stream)
+                  : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, stream);
+}
+
+}  // namespace la
