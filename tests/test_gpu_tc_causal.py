@@ -87,12 +87,17 @@ def test_causal_tc_constant_values(d):
     torch.testing.assert_close(y.float(), v.float(), rtol=2e-2, atol=2e-2)
 
 
-def test_causal_tc_repeated_calls_are_identical():
+def test_causal_tc_repeated_calls_agree_to_rounding():
+    """The look-back adds whichever predecessor states are already published
+    (local aggregates or an inclusive prefix), so the fp32 summation order of
+    a segment's start state depends on timing: repeated calls agree to
+    rounding, not bit for bit."""
     q, k, v = (t.cuda() for t in wl.make_qkv(1, 4, 900, 128, "bf16", seed=3))
     a = la.forward(q, k, v, causal=True, path=2, segment_chunks=2)
-    b = la.forward(q, k, v, causal=True, path=2, segment_chunks=2)
-    la.check_device_status()
-    assert torch.equal(a, b)
+    for _ in range(3):
+        b = la.forward(q, k, v, causal=True, path=2, segment_chunks=2)
+        la.check_device_status()
+        assert wl.max_row_rel_err(b.cpu(), a.cpu()) <= 1e-2
 
 
 def test_auto_path_uses_tensor_cores_for_bf16():
