@@ -122,6 +122,43 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k,
                          const void *v, void *out, int B, int H, int d,
                          la_dtype dtype, la_stream_t stream);
 
+/* Size of the fixed device scratch used by la_forward_causal_noalloc. */
+#define LA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * la_forward_causal_noalloc -- the causal form of la_forward (bf16 only),
+ * for callers that cannot allocate device memory: work recorded into a CUDA
+ * graph whose capture forbids allocation, hosts that reserve all device
+ * memory up front, and plug-in layers that are handed their buffers and may
+ * not own allocations.  The pages have no counterpart of this entry point;
+ * it exists only for such callers.
+ *
+ * Same arguments and meaning as la_forward with causal == 1 and
+ * dtype == LA_BF16: q, k, v, out are caller-owned device tensors
+ * [B][H][N][d] (16-byte aligned), d must be 64 or 128, `decay` is a host
+ * array of H values in [0, 1] or NULL.  It runs the same tensor-core kernel,
+ * but its workspace lives in a static device array of
+ * LA_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads the library's
+ * causal kernels keeps until the process exits.  The call makes no
+ * cudaMalloc/cudaFree or other allocating call; it clears the part of the
+ * scratch that must start at zero with cudaMemsetAsync on `stream`.
+ *   - Sequence segments are lengthened until the workspace fits the
+ *     scratch; if it cannot fit even with one segment per head the call
+ *     returns LA_ERR_UNSUPPORTED ("needs more workspace than ...") and
+ *     enqueues nothing.  Other shapes or dtypes: LA_ERR_UNSUPPORTED.
+ *   - The first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the one scratch array, which keeps the
+ *     last call's contents.  Calls whose kernels can overlap on the GPU
+ *     (different streams without ordering between them, or several host
+ *     threads) race on it and give wrong results: order them.
+ */
+la_status la_forward_causal_noalloc(const void *q, const void *k,
+                                    const void *v, void *out, int B, int H,
+                                    int N, int d, const float *decay,
+                                    la_stream_t stream);
+
 /*
  * la_check_device_status -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns LA_ERR_TIMEOUT if a kernel gave up

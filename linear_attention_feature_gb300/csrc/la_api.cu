@@ -56,6 +56,10 @@ int *device_status_word(cudaError_t *err) {
 
 void note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
+void set_last_error(const char *msg) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 }  // namespace la
 
 using namespace la;

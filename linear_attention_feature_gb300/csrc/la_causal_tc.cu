@@ -36,6 +36,9 @@
 #include "la_tc_host.h"
 #include "la_tc_ptx.cuh"
 
+#include <cstdio>
+#include <mutex>
+
 namespace la {
 namespace causal_tc {
 
@@ -948,3 +951,200 @@ TcResult launch_causal_tc(const void *q, const void *k, const void *v,
 }
 
 }  // namespace la
+
+// ============================================================================
+// Allocation-free variant of the causal tensor-core forward.
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: code recorded into a CUDA graph whose capture mode forbids
+// allocation nodes, hosts that reserve all device memory up front (embedded
+// and real-time deployments, memory-pool-managed servers), and plug-in or
+// interop layers that are handed input and output buffers by a host
+// framework and must not own allocations of their own.  For them
+// la_forward_causal_noalloc runs the same chunkwise causal kernel, but its
+// workspace (ticket counter, segment flags and published segment states)
+// lives in the fixed device array below instead of a cudaMallocAsync block.
+//
+// The array is LA_NOALLOC_SCRATCH_BYTES (16 MiB) and every GPU that loads
+// this library's causal kernels keeps it until the process exits.  Requests
+// are fitted into it by lengthening the sequence segments; a request whose
+// workspace does not fit even with one segment per head is rejected.
+// ============================================================================
+
+static __device__ __align__(256) unsigned char
+    la_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
+
+namespace la {
+namespace {
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {};
+
+// Device address of la_noalloc_scratch on the current device.  The symbol's
+// name is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+cudaError_t noalloc_scratch(char **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, la_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = static_cast<char *>(g_noalloc_ptr[dev]);
+    return cudaSuccess;
+}
+
+template <int DK, bool kDecay>
+TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
+                                 void *out, const FwdShape &sh,
+                                 const DecayArgs &dk, int *status,
+                                 cudaStream_t stream) {
+    using namespace causal_tc;
+    using L = Layout<DK, kDecay>;
+    const int BH = (int)sh.BH(), N = sh.N;
+    CUtensorMap tq, tk, tv, to;
+    cudaError_t e;
+    if ((e = tchost::make_seq_map(&tq, q, BH, N, DK, C)) != cudaSuccess ||
+        (e = tchost::make_seq_map(&tk, k, BH, N, DK, C)) != cudaSuccess ||
+        (e = tchost::make_seq_map(&tv, v, BH, N, DK, C)) != cudaSuccess ||
+        (e = tchost::make_seq_map(&to, out, BH, N, DK, C)) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: TMA descriptor"};
+    int sms = 0;
+    if ((e = tchost::sm_count(&sms)) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: device query"};
+    char *scratch = nullptr;
+    if ((e = noalloc_scratch(&scratch)) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: scratch address"};
+
+    Params p{};
+    p.BH = BH;
+    p.H = sh.H;
+    p.N = N;
+    p.nchunks = (N + C - 1) / C;
+    p.nhalf = DK / DV;
+    long long units = (long long)BH * p.nchunks * p.nhalf;
+    long long want = (units + 3LL * sms - 1) / (3LL * sms);
+    int seg = (int)(want < 2 ? 2 : (want > 8 ? 8 : want));
+    // lengthen segments until the workspace fits the static scratch
+    size_t off_agg = 0, off_incl = 0, total = 0;
+    long long items = 0;
+    for (;;) {
+        const int nseg = (p.nchunks + seg - 1) / seg;
+        items = (long long)BH * nseg * p.nhalf;
+        off_agg = align_up(256 + sizeof(int) * (size_t)items, 256);
+        const size_t sb = nseg > 1 ? sizeof(float) * L::STATE * (size_t)items : 0;
+        off_incl = align_up(off_agg + sb, 256);
+        total = off_incl + sb;
+        if (total <= (size_t)LA_NOALLOC_SCRATCH_BYTES || seg >= p.nchunks) break;
+        seg = seg * 2 < p.nchunks ? seg * 2 : p.nchunks;
+    }
+    if (total > (size_t)LA_NOALLOC_SCRATCH_BYTES || items > (1LL << 30))
+        return {LA_ERR_UNSUPPORTED, cudaSuccess,
+                "la_forward_causal_noalloc: the problem needs more workspace "
+                "than the 16 MiB static scratch holds (too many heads)"};
+    p.seg_chunks = seg;
+    p.nseg = (p.nchunks + seg - 1) / seg;
+    p.items = (int)items;
+    p.timeout = 1LL << 32;
+    p.ctrl = reinterpret_cast<int *>(scratch);
+    p.flags = reinterpret_cast<int *>(scratch + 256);
+    p.agg = reinterpret_cast<float *>(scratch + off_agg);
+    p.incl = reinterpret_cast<float *>(scratch + off_incl);
+    p.status = status;
+    // the counter and flags must start at zero; the states need no clearing
+    if ((e = cudaMemsetAsync(scratch, 0, off_agg, stream)) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: clearing flags"};
+    const size_t smem = smem_bytes<DK, kDecay>();
+    auto kern = causal_kernel<DK, kDecay>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel attribute"};
+    const int grid = (int)(items < sms ? items : sms);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p, dk);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel launch"};
+    note_launches(1);
+    return {LA_OK, cudaSuccess, ""};
+}
+
+la_status noalloc_fail(la_status s, const char *msg) {
+    set_last_error(msg);
+    return s;
+}
+
+}  // namespace
+}  // namespace la
+
+extern "C" __attribute__((visibility("default")))
+la_status la_forward_causal_noalloc(const void *q, const void *k,
+                                    const void *v, void *out, int B, int H,
+                                    int N, int d, const float *decay,
+                                    la_stream_t stream) {
+    using namespace la;
+    if (!q || !k || !v || !out)
+        return noalloc_fail(LA_ERR_INVALID_ARG,
+                            "la_forward_causal_noalloc: null tensor pointer");
+    if (B < 0 || H < 0 || N < 0)
+        return noalloc_fail(LA_ERR_INVALID_ARG,
+                            "la_forward_causal_noalloc: negative B, H or N");
+    if (d != 64 && d != 128)
+        return noalloc_fail(LA_ERR_UNSUPPORTED,
+                            "la_forward_causal_noalloc: d must be 64 or 128");
+    if (out == q || out == k || out == v)
+        return noalloc_fail(LA_ERR_INVALID_ARG,
+                            "la_forward_causal_noalloc: out aliases an input");
+    const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15u;
+    if (mis)
+        return noalloc_fail(LA_ERR_UNSUPPORTED,
+                            "la_forward_causal_noalloc: tensors must be 16-byte aligned");
+    DecayArgs dk;
+    dk.has = 0;
+    dk.H = H > 0 ? H : 1;
+    if (decay) {
+        if (H > LA_MAX_DECAY_HEADS)
+            return noalloc_fail(LA_ERR_UNSUPPORTED,
+                                "la_forward_causal_noalloc: decay given for more than 1024 heads");
+        for (int h = 0; h < H; ++h) {
+            const float g = decay[h];
+            if (!(g >= 0.f && g <= 1.f))
+                return noalloc_fail(LA_ERR_INVALID_ARG,
+                                    "la_forward_causal_noalloc: decay values must lie in [0, 1]");
+            dk.g[h] = g;
+        }
+        dk.has = 1;
+    }
+    const FwdShape sh{B, H, N, d};
+    if (sh.BH() == 0 || N == 0) return LA_OK;
+    if (sh.BH() > 2147483647LL || (long long)N * d > (1LL << 40))
+        return noalloc_fail(LA_ERR_UNSUPPORTED,
+                            "la_forward_causal_noalloc: problem too large");
+    cudaError_t ce;
+    int *status = device_status_word(&ce);
+    if (!status) {
+        set_last_error("la_forward_causal_noalloc: status word lookup failed");
+        return LA_ERR_CUDA;
+    }
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    TcResult r;
+    if (d == 128)
+        r = dk.has ? launch_causal_noalloc_t<128, true>(q, k, v, out, sh, dk, status, s)
+                   : launch_causal_noalloc_t<128, false>(q, k, v, out, sh, dk, status, s);
+    else
+        r = dk.has ? launch_causal_noalloc_t<64, true>(q, k, v, out, sh, dk, status, s)
+                   : launch_causal_noalloc_t<64, false>(q, k, v, out, sh, dk, status, s);
+    if (r.status != LA_OK) {
+        char msg[256];
+        if (r.status == LA_ERR_CUDA)
+            std::snprintf(msg, sizeof(msg), "%s: %s", r.where, cudaGetErrorString(r.cuda));
+        else
+            std::snprintf(msg, sizeof(msg), "%s", r.where);
+        set_last_error(msg);
+    }
+    return r.status;
+}

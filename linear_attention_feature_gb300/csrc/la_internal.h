@@ -46,4 +46,7 @@ int *device_status_word(cudaError_t *err);
 // Counts every kernel enqueued by the library (la_kernel_launch_count).
 void note_launches(int n);
 
+// Records the detail returned by la_last_error() on the calling thread.
+void set_last_error(const char *msg);
+
 }  // namespace la
