@@ -8,28 +8,36 @@
 //   P      = phi(Q) phi(K)^T                       (tcgen05, TMEM fp32)
 //   Pt_ij  = P_ij g^(i-j) for j <= i, else 0       (epilogue, rounded bf16)
 //   O      = Pt V + diag(g^(i+1)) phi(Q) S         (tcgen05; Pt read from TMEM)
-//   den_i  = rowsum(Pt_i) + g^(i+1) phi(q_i).z
+//   den    = Pt 1 + diag(g^(i+1)) phi(Q) z
 //   out_i  = O_i / den_i
-//   S     <- g^n S + Khat^T V,  Khat_t = g^(n-1-t) phi(k_t)   (n = chunk length)
-//   z     <- g^n z + sum_t Khat_t
-// S is carried in TMEM in fp32 and copied to shared memory in bf16 as the B
-// operand of the next chunk's phi(Q) S.
+//   S     <- g^n S + phi(K)^T Vhat,  Vhat_t = g^(n-1-t) v_t   (n = chunk length)
+//   z     <- g^n z + phi(K)^T w,     w_t = g^(n-1-t)
+// A tcgen05.mma costs about the same for any N up to 128, so the normaliser
+// rides along as a 65th column of the wide products: phi(Q) [S | z],
+// Pt [V | 1] and phi(K)^T [Vhat | w] are single N = 80 MMAs (the extra
+// 64-column operand block holds z, ones or w in its first column).  S and z
+// are carried in TMEM in fp32 and copied to shared memory in bf16 as the B
+// operand of the next chunk's phi(Q) [S | z], so numerator and denominator
+// are formed from the same bf16 operands.  The feature
+// map is evaluated on packed bf16 pairs: phi(x) = max(x, 0) + 2^(min(x, 0)
+// log2 e), which is elu(x) + 1 with alpha = 1.
 //
 // Sequence parallelism inside a head: a head's chunks are cut into segments
 // of `seg_chunks` chunks, and the value dimension into halves of 64 columns
 // (d = 128 gives two halves, each with all 128 key features).  A work item
 // is (head, segment, half); persistent CTAs take items from a ticket counter
 // (so a CTA only ever waits on items held by running CTAs).  A segment that
-// has successors first reduces its local decayed state (phase A: phi(K)^T V
-// only) and publishes it; it then looks back over its predecessors' published
-// states (inclusive prefixes end the walk) to get its start state, publishes
-// its own inclusive prefix, and runs the chunk loop (phase B).  The phase-B
-// re-read of K and V normally hits L2 (phase A loads them with evict-last).
+// has successors first reduces its local decayed state (phase A:
+// Khat^T [V | 1] only, Khat_t = g^(L-1-t) phi(k_t) relative to its end) and publishes it; it then looks back over its
+// predecessors' published states (an inclusive prefix ends the walk) to get
+// its start state, publishes its own inclusive prefix, and runs the chunk
+// loop (phase B).  The phase-B re-read of K and V normally hits L2 (phase A
+// loads them with evict-last).
 //
-// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-5 feature-map transform (T), warps 6-9 score and output
-// epilogues (E), warps 10-13 state epilogue and look-back (S).  All waits are
-// bounded; a wait that runs out sets the device status word to
+// Warp roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-9 feature-map transform (T), warps 10-13 score and output
+// epilogues (E), warps 14-17 state epilogue and look-back (S).  All waits
+// are bounded; a wait that runs out sets the device status word to
 // LA_ERR_TIMEOUT and an abort flag, after which every wait passes through so
 // that the kernel finishes (with invalid output) instead of hanging.
 #include "la_tc.h"
@@ -46,12 +54,18 @@ using namespace la::tc;
 
 constexpr int C = 128;           // chunk length (tokens) = MMA M
 constexpr int DV = 64;           // value columns per work item
-constexpr int kThreads = 448;
-constexpr int kWarpT = 2, kWarpE = 6, kWarpS = 10;
+constexpr int kWarpT = 2, kNumT = 8, kWarpE = 10, kWarpS = 14;
+constexpr int kThreads = (kWarpS + 4) * 32;  // 576
+constexpr int kTThreads = kNumT * 32;
 constexpr int BAR_T = 1, BAR_E = 2, BAR_S = 3;
-constexpr uint32_t TM_P = 0, TM_O = 128, TM_OQS = 192, TM_S = 256;
+// TMEM columns
+// P (128), O | den (80), inter-chunk O | den with decay (80), S | z (80)
+constexpr uint32_t TM_P = 0, TM_O = 128, TM_OQS = 208, TM_S = 288;
 constexpr uint32_t TM_COLS = 512;
+constexpr int NX = DV + 16;  // extended N of the wide products
 constexpr int FLAG_AGG = 1, FLAG_INCL = 2;
+constexpr uint32_t kBf16One2 = 0x3F803F80u;    // (1, 1)
+constexpr uint32_t kBf16Log2e2 = 0x3FB93FB9u;  // (log2 e, log2 e) in bf16
 
 struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
@@ -65,29 +79,34 @@ struct Params {
 template <int DK, bool kDecay>
 struct Layout {
     static constexpr int KB = DK / 64;
-    static constexpr int STAGES = DK == 128 ? 2 : 3;
+    static constexpr int STAGES = DK == 128 ? 2 : (kDecay ? 3 : 4);
     static constexpr int TILE = DK * C * 2;   // a Q or K tile (bf16)
     static constexpr int VTILE = C * DV * 2;  // a V (or O) tile half
     static constexpr int STAGE = 2 * TILE + VTILE;
     static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 2 * TILE;
+    // [S | z] in bf16: MN-major B operand [K = a][N = 80]; block 0 = S,
+    // block 1 column 0 = z (rest zero)
     static constexpr int OFF_SB = STAGES * STAGE;
-    static constexpr int SB = DK * DV * 2;
-    static constexpr int OFF_KHAT = OFF_SB + SB;
-    static constexpr int KHAT = kDecay ? TILE : 0;
-    static constexpr int OFF_SMALL = OFF_KHAT + KHAT;
+    static constexpr int SBLK = DK * 128;
+    static constexpr int SB = 2 * SBLK;
+    // [V | 1]: 64-column block whose column 0 is one (rest zero), the
+    // second N block of the V operand (reached through the descriptor LBO)
+    static constexpr int OFF_ONESX = OFF_SB + SB;
+    static constexpr int ONESX = 16384;
+    // [Vhat | w] with decay: for d = 128 it lives in the stage's Q slot once
+    // phi(Q) is consumed; for d = 64 in its own buffer
+    static constexpr bool VHAT_IN_Q = DK == 128;
+    static constexpr int OFF_VHAT_OWN = OFF_ONESX + ONESX;
+    static constexpr int VHAT_OWN = (kDecay && !VHAT_IN_Q) ? 2 * 16384 : 0;
+    static constexpr int OFF_SMALL = OFF_VHAT_OWN + VHAT_OWN;
     static constexpr int STATE = DK * DV + DK;
 };
 
 struct Small {
-    float zbuf[128];        // T: running z (state before the chunk)
-    float zstart[128];      // S -> T: z at the start of the segment
-    float dzbuf[128];       // T -> S: phase-A local z
-    float colsum[128];      // T scratch
-    float den_inter[3][128];
-    float gtab[128];        // E: g^0 .. g^127 of the current head
-    uint64_t full[3], empty[3], xf[3];
-    uint64_t pfull, pt_ready, o_full, o_empty, pv_done, s_full, sb_ready,
-        zready, dz_ready;
+    float gtab[32];  // E: g^0 .. g^31 of the current head
+    uint64_t full[4], empty[4], xf[4];
+    uint64_t pfull, pt_ready, o_full, o_empty, pv_done, s_full, sb_ready;
+    uint64_t qs_done, vhat_ready;
     uint64_t item_full[2], item_empty[2];
     int ring[2];
     uint32_t tmem_base;
@@ -129,6 +148,7 @@ __device__ __forceinline__ void raise_timeout(const Ctx &cx) {
 // Bounded mbarrier wait; passes through (returns false) once aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
                                          const Ctx &cx) {
+    if (mbar_try_wait(bar, parity)) return true;
     if (*cx.abort) return false;
     const long long dl = clock64() + cx.timeout;
     for (int n = 1;; ++n) {
@@ -159,7 +179,7 @@ __device__ __forceinline__ int poll_flag(const int *f, const Ctx &cx) {
             raise_timeout(cx);
             return FLAG_INCL;
         }
-        __nanosleep(100);
+        __nanosleep(64);
     }
 }
 
@@ -178,17 +198,16 @@ __device__ __forceinline__ float head_log2g(const DecayArgs &dk, int bh) {
     return log2f(dk.g[bh % dk.H]);
 }
 
-// elu(x) + 1 (alpha = 1)
-__device__ __forceinline__ float phi(float x) {
-    return x > 0.f ? x + 1.f : __expf(x);
+// elu(x) + 1 on two packed bf16 values: max(x, 0) + 2^(min(x, 0) log2 e)
+__device__ __forceinline__ uint32_t phi2(uint32_t x) {
+    return bf2_add(bf2_max(x, 0u), bf2_ex2(bf2_mul(bf2_min(x, 0u), kBf16Log2e2)));
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t w) {
-    return __uint_as_float(w << 16);
+__device__ __forceinline__ uint32_t bf2_splat(float w) {
+    return pack_bf16x2(w, w);
 }
-__device__ __forceinline__ float bf_hi(uint32_t w) {
-    return __uint_as_float(w & 0xFFFF0000u);
-}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
 // Pop the next item id from the CTA's item ring (every thread of a role
 // calls; `nthreads` threads share the named barrier `bar_id`, or 0 for a
@@ -248,17 +267,30 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
 
 // ---------------------------------------------------------------- MMA issuer
 
+// Offset of K-step `ks` (16 elements) in a K-major, 128-byte-swizzled tile
+// made of 64-element atoms of `atom_bytes` each.
+__device__ __forceinline__ uint32_t kmajor_off(int ks, uint32_t atom_bytes) {
+    return (uint32_t)(ks >> 2) * atom_bytes + (uint32_t)(ks & 3) * 32u;
+}
+
+template <int DK, bool kDecay>
+__device__ __forceinline__ uint32_t vhat_base(uint8_t *smem, int st) {
+    using L = Layout<DK, kDecay>;
+    return L::VHAT_IN_Q ? smem_u32(smem + st * L::STAGE + L::OFF_Q)
+                        : smem_u32(smem + L::OFF_VHAT_OWN);
+}
+
 template <int DK, bool kDecay>
 __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                            const Ctx &cx, uint32_t tmem) {
     using L = Layout<DK, kDecay>;
     constexpr uint32_t idP = idesc_bf16(128, 128, 0, 0);
-    constexpr uint32_t idPV = idesc_bf16(128, DV, 0, 1);
-    constexpr uint32_t idQS = idesc_bf16(128, DV, 0, 1);
-    constexpr uint32_t idSU = idesc_bf16(128, DV, 1, 1);
-    constexpr uint32_t lboA = DK == 128 ? 16384 : 0;  // d=64: rows 64..127 alias
+    constexpr uint32_t idPV = idesc_bf16(128, NX, 0, 1);  // Pt [V | 1]
+    constexpr uint32_t idQS = idesc_bf16(128, NX, 0, 1);  // phi(Q) [S | z]
+    constexpr uint32_t idSU = idesc_bf16(128, NX, 1, 1);  // phi(K)^T [V | 1]
+    constexpr uint32_t lboA = DK == 128 ? 16384 : 0;      // d=64: rows 64..127 alias
     const uint32_t sb = smem_u32(smem + L::OFF_SB);
-    const uint32_t khat = smem_u32(smem + L::OFF_KHAT);
+    const uint32_t onesx = smem_u32(smem + L::OFF_ONESX);
     int j = 0, nb = 0, nsb = 0, tl = 0;
     for (;;) {
         const int t = pop_item(sm, tl, cx, 0, 0, true);
@@ -273,9 +305,10 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 tc_fence_after();
                 const uint32_t kb = smem_u32(smem + st * L::STAGE + L::OFF_K);
                 const uint32_t vb = smem_u32(smem + st * L::STAGE + L::OFF_V);
+                // Khat^T [V | 1]
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
-                           sdesc_sw128(vb + ks * 2048, 16384, 1024), idSU,
+                           sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idSU,
                            (c > it.c0 || ks > 0) ? 1u : 0u);
                 if (c == it.c1 - 1) mma_commit(&sm.s_full);
                 mma_commit(&sm.empty[st]);
@@ -291,7 +324,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             const uint32_t vb = smem_u32(smem + st * L::STAGE + L::OFF_V);
             // P = phi(Q) phi(K)^T
             for (int ks = 0; ks < DK / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                const uint32_t off = kmajor_off(ks, 16384);
                 mma_ss(tmem + TM_P, sdesc_sw128(qb + off, 16, 1024),
                        sdesc_sw128(kb + off, 16, 1024), idP, ks > 0 ? 1u : 0u);
             }
@@ -300,27 +333,32 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             ++nsb;
             wait_bar(&sm.o_empty, (nb & 1) ^ 1, cx);
             tc_fence_after();
-            // phi(Q) S (into O, or into the separate inter-chunk accumulator
-            // when a decay weight must be applied per row)
-            for (int ks = 0; ks < DK / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            // inter-chunk read: phi(Q) [S | z]
+            for (int ks = 0; ks < DK / 16; ++ks)
                 mma_ss(tmem + (kDecay ? TM_OQS : TM_O),
-                       sdesc_sw128(qb + off, 16, 1024),
-                       sdesc_sw128(sb + ks * 2048, 16384, 1024), idQS,
+                       sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
+                       sdesc_sw128(sb + ks * 2048, L::SBLK, 1024), idQS,
                        ks > 0 ? 1u : 0u);
+            // state update: phi(K)^T [V | 1], or phi(K)^T [Vhat | w] (decay;
+            // Vhat is written once phi(Q) has been consumed)
+            uint32_t vsu = vb, lsu = onesx - vb;
+            if (kDecay) {
+                mma_commit(&sm.qs_done);
+                wait_bar(&sm.vhat_ready, nb & 1, cx);
+                tc_fence_after();
+                vsu = vhat_base<DK, kDecay>(smem, st);
+                lsu = 16384;
             }
-            // S += Khat^T V
-            const uint32_t ka = kDecay ? khat : kb;
             for (int ks = 0; ks < C / 16; ++ks)
-                mma_ss(tmem + TM_S, sdesc_sw128(ka + ks * 2048, lboA, 1024),
-                       sdesc_sw128(vb + ks * 2048, 16384, 1024), idSU, 1u);
+                mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
+                       sdesc_sw128(vsu + ks * 2048, lsu, 1024), idSU, 1u);
             mma_commit(&sm.s_full);
             wait_bar(&sm.pt_ready, nb & 1, cx);
             tc_fence_after();
-            // O += Pt V, Pt (bf16) read from TMEM
+            // intra-chunk: Pt [V | 1] (Pt read from TMEM)
             for (int ks = 0; ks < C / 16; ++ks)
                 mma_ts(tmem + TM_O, tmem + TM_P + ks * 8,
-                       sdesc_sw128(vb + ks * 2048, 16384, 1024), idPV,
+                       sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV,
                        (kDecay && ks == 0) ? 0u : 1u);
             mma_commit(&sm.o_full);
             mma_commit(&sm.pv_done);
@@ -331,151 +369,119 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
 
 // ---------------------------------------------------------------- transform
 
-// Sum over the rows of column `col` (bf16) of a [128][DK] swizzled tile,
-// rows [r0, r0 + nr).
+// phi (bf16 pairs) over this thread's share of one row of a [128][DK]
+// swizzled tile, in place; rows with `zero` set become 0.
 template <int DK>
-__device__ __forceinline__ float column_sum(const uint8_t *tile, int col,
-                                            int r0, int nr) {
-    const uint8_t *blk = tile + (col >> 6) * 16384;
-    const int c = col & 63;
-    float s = 0.f;
-#pragma unroll 8
-    for (int r = r0; r < r0 + nr; ++r) {
-        const uint16_t h = *reinterpret_cast<const uint16_t *>(blk + sw128_offset(r, c));
-        s += __uint_as_float((uint32_t)h << 16);
+__device__ __forceinline__ void transform_row(uint8_t *tile, int row, int part,
+                                              bool zero) {
+    constexpr int NCH = DK / 16;  // 16-byte chunks per thread (half a row)
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int cc = part * NCH + i;
+        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
+        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
+        uint4 y;
+        y.x = phi2(x.x);
+        y.y = phi2(x.y);
+        y.z = phi2(x.z);
+        y.w = phi2(x.w);
+        if (zero) y = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(tile + off) = y;
     }
-    return s;
 }
 
-// Column sums of a [128][DK] tile into `out` (thread a of 128 owns column a
-// for DK = 128; for DK = 64 two threads split the rows and combine).
+// Khat = w phi(K) in place (phase A weights relative to the segment end).
 template <int DK>
-__device__ __forceinline__ float tile_colsum(const uint8_t *tile, int et,
-                                             Small &sm) {
-    if (DK == 128) return column_sum<DK>(tile, et, 0, 128);
-    const float part = column_sum<DK>(tile, et & 63, (et >> 6) * 64, 64);
-    sm.colsum[et] = part;
-    named_bar_sync(BAR_T, 128);
-    const float s = (et < 64) ? sm.colsum[et] + sm.colsum[et + 64] : 0.f;
-    return s;
+__device__ __forceinline__ void transform_row_scaled(uint8_t *tile, int row,
+                                                     int part, uint32_t w2) {
+    constexpr int NCH = DK / 16;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int cc = part * NCH + i;
+        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
+        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
+        uint4 y;
+        y.x = bf2_mul(phi2(x.x), w2);
+        y.y = bf2_mul(phi2(x.y), w2);
+        y.z = bf2_mul(phi2(x.z), w2);
+        y.w = bf2_mul(phi2(x.w), w2);
+        *reinterpret_cast<uint4 *>(tile + off) = y;
+    }
 }
 
 template <int DK, bool kDecay>
 __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                           const Ctx &cx, const DecayArgs &dk) {
     using L = Layout<DK, kDecay>;
-    const int et = threadIdx.x - kWarpT * 32;  // 0..127: row / column owned
-    uint8_t *khat = smem + L::OFF_KHAT;
-    int j = 0, tl = 0, ns = 0, nzr = 0;
+    const int et = threadIdx.x - kWarpT * 32;  // 0..255
+    const int row = et & 127, part = et >> 7;
+    int j = 0, nb = 0, tl = 0;
     for (;;) {
-        const int t = pop_item(sm, tl, cx, BAR_T, 128, et == 0);
+        const int t = pop_item(sm, tl, cx, BAR_T, kTThreads, et == 0);
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         if (it.hasA) {
             // phase A: Khat_t = g^(L-1-t) phi(k_t), t relative to the segment
             const int seg_end = min(it.c1 * C, p.N);
-            float dz = 0.f;
             for (int c = it.c0; c < it.c1; ++c, ++j) {
                 const int st = j % L::STAGES;
                 wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
                 uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
-                const int tok = c * C + et;
-                const float w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
-#pragma unroll
-                for (int kb = 0; kb < L::KB; ++kb)
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4 *ptr = reinterpret_cast<uint4 *>(
-                            kt + kb * 16384 + sw128_offset(et, ch * 8));
-                        uint4 x = *ptr;
-                        uint32_t *xw = reinterpret_cast<uint32_t *>(&x);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            xw[e] = pack_bf16x2(w * phi(bf_lo(xw[e])),
-                                                w * phi(bf_hi(xw[e])));
-                        *ptr = x;
-                    }
+                const int tok = c * C + row;
+                if (kDecay || tok >= p.N) {
+                    const float w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
+                    transform_row_scaled<DK>(kt, row, part, bf2_splat(w));
+                } else {
+                    transform_row<DK>(kt, row, part, false);
+                }
                 fence_async_shared();
-                named_bar_sync(BAR_T, 128);
+                named_bar_sync(BAR_T, kTThreads);
                 if (et == 0) mbar_arrive(&sm.xf[st]);
-                dz += tile_colsum<DK>(kt, et, sm);
-                named_bar_sync(BAR_T, 128);
-                if (et == 0) mbar_arrive(&sm.empty[st]);
             }
-            if (et < DK) sm.dzbuf[et] = dz;
-            named_bar_sync(BAR_T, 128);
-            if (et == 0) mbar_arrive(&sm.dz_ready);
-            ++ns;
         }
-        // phase B: start state from the look-back
-        wait_bar(&sm.zready, nzr & 1, cx);
-        ++nzr;
-        if (et < DK) sm.zbuf[et] = sm.zstart[et];
-        named_bar_sync(BAR_T, 128);
-        for (int c = it.c0; c < it.c1; ++c, ++j) {
+        for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % L::STAGES;
             wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
             uint8_t *qt = smem + st * L::STAGE + L::OFF_Q;
             uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
             const int n = min(C, p.N - c * C);
-            // phi(Q) in place; den_inter_i = g^(i+1) phi(q_i) . z
-            float dot = 0.f;
-#pragma unroll
-            for (int kb = 0; kb < L::KB; ++kb)
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 *ptr = reinterpret_cast<uint4 *>(
-                        qt + kb * 16384 + sw128_offset(et, ch * 8));
-                    uint4 x = *ptr;
-                    uint32_t *xw = reinterpret_cast<uint32_t *>(&x);
-                    const float *zz = sm.zbuf + kb * 64 + ch * 8;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        xw[e] = pack_bf16x2(phi(bf_lo(xw[e])), phi(bf_hi(xw[e])));
-                        dot = fmaf(bf_lo(xw[e]), zz[2 * e], dot);
-                        dot = fmaf(bf_hi(xw[e]), zz[2 * e + 1], dot);
-                    }
-                    *ptr = x;
-                }
-            sm.den_inter[st][et] = kDecay ? gpow(lg, et + 1) * dot : dot;
-            // phi(K) in place (rows past the sequence end masked to 0);
-            // with decay also Khat = g^(n-1-t) phi(K) for the state update
-            const bool valid = et < n;
-            float w = 1.f;
-            if (kDecay) {
-                if (ns > 0) wait_bar(&sm.s_full, (ns - 1) & 1, cx);
-                w = valid ? gpow(lg, n - 1 - et) : 0.f;
-            }
-#pragma unroll
-            for (int kb = 0; kb < L::KB; ++kb)
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t off = kb * 16384 + sw128_offset(et, ch * 8);
-                    uint4 *ptr = reinterpret_cast<uint4 *>(kt + off);
-                    uint4 x = *ptr, xh;
-                    uint32_t *xw = reinterpret_cast<uint32_t *>(&x);
-                    uint32_t *hw = reinterpret_cast<uint32_t *>(&xh);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float a0 = valid ? phi(bf_lo(xw[e])) : 0.f;
-                        const float a1 = valid ? phi(bf_hi(xw[e])) : 0.f;
-                        xw[e] = pack_bf16x2(a0, a1);
-                        if (kDecay) hw[e] = pack_bf16x2(w * a0, w * a1);
-                    }
-                    *ptr = x;
-                    if (kDecay) *reinterpret_cast<uint4 *>(khat + off) = xh;
-                }
+            transform_row<DK>(qt, row, part, false);
+            transform_row<DK>(kt, row, part, row >= n);  // rows past N -> 0
             fence_async_shared();
-            named_bar_sync(BAR_T, 128);
+            named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
-            // z <- g^n z + sum_t Khat_t
-            const float cs = tile_colsum<DK>(kDecay ? khat : kt, et, sm);
-            named_bar_sync(BAR_T, 128);
-            if (et == 0) mbar_arrive(&sm.empty[st]);
-            if (et < DK) sm.zbuf[et] = gpow(lg, n) * sm.zbuf[et] + cs;
-            named_bar_sync(BAR_T, 128);
-            ++ns;
+            if (kDecay) {
+                // [Vhat | w] with w_t = g^(n-1-t): written once phi(Q) [S | z]
+                // (which reads the Q slot) and the previous state update
+                // (which read the previous [Vhat | w]) have completed
+                wait_bar(&sm.qs_done, nb & 1, cx);
+                uint8_t *vh = smem + (L::VHAT_IN_Q ? st * L::STAGE + L::OFF_Q
+                                                   : L::OFF_VHAT_OWN);
+                const uint8_t *vt = smem + st * L::STAGE + L::OFF_V;
+                const float w = row < n ? gpow(lg, n - 1 - row) : 0.f;
+                const uint32_t w2 = bf2_splat(w);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t off = sw128_offset(row, (part * 4 + i) * 8);
+                    const uint4 x = *reinterpret_cast<const uint4 *>(vt + off);
+                    *reinterpret_cast<uint4 *>(vh + off) =
+                        make_uint4(bf2_mul(x.x, w2), bf2_mul(x.y, w2),
+                                   bf2_mul(x.z, w2), bf2_mul(x.w, w2));
+                }
+                // w block: column 0 = w_t, the rest zero
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ch = part * 4 + i;
+                    const uint32_t off = sw128_offset(row, ch * 8);
+                    const uint32_t lo = (ch == 0) ? (w2 & 0xFFFFu) : 0u;
+                    *reinterpret_cast<uint4 *>(vh + 16384 + off) =
+                        make_uint4(lo, 0u, 0u, 0u);
+                }
+                fence_async_shared();
+                named_bar_sync(BAR_T, kTThreads);
+                if (et == 0) mbar_arrive(&sm.vhat_ready);
+            }
         }
     }
 }
@@ -499,7 +505,7 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         if (kDecay) {
-            sm.gtab[et] = gpow(lg, et);
+            if (et < 32) sm.gtab[et] = gpow(lg, et);
             named_bar_sync(BAR_E, 128);
         }
         const float wq = kDecay ? gpow(lg, row + 1) : 1.f;
@@ -511,10 +517,9 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
             }
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % L::STAGES;
-            // ---- scores: mask, decay, bf16 into TMEM (in place), row sums
+            // ---- scores: causal mask, decay, bf16 into TMEM (in place)
             wait_bar(&sm.pfull, nb & 1, cx);
             tc_fence_after();
-            float rowsum = 0.f;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 uint32_t pk[16];
@@ -525,21 +530,33 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
                     uint32_t v[32];
                     tmem_ld32(lb + TM_P + 32 * b, v);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int j0 = 32 * b + e;
-                        float x0 = __uint_as_float(v[e]);
-                        float x1 = __uint_as_float(v[e + 1]);
+                    if (b < q) {
                         if (kDecay) {
-                            x0 = j0 <= row ? x0 * sm.gtab[row - j0] : 0.f;
-                            x1 = j0 + 1 <= row ? x1 * sm.gtab[row - j0 - 1] : 0.f;
-                        } else if (b == q) {
-                            x0 = j0 <= row ? x0 : 0.f;
-                            x1 = j0 + 1 <= row ? x1 : 0.f;
+                            // g^(row - j) = g^(row - 32b - 31) g^(31 - e)
+                            const float base = gpow(lg, row - 32 * b - 31);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2)
+                                pk[e >> 1] = pack_bf16x2(
+                                    u2f(v[e]) * (base * sm.gtab[31 - e]),
+                                    u2f(v[e + 1]) * (base * sm.gtab[30 - e]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2)
+                                pk[e >> 1] = pack_bf16x2(u2f(v[e]), u2f(v[e + 1]));
                         }
-                        const uint32_t w2 = pack_bf16x2(x0, x1);
-                        rowsum += bf_lo(w2) + bf_hi(w2);
-                        pk[e >> 1] = w2;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            // g^(lane - e) only where e <= lane: for g = 0 a
+                            // negative power is +inf, and 0 * inf is NaN
+                            float x0 = 0.f, x1 = 0.f;
+                            if (e <= lane)
+                                x0 = kDecay ? u2f(v[e]) * gpow(lg, lane - e) : u2f(v[e]);
+                            if (e + 1 <= lane)
+                                x1 = kDecay ? u2f(v[e + 1]) * gpow(lg, lane - e - 1)
+                                            : u2f(v[e + 1]);
+                            pk[e >> 1] = pack_bf16x2(x0, x1);
+                        }
                     }
                 }
                 tmem_st16(lb + TM_P + 16 * b, pk);
@@ -549,43 +566,44 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
             named_bar_sync(BAR_E, 128);
             if (et == 0) mbar_arrive(&sm.pt_ready);
 
-            // ---- output: (O + g^(i+1) O_inter) / den
+            // ---- output: (O + g^(i+1) O_inter) / (den + g^(i+1) den_inter)
             wait_bar(&sm.o_full, nb & 1, cx);
             tc_fence_after();
-            uint32_t o0[32], o1[32];
-            tmem_ld32(lb + TM_O, o0);
-            tmem_ld32(lb + TM_O + 32, o1);
-            tmem_wait_ld();
-            float y[64];
+            float den = u2f(tmem_ld1(lb + TM_O + DV));
+            if (kDecay) den = fmaf(wq, u2f(tmem_ld1(lb + TM_OQS + DV)), den);
+            uint32_t packed[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                y[e] = __uint_as_float(o0[e]);
-                y[32 + e] = __uint_as_float(o1[e]);
-            }
-            if (kDecay) {
-                tmem_ld32(lb + TM_OQS, o0);
-                tmem_ld32(lb + TM_OQS + 32, o1);
-                tmem_wait_ld();
+            for (int h = 0; h < 2; ++h) {
+                uint32_t o[32];
+                tmem_ld32(lb + TM_O + 32 * h, o);
+                if (kDecay) {
+                    uint32_t oi[32];
+                    tmem_ld32(lb + TM_OQS + 32 * h, oi);
+                    tmem_wait_ld();
+                    const float inv = 1.f / den;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    y[e] = fmaf(wq, __uint_as_float(o0[e]), y[e]);
-                    y[32 + e] = fmaf(wq, __uint_as_float(o1[e]), y[32 + e]);
+                    for (int e = 0; e < 32; e += 2)
+                        packed[16 * h + (e >> 1)] =
+                            pack_bf16x2(fmaf(wq, u2f(oi[e]), u2f(o[e])) * inv,
+                                        fmaf(wq, u2f(oi[e + 1]), u2f(o[e + 1])) * inv);
+                } else {
+                    tmem_wait_ld();
+                    const float inv = 1.f / den;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2)
+                        packed[16 * h + (e >> 1)] =
+                            pack_bf16x2(u2f(o[e]) * inv, u2f(o[e + 1]) * inv);
                 }
             }
             tc_fence_before();
             named_bar_sync(BAR_E, 128);
             if (et == 0) mbar_arrive(&sm.o_empty);
-            const float inv = 1.f / (rowsum + sm.den_inter[st][row]);
-            uint8_t *stage_o = smem + st * L::STAGE + L::OFF_Q;  // phi(Q) is dead
+            uint8_t *stage_o = smem + st * L::STAGE + L::OFF_Q;  // Q slot is dead
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint4 v;
-                v.x = pack_bf16x2(y[8 * ch + 0] * inv, y[8 * ch + 1] * inv);
-                v.y = pack_bf16x2(y[8 * ch + 2] * inv, y[8 * ch + 3] * inv);
-                v.z = pack_bf16x2(y[8 * ch + 4] * inv, y[8 * ch + 5] * inv);
-                v.w = pack_bf16x2(y[8 * ch + 6] * inv, y[8 * ch + 7] * inv);
-                *reinterpret_cast<uint4 *>(stage_o + sw128_offset(row, ch * 8)) = v;
-            }
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(stage_o + sw128_offset(row, ch * 8)) =
+                    make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2],
+                               packed[4 * ch + 3]);
             fence_async_shared();
             named_bar_sync(BAR_E, 128);
             if (et == 0) {
@@ -601,6 +619,34 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
 
 // ---------------------------------------------------------------- state S
 
+// Writes bf16 values of one 32-column half of S row `a` into block 0 of the
+// [S | z] operand (MN-major, K = a rows).
+__device__ __forceinline__ void store_sb_half(uint8_t *sb, int a, int h,
+                                              const float (&x)[32]) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4 *>(sb + sw128_offset(a, 32 * h + ch * 8)) =
+            make_uint4(pack_bf16x2(x[8 * ch], x[8 * ch + 1]),
+                       pack_bf16x2(x[8 * ch + 2], x[8 * ch + 3]),
+                       pack_bf16x2(x[8 * ch + 4], x[8 * ch + 5]),
+                       pack_bf16x2(x[8 * ch + 6], x[8 * ch + 7]));
+}
+
+// z[a] in bf16 at column 0 of block 1 of the [S | z] operand.
+__device__ __forceinline__ void store_zb(uint8_t *sb_z, int a, float z) {
+    *reinterpret_cast<__nv_bfloat16 *>(sb_z + sw128_offset(a, 0)) =
+        __float2bfloat16_rn(z);
+}
+
+// z column of the [S | z] accumulator: (z, 0, ..., 0) over 16 columns.
+__device__ __forceinline__ void tmem_put_z(uint32_t taddr, float z) {
+    uint32_t v[16];
+    v[0] = __float_as_uint(z);
+#pragma unroll
+    for (int e = 1; e < 16; ++e) v[e] = 0u;
+    tmem_st16(taddr, v);
+}
+
 template <int DK, bool kDecay>
 __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                            const Ctx &cx, const DecayArgs &dk, uint32_t tmem) {
@@ -612,7 +658,8 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
     const bool act = a < DK;      // warp-uniform
     const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);
     uint8_t *sb = smem + L::OFF_SB;
-    int tl = 0, ns = 0, ndz = 0;
+    uint8_t *sbz = sb + L::SBLK;
+    int tl = 0, ns = 0;
     bool pending = false;
     for (;;) {
         const int t = pop_item(sm, tl, cx, BAR_S, 128, et == 0);
@@ -635,113 +682,101 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
             if (et == 0) mbar_arrive(&sm.sb_ready);
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
-            wait_bar(&sm.dz_ready, ndz & 1, cx);
-            ++ndz;
             tc_fence_after();
             if (act) {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(lb + TM_S, v0);
-                tmem_ld32(lb + TM_S + 32, v1);
-                tmem_wait_ld();
-                float4 *dst = reinterpret_cast<float4 *>(agg + a * DV);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    dst[e] = make_float4(__uint_as_float(v0[4 * e]), __uint_as_float(v0[4 * e + 1]),
-                                         __uint_as_float(v0[4 * e + 2]), __uint_as_float(v0[4 * e + 3]));
-                    dst[8 + e] = make_float4(__uint_as_float(v1[4 * e]), __uint_as_float(v1[4 * e + 1]),
-                                             __uint_as_float(v1[4 * e + 2]), __uint_as_float(v1[4 * e + 3]));
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_S + 32 * h, v);
+                    tmem_wait_ld();
+                    float4 *dst = reinterpret_cast<float4 *>(agg + a * DV + 32 * h);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
+                                             u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
                 }
-                agg[DK * DV + a] = sm.dzbuf[a];
+                const uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                tmem_wait_ld();
+                agg[DK * DV + a] = u2f(zl);
             }
             __threadfence();
             named_bar_sync(BAR_S, 128);
             if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
         }
-        // look-back over the predecessors of this segment
-        float acc[DV];
+        // look-back over this segment's predecessors, one 32-column half of
+        // S at a time; then the inclusive prefix and the phase-B start state
+        const int n0 = min(C, p.N - it.c0 * C);
+        const float f0 = gpow(lg, n0);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+            float acc[32];
 #pragma unroll
-        for (int e = 0; e < DV; ++e) acc[e] = 0.f;
-        float accz = 0.f;
-        {
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            float accz = 0.f;
             float w = 1.f;
             for (int s2 = it.seg - 1; s2 >= 0; --s2) {
                 const int pi = item_index(it.bh, s2, it.half, p);
                 const int f = poll_flag(p.flags + pi, cx);
-                const float *src = (f == FLAG_INCL ? p.incl : p.agg) + (size_t)pi * L::STATE;
+                const float *src =
+                    (f == FLAG_INCL ? p.incl : p.agg) + (size_t)pi * L::STATE;
                 if (act) {
-                    const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV);
+                    const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV + 32 * h);
 #pragma unroll
-                    for (int e = 0; e < DV / 4; ++e) {
+                    for (int e = 0; e < 8; ++e) {
                         const float4 u = __ldcg(s4 + e);
                         acc[4 * e] = fmaf(w, u.x, acc[4 * e]);
                         acc[4 * e + 1] = fmaf(w, u.y, acc[4 * e + 1]);
                         acc[4 * e + 2] = fmaf(w, u.z, acc[4 * e + 2]);
                         acc[4 * e + 3] = fmaf(w, u.w, acc[4 * e + 3]);
                     }
-                    accz = fmaf(w, __ldcg(src + DK * DV + a), accz);
+                    if (h == 0) accz = fmaf(w, __ldcg(src + DK * DV + a), accz);
                 }
                 if (f == FLAG_INCL) break;
                 w *= gL;
             }
+            if (act) {
+                if (it.hasA) {
+                    // inclusive prefix = g^L S_start + local state
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_S + 32 * h, v);
+                    tmem_wait_ld();
+                    float4 *dst = reinterpret_cast<float4 *>(incl + a * DV + 32 * h);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(fmaf(gL, acc[4 * e], u2f(v[4 * e])),
+                                             fmaf(gL, acc[4 * e + 1], u2f(v[4 * e + 1])),
+                                             fmaf(gL, acc[4 * e + 2], u2f(v[4 * e + 2])),
+                                             fmaf(gL, acc[4 * e + 3], u2f(v[4 * e + 3])));
+                    if (h == 0) {
+                        const uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                        tmem_wait_ld();
+                        incl[DK * DV + a] = fmaf(gL, accz, u2f(zl));
+                    }
+                }
+                // phase-B start: TMEM [S | z] = g^n0 [S_start | z_start], and
+                // the bf16 [S_start | z_start] operand
+                uint32_t v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f0 * acc[e]);
+                tmem_st32(lb + TM_S + 32 * h, v);
+                store_sb_half(sb, a, h, acc);
+                if (h == 0) {
+                    tmem_put_z(lb + TM_S + DV, f0 * accz);
+                    store_zb(sbz, a, accz);
+                }
+                tmem_wait_st();
+            }
         }
         if (it.hasA) {
-            // inclusive prefix = g^L S_start + local state
-            if (act) {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(lb + TM_S, v0);
-                tmem_ld32(lb + TM_S + 32, v1);
-                tmem_wait_ld();
-                float4 *dst = reinterpret_cast<float4 *>(incl + a * DV);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    dst[e] = make_float4(fmaf(gL, acc[4 * e], __uint_as_float(v0[4 * e])),
-                                         fmaf(gL, acc[4 * e + 1], __uint_as_float(v0[4 * e + 1])),
-                                         fmaf(gL, acc[4 * e + 2], __uint_as_float(v0[4 * e + 2])),
-                                         fmaf(gL, acc[4 * e + 3], __uint_as_float(v0[4 * e + 3])));
-                    dst[8 + e] = make_float4(fmaf(gL, acc[32 + 4 * e], __uint_as_float(v1[4 * e])),
-                                             fmaf(gL, acc[32 + 4 * e + 1], __uint_as_float(v1[4 * e + 1])),
-                                             fmaf(gL, acc[32 + 4 * e + 2], __uint_as_float(v1[4 * e + 2])),
-                                             fmaf(gL, acc[32 + 4 * e + 3], __uint_as_float(v1[4 * e + 3])));
-                }
-                incl[DK * DV + a] = fmaf(gL, accz, sm.dzbuf[a]);
-            }
             __threadfence();
             named_bar_sync(BAR_S, 128);
             if (et == 0) publish_flag(p.flags + t, FLAG_INCL);
         }
-        // phase-B start: TMEM S = g^n0 S_start, bf16 S_start as MMA operand
-        {
-            const int n0 = min(C, p.N - it.c0 * C);
-            const float f0 = gpow(lg, n0);
-            if (act) {
-                uint32_t v[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f0 * acc[32 * h + e]);
-                    tmem_st32(lb + TM_S + 32 * h, v);
-                }
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 u;
-                    u.x = pack_bf16x2(acc[8 * ch + 0], acc[8 * ch + 1]);
-                    u.y = pack_bf16x2(acc[8 * ch + 2], acc[8 * ch + 3]);
-                    u.z = pack_bf16x2(acc[8 * ch + 4], acc[8 * ch + 5]);
-                    u.w = pack_bf16x2(acc[8 * ch + 6], acc[8 * ch + 7]);
-                    *reinterpret_cast<uint4 *>(sb + sw128_offset(a, ch * 8)) = u;
-                }
-                sm.zstart[a] = accz;
-                tmem_wait_st();
-            }
-            fence_async_shared();
-            tc_fence_before();
-            named_bar_sync(BAR_S, 128);
-            if (et == 0) {
-                mbar_arrive(&sm.sb_ready);
-                mbar_arrive(&sm.zready);
-            }
-            pending = true;
-        }
+        fence_async_shared();
+        tc_fence_before();
+        named_bar_sync(BAR_S, 128);
+        if (et == 0) mbar_arrive(&sm.sb_ready);
+        pending = true;
         for (int c = it.c0 + 1; c < it.c1; ++c) {
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
@@ -754,22 +789,23 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                     uint32_t v[32];
                     tmem_ld32(lb + TM_S + 32 * h, v);
                     tmem_wait_ld();
+                    float x[32];
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint4 u;
-                        u.x = pack_bf16x2(__uint_as_float(v[8 * ch + 0]), __uint_as_float(v[8 * ch + 1]));
-                        u.y = pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3]));
-                        u.z = pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5]));
-                        u.w = pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7]));
-                        *reinterpret_cast<uint4 *>(sb + sw128_offset(a, 32 * h + ch * 8)) = u;
-                    }
+                    for (int e = 0; e < 32; ++e) x[e] = u2f(v[e]);
+                    store_sb_half(sb, a, h, x);
                     if (kDecay) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f * __uint_as_float(v[e]));
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f * x[e]);
                         tmem_st32(lb + TM_S + 32 * h, v);
                     }
                 }
-                if (kDecay) tmem_wait_st();
+                const float z = u2f(tmem_ld1(lb + TM_S + DV));
+                tmem_wait_ld();
+                store_zb(sbz, a, z);
+                if (kDecay) {
+                    tmem_put_z(lb + TM_S + DV, f * z);
+                    tmem_wait_st();
+                }
             }
             fence_async_shared();
             tc_fence_before();
@@ -800,7 +836,7 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::STAGES; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 3);
+            mbar_init(&sm.empty[s], 2);
             mbar_init(&sm.xf[s], 1);
         }
         mbar_init(&sm.pfull, 1);
@@ -810,14 +846,25 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
         mbar_init(&sm.pv_done, 1);
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.sb_ready, 1);
-        mbar_init(&sm.zready, 1);
-        mbar_init(&sm.dz_ready, 1);
+        mbar_init(&sm.qs_done, 1);
+        mbar_init(&sm.vhat_ready, 1);
         for (int r = 0; r < 2; ++r) {
             mbar_init(&sm.item_full[r], 1);
             mbar_init(&sm.item_empty[r], 4);
         }
         fence_mbar_init();
     }
+    // constant operand blocks: the ones column of [V | 1], and the z block of
+    // [S | z] (column 0 is rewritten per chunk, the rest stays zero)
+    for (int i = threadIdx.x; i < L::ONESX / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + L::OFF_ONESX)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < L::SBLK / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + L::OFF_SB + L::SBLK)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (threadIdx.x < C)
+        *reinterpret_cast<uint16_t *>(smem + L::OFF_ONESX + sw128_offset(threadIdx.x, 0)) =
+            (uint16_t)(kBf16One2 & 0xFFFFu);
+    fence_async_shared();
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, TM_COLS);
         tmem_relinquish();

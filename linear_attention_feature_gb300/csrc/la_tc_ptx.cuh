@@ -237,6 +237,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 32 lanes x 1 32-bit column.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                 : "=r"(r)
+                 : "r"(taddr)
+                 : "memory");
+    return r;
+}
+
 // 32 lanes x 16 consecutive 32-bit columns (store).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr,
                                           const uint32_t (&r)[16]) {
@@ -303,6 +313,34 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row,
                                                           uint32_t col) {
     uint32_t chunk = (col >> 3) ^ (row & 7);
     return row * 128u + chunk * 16u + (col & 7) * 2u;
+}
+
+// ---------------------------------------------------------- bf16x2 math
+
+__device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf2_ex2(uint32_t a) {
+    uint32_t d;
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
