@@ -9,10 +9,11 @@ other paths of the hot path (non-causal form on the same batch, long-context
 causal, causal with per-head decay, fp32 causal, recurrent decode) are timed
 in the same run and reported under "paths".  Rank 0 prints one JSON line.
 
-Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
-on the stream the library launches on, with a 256 MiB write between steps to
-flush L2; barrier + synchronize on both sides of the timed region; the max
-over ranks is taken.  `value` = tokens (B*N per step, summed over ranks) per
+Timing: each step is captured once in a CUDA graph (so that host-side
+launch work does not sit between the events); W untimed warm-up replays, then
+K replays, each bracketed by CUDA events on the stream the library launches
+on, with a 256 MiB write between steps to flush L2; barrier + synchronize on
+both sides of the timed region; the max over ranks is taken.  `value` = tokens (B*N per step, summed over ranks) per
 second.  `e2e` repeats the main step through the C ABI with pinned host
 buffers, the host->device copies of q, k, v and the device->host copy of the
 output inside the timed region.
@@ -151,6 +152,26 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def capture(fn):
+    """Capture one call of `fn` in a CUDA graph; returns (replay, launches)
+    where `launches` is the number of library kernels one call enqueues."""
+    import torch
+    import linear_attention_feature_gb300 as la
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        fn()
+        torch.cuda.synchronize()
+        n0 = la.kernel_launch_count()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        launches = la.kernel_launch_count() - n0
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g.replay, launches
+
+
 def timed_steps(fn, K, W, world, flush=None):
     """Per-step CUDA-event durations (ms) of K steps after W warm-ups."""
     import torch
@@ -233,11 +254,9 @@ def run_ours(args):
     q, k, v = (t.to(dev) for t in wl.make_workload_qkv(w, seed=rank))
     out = torch.empty_like(q)
     main_fn = lambda: la.forward(q, k, v, causal=True, out=out)  # noqa: E731
-    n0 = la.kernel_launch_count()
-    steps_ms = timed_steps(main_fn, K, W, world, flush)
-    launches = (la.kernel_launch_count() - n0)
-    # launches in the timed region = total minus the W warm-ups' share
-    launches = launches * K // (K + W)
+    replay, per_call = capture(main_fn)
+    steps_ms = timed_steps(replay, K, W, world, flush)
+    launches = per_call * K  # library kernels inside the timed region
     la.check_device_status()
     ms = max_over_ranks(sum(steps_ms) / K, world)
     tokens_step = w.B * w.N
@@ -315,7 +334,8 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
                 qq, kk, vv = inputs
             oo = torch.empty_like(qq)
             fn = lambda: la.forward(qq, kk, vv, causal=causal, decay=decay, out=oo)  # noqa
-            steps = timed_steps(fn, Kx, Wx, world, flush)
+            replay, _ = capture(fn)
+            steps = timed_steps(replay, Kx, Wx, world, flush)
             la.check_device_status()
             ms = max_over_ranks(sum(steps) / Kx, world)
             r = {"tokens_per_s": round(w.B * w.N * world / (ms * 1e-3), 1),
@@ -365,14 +385,21 @@ def run_decode(la, wl, dev, peaks, world, rank, args):
     o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
     for t in range(P):  # prefill from the 1024 seeded tokens (untimed)
         la.decode_step(S, z, q[t], k[t], v[t], out=o)
+    # the T timed steps, captured once as one graph of T launches
+    replay, _ = capture(lambda: [la.decode_step(S, z, q[t], k[t], v[t], out=o)
+                                  for t in range(P, P + T)])
+    # capturing ran the steps once: restore the prefilled state
+    S.zero_()
+    z.zero_()
+    for t in range(P):
+        la.decode_step(S, z, q[t], k[t], v[t], out=o)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
-    for t in range(P, P + T):
-        la.decode_step(S, z, q[t], k[t], v[t], out=o)
+    replay()
     e1.record(st)
     torch.cuda.synchronize()
     barrier(world)
@@ -407,15 +434,20 @@ def cpu_baseline(w, q, k, v, seconds):
     qf = qs.reshape(BH, w.N, w.d)[:heads]
     kf = ks.reshape(BH, w.N, w.d)[:heads]
     vf = vs.reshape(BH, w.N, w.d)[:heads]
+    reps = 0
     t0 = time.perf_counter()
-    oracle.causal(qf, kf, vf, nthreads=cores)
-    dt = time.perf_counter() - t0
+    while True:
+        oracle.causal(qf, kf, vf, nthreads=cores)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
     frac = heads / BH
-    return {"value": round(frac * w.B * w.N / dt, 1), "unit": "tokens/s",
+    return {"value": round(reps * frac * w.B * w.N / dt, 1), "unit": "tokens/s",
             "cores": min(cores, heads), "kind": "oracle",
             "sample": f"causal form, {heads} of {BH} heads of {MAIN} "
-                      f"(N={w.N}, d={w.d}), fp64, {dt:.2f} s; tokens/s "
-                      f"scaled by the head fraction"}
+                      f"(N={w.N}, d={w.d}), fp64, {reps} passes in {dt:.1f} s; "
+                      f"tokens/s scaled by the head fraction"}
 
 
 def run_reference(args):

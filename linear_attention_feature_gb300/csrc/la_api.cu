@@ -11,9 +11,12 @@
 
 namespace la {
 
-// Per-device status word.  A kernel that gives up on a bounded wait stores a
-// non-zero la_status here; la_check_device_status reads and clears it.
-__device__ int g_status_word;
+// Per-device status words.  A kernel that gives up on a bounded wait stores a
+// non-zero la_status in word 0 and where it gave up in word 1 (block index in
+// the high 12 bits, the wait's identifier in the low 20 bits: a barrier's
+// shared-memory address, or 0x80000 | a flag's word address);
+// la_check_device_status reads and clears both.
+__device__ int g_status_word[2];
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -185,15 +188,18 @@ la_status la_check_device_status(la_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status: sync");
     int *p = device_status_word(&e);
     if (!p) return cuda_fail(e, "la_check_device_status: status word");
-    int word = 0;
-    e = cudaMemcpy(&word, p, sizeof(int), cudaMemcpyDeviceToHost);
+    int word[2] = {0, 0};
+    e = cudaMemcpy(word, p, sizeof(word), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status: read");
-    if (word != 0) {
-        int zero = 0;
-        e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (word[0] != 0) {
+        int zero[2] = {0, 0};
+        e = cudaMemcpy(p, zero, sizeof(zero), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status: clear");
-        return fail(static_cast<la_status>(word),
-                    "a kernel reported a device-side failure");
+        char msg[160];
+        std::snprintf(msg, sizeof(msg),
+                      "a kernel reported a device-side failure (block %d, wait 0x%05x)",
+                      (word[1] >> 20) & 0xFFF, word[1] & 0xFFFFF);
+        return fail(static_cast<la_status>(word[0]), msg);
     }
     return LA_OK;
 }

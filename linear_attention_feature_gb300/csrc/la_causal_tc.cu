@@ -42,6 +42,7 @@
 // that the kernel finishes (with invalid output) instead of hanging.
 #include "la_tc.h"
 #include "la_tc_host.h"
+#include "la_tc_common.cuh"
 #include "la_tc_ptx.cuh"
 
 #include <cstdio>
@@ -51,6 +52,7 @@ namespace la {
 namespace causal_tc {
 
 using namespace la::tc;
+using namespace la::tcc;
 
 constexpr int C = 128;           // chunk length (tokens) = MMA M
 constexpr int DV = 64;           // value columns per work item
@@ -63,9 +65,6 @@ constexpr int BAR_T = 1, BAR_E = 2, BAR_S = 3;
 constexpr uint32_t TM_P = 0, TM_O = 128, TM_OQS = 208, TM_S = 288;
 constexpr uint32_t TM_COLS = 512;
 constexpr int NX = DV + 16;  // extended N of the wide products
-constexpr int FLAG_AGG = 1, FLAG_INCL = 2;
-constexpr uint32_t kBf16One2 = 0x3F803F80u;    // (1, 1)
-constexpr uint32_t kBf16Log2e2 = 0x3FB93FB9u;  // (log2 e, log2 e) in bf16
 
 struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
@@ -112,12 +111,6 @@ struct Small {
     uint32_t tmem_base;
 };
 
-struct Ctx {
-    volatile int *abort;
-    int *status;
-    long long timeout;
-};
-
 struct Item {
     int bh, seg, half, c0, c1;
     bool hasA;
@@ -139,75 +132,6 @@ __device__ __forceinline__ int item_index(int bh, int seg, int half,
                                           const Params &p) {
     return (seg * p.BH + bh) * p.nhalf + half;
 }
-
-__device__ __forceinline__ void raise_timeout(const Ctx &cx) {
-    atomicExch(cx.status, (int)LA_ERR_TIMEOUT);
-    *cx.abort = 1;
-}
-
-// Bounded mbarrier wait; passes through (returns false) once aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
-                                         const Ctx &cx) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*cx.abort) return false;
-    const long long dl = clock64() + cx.timeout;
-    for (int n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63) == 0) {
-            if (*cx.abort) return false;
-            if (clock64() > dl) {
-                raise_timeout(cx);
-                return false;
-            }
-        }
-    }
-}
-
-// Bounded poll of a published-state flag; returns FLAG_AGG or FLAG_INCL
-// (FLAG_INCL with garbage data once aborted, which ends the look-back).
-__device__ __forceinline__ int poll_flag(const int *f, const Ctx &cx) {
-    const long long dl = clock64() + cx.timeout;
-    for (;;) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
-                     : "=r"(v)
-                     : "l"(f)
-                     : "memory");
-        if (v >= FLAG_AGG) return v;
-        if (*cx.abort) return FLAG_INCL;
-        if (clock64() > dl) {
-            raise_timeout(cx);
-            return FLAG_INCL;
-        }
-        __nanosleep(64);
-    }
-}
-
-__device__ __forceinline__ void publish_flag(int *f, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v)
-                 : "memory");
-}
-
-// g^k from log2(g) (log2(0) = -inf gives 0 for k > 0); k = 0 gives 1.
-__device__ __forceinline__ float gpow(float lg, int k) {
-    return k == 0 ? 1.f : exp2f(lg * (float)k);
-}
-
-__device__ __forceinline__ float head_log2g(const DecayArgs &dk, int bh) {
-    if (!dk.has) return 0.f;
-    return log2f(dk.g[bh % dk.H]);
-}
-
-// elu(x) + 1 on two packed bf16 values: max(x, 0) + 2^(min(x, 0) log2 e)
-__device__ __forceinline__ uint32_t phi2(uint32_t x) {
-    return bf2_add(bf2_max(x, 0u), bf2_ex2(bf2_mul(bf2_min(x, 0u), kBf16Log2e2)));
-}
-
-__device__ __forceinline__ uint32_t bf2_splat(float w) {
-    return pack_bf16x2(w, w);
-}
-
-__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
 // Pop the next item id from the CTA's item ring (every thread of a role
 // calls; `nthreads` threads share the named barrier `bar_id`, or 0 for a
@@ -266,12 +190,6 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
 }
 
 // ---------------------------------------------------------------- MMA issuer
-
-// Offset of K-step `ks` (16 elements) in a K-major, 128-byte-swizzled tile
-// made of 64-element atoms of `atom_bytes` each.
-__device__ __forceinline__ uint32_t kmajor_off(int ks, uint32_t atom_bytes) {
-    return (uint32_t)(ks >> 2) * atom_bytes + (uint32_t)(ks & 3) * 32u;
-}
 
 template <int DK, bool kDecay>
 __device__ __forceinline__ uint32_t vhat_base(uint8_t *smem, int st) {
@@ -530,6 +448,7 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
                     uint32_t v[32];
                     tmem_ld32(lb + TM_P + 32 * b, v);
                     tmem_wait_ld();
+                    reg_fence(v);
                     if (b < q) {
                         if (kDecay) {
                             // g^(row - j) = g^(row - 32b - 31) g^(31 - e)
@@ -569,8 +488,8 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
             // ---- output: (O + g^(i+1) O_inter) / (den + g^(i+1) den_inter)
             wait_bar(&sm.o_full, nb & 1, cx);
             tc_fence_after();
-            float den = u2f(tmem_ld1(lb + TM_O + DV));
-            if (kDecay) den = fmaf(wq, u2f(tmem_ld1(lb + TM_OQS + DV)), den);
+            uint32_t dreg = tmem_ld1(lb + TM_O + DV);
+            uint32_t direg = kDecay ? tmem_ld1(lb + TM_OQS + DV) : 0u;
             uint32_t packed[32];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -580,7 +499,11 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
                     uint32_t oi[32];
                     tmem_ld32(lb + TM_OQS + 32 * h, oi);
                     tmem_wait_ld();
-                    const float inv = 1.f / den;
+                    reg_fence(o);
+                    reg_fence(oi);
+                    reg_fence(dreg);
+                    reg_fence(direg);
+                    const float inv = 1.f / fmaf(wq, u2f(direg), u2f(dreg));
 #pragma unroll
                     for (int e = 0; e < 32; e += 2)
                         packed[16 * h + (e >> 1)] =
@@ -588,7 +511,9 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
                                         fmaf(wq, u2f(oi[e + 1]), u2f(o[e + 1])) * inv);
                 } else {
                     tmem_wait_ld();
-                    const float inv = 1.f / den;
+                    reg_fence(o);
+                    reg_fence(dreg);
+                    const float inv = 1.f / u2f(dreg);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2)
                         packed[16 * h + (e >> 1)] =
@@ -689,14 +614,16 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                     uint32_t v[32];
                     tmem_ld32(lb + TM_S + 32 * h, v);
                     tmem_wait_ld();
+                    reg_fence(v);
                     float4 *dst = reinterpret_cast<float4 *>(agg + a * DV + 32 * h);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
                                              u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
                 }
-                const uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                uint32_t zl = tmem_ld1(lb + TM_S + DV);
                 tmem_wait_ld();
+                reg_fence(zl);
                 agg[DK * DV + a] = u2f(zl);
             }
             __threadfence();
@@ -716,7 +643,7 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
             float w = 1.f;
             for (int s2 = it.seg - 1; s2 >= 0; --s2) {
                 const int pi = item_index(it.bh, s2, it.half, p);
-                const int f = poll_flag(p.flags + pi, cx);
+                const int f = poll_flag_at_least(p.flags + pi, FLAG_AGG, FLAG_INCL, cx);
                 const float *src =
                     (f == FLAG_INCL ? p.incl : p.agg) + (size_t)pi * L::STATE;
                 if (act) {
@@ -740,6 +667,7 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                     uint32_t v[32];
                     tmem_ld32(lb + TM_S + 32 * h, v);
                     tmem_wait_ld();
+                    reg_fence(v);
                     float4 *dst = reinterpret_cast<float4 *>(incl + a * DV + 32 * h);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -748,8 +676,9 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                                              fmaf(gL, acc[4 * e + 2], u2f(v[4 * e + 2])),
                                              fmaf(gL, acc[4 * e + 3], u2f(v[4 * e + 3])));
                     if (h == 0) {
-                        const uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                        uint32_t zl = tmem_ld1(lb + TM_S + DV);
                         tmem_wait_ld();
+                        reg_fence(zl);
                         incl[DK * DV + a] = fmaf(gL, accz, u2f(zl));
                     }
                 }
@@ -789,6 +718,7 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                     uint32_t v[32];
                     tmem_ld32(lb + TM_S + 32 * h, v);
                     tmem_wait_ld();
+                    reg_fence(v);
                     float x[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[e] = u2f(v[e]);
@@ -799,8 +729,10 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                         tmem_st32(lb + TM_S + 32 * h, v);
                     }
                 }
-                const float z = u2f(tmem_ld1(lb + TM_S + DV));
+                uint32_t zr = tmem_ld1(lb + TM_S + DV);
                 tmem_wait_ld();
+                reg_fence(zr);
+                const float z = u2f(zr);
                 store_zb(sbz, a, z);
                 if (kDecay) {
                     tmem_put_z(lb + TM_S + DV, f * z);

@@ -39,8 +39,9 @@ cudaError_t launch_decode_step(float *S, float *z, const void *q,
                                long long BH, int d, la_dtype dtype,
                                cudaStream_t stream);
 
-// Address of the current device's status word (kernels set it to a non-zero
-// la_status when a bounded wait gives up).  Looked up once per device.
+// Address of the current device's two status words (kernels set word 0 to a
+// non-zero la_status when a bounded wait gives up, and word 1 to where).
+// Looked up once per device.
 int *device_status_word(cudaError_t *err);
 
 // Counts every kernel enqueued by the library (la_kernel_launch_count).

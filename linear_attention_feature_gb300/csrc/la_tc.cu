@@ -14,7 +14,7 @@ bool tc_supported(const FwdShape &sh, la_dtype dtype, int causal,
                   const void *out) {
     if (dtype != LA_BF16) return false;
     if (sh.d != 64 && sh.d != 128) return false;
-    if (!causal) return false;  // the non-causal tensor-core kernel is separate
+    (void)causal;
     return aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out);
 }
 
@@ -24,8 +24,7 @@ TcResult tc_forward(const void *q, const void *k, const void *v, void *out,
     if (causal)
         return launch_causal_tc(q, k, v, out, sh, dk, segment_chunks, status,
                                 stream);
-    return {LA_ERR_UNSUPPORTED, cudaSuccess,
-            "la_forward: no tensor-core kernel for this form"};
+    return launch_noncausal_tc(q, k, v, out, sh, segment_chunks, status, stream);
 }
 
 }  // namespace la

@@ -23,6 +23,11 @@ TcResult tc_forward(const void *q, const void *k, const void *v, void *out,
                     const FwdShape &sh, int causal, const DecayArgs &dk,
                     int segment_chunks, int *status, cudaStream_t stream);
 
+// Non-causal two-pass kernel (la_noncausal_tc.cu).
+TcResult launch_noncausal_tc(const void *q, const void *k, const void *v,
+                             void *out, const FwdShape &sh, int seg_chunks,
+                             int *status, cudaStream_t stream);
+
 // Chunkwise causal kernel (la_causal_tc.cu).
 TcResult launch_causal_tc(const void *q, const void *k, const void *v,
                           void *out, const FwdShape &sh, const DecayArgs &dk,

@@ -1,0 +1,103 @@
+// Device helpers shared by the tensor-core kernels: bounded waits, the
+// published-state flags, decay powers and the packed-bf16 feature map.
+#pragma once
+
+#include "la_internal.h"
+#include "la_tc_ptx.cuh"
+
+namespace la {
+namespace tcc {
+
+using namespace la::tc;
+
+constexpr int FLAG_AGG = 1, FLAG_INCL = 2;
+constexpr uint32_t kBf16One2 = 0x3F803F80u;    // (1, 1)
+constexpr uint32_t kBf16Log2e2 = 0x3FB93FB9u;  // (log2 e, log2 e) in bf16
+
+struct Ctx {
+    volatile int *abort;  // set once any wait of the launch gave up
+    int *status;          // device status word
+    long long timeout;    // clock cycles per bounded wait
+};
+
+// Records the first wait that gave up: block index and an identifier (the
+// barrier's shared-memory offset, or the low bits of a flag's address).
+__device__ __forceinline__ void raise_timeout(const Ctx &cx, uint32_t where) {
+    if (atomicCAS(cx.status, 0, (int)LA_ERR_TIMEOUT) == 0)
+        atomicExch(cx.status + 1, (int)((blockIdx.x << 20) | (where & 0xFFFFFu)));
+    *cx.abort = 1;
+}
+
+// Bounded mbarrier wait; passes through (returns false) once aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
+                                         const Ctx &cx) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*cx.abort) return false;
+    const long long dl = clock64() + cx.timeout;
+    for (int n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*cx.abort) return false;
+            if (clock64() > dl) {
+                raise_timeout(cx, smem_u32(bar));
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded poll until *f >= want; returns the value seen (or `give_up` once
+// aborted or timed out).
+__device__ __forceinline__ int poll_flag_at_least(const int *f, int want,
+                                                  int give_up, const Ctx &cx) {
+    const long long dl = clock64() + cx.timeout;
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
+                     : "=r"(v)
+                     : "l"(f)
+                     : "memory");
+        if (v >= want) return v;
+        if (*cx.abort) return give_up;
+        if (clock64() > dl) {
+            raise_timeout(cx, 0x80000u | ((uint32_t)(reinterpret_cast<uintptr_t>(f) >> 2) & 0x7FFFFu));
+            return give_up;
+        }
+        __nanosleep(64);
+    }
+}
+
+__device__ __forceinline__ void publish_flag(int *f, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v)
+                 : "memory");
+}
+
+// g^k from log2(g) (log2(0) = -inf gives 0 for k > 0); k = 0 gives 1.
+__device__ __forceinline__ float gpow(float lg, int k) {
+    return k == 0 ? 1.f : exp2f(lg * (float)k);
+}
+
+__device__ __forceinline__ float head_log2g(const DecayArgs &dk, int bh) {
+    if (!dk.has) return 0.f;
+    return log2f(dk.g[bh % dk.H]);
+}
+
+// elu(x) + 1 on two packed bf16 values: max(x, 0) + 2^(min(x, 0) log2 e)
+__device__ __forceinline__ uint32_t phi2(uint32_t x) {
+    return bf2_add(bf2_max(x, 0u), bf2_ex2(bf2_mul(bf2_min(x, 0u), kBf16Log2e2)));
+}
+
+__device__ __forceinline__ uint32_t bf2_splat(float w) {
+    return pack_bf16x2(w, w);
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// Offset of K-step `ks` (16 elements) in a K-major, 128-byte-swizzled tile
+// made of 64-element atoms of `atom_bytes` each.
+__device__ __forceinline__ uint32_t kmajor_off(int ks, uint32_t atom_bytes) {
+    return (uint32_t)(ks >> 2) * atom_bytes + (uint32_t)(ks & 3) * 32u;
+}
+
+}  // namespace tcc
+}  // namespace la

@@ -237,6 +237,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// tcgen05.ld writes its destination registers asynchronously: they may only
+// be read after tcgen05.wait::ld.  These empty volatile statements, placed
+// right after the wait, "modify" the registers so that the compiler cannot
+// move any use of them above the wait.
+__device__ __forceinline__ void reg_fence(uint32_t &r) {
+    asm volatile("" : "+r"(r));
+}
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // 32 lanes x 1 32-bit column.
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
     uint32_t r;
