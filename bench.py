@@ -198,7 +198,12 @@ def timed_steps(fn, K, W, world, flush=None):
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of a kernel, keyed by kernel and workload, valid only while
 # the kernel's sources hash to the recorded digest (else reported as null).
-KNOWN_TRAFFIC = {}
+KNOWN_TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:causal_kernel
+    #     -s 3 -c 1 python bench.py --kernel-case 4 16 4096 64 causal
+    ("causal_kernel<64,false>", "bf16_b4h16_n4096_d64"):
+        {"sources": "5dd173277415a42b", "bytes": 100742400 + 3939072},
+}
 
 
 def kernel_sources_digest():
