@@ -199,10 +199,13 @@ def timed_steps(fn, K, W, world, flush=None):
 # one ncu capture of a kernel, keyed by kernel and workload, valid only while
 # the kernel's sources hash to the recorded digest (else reported as null).
 KNOWN_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:causal_kernel
-    #     -s 3 -c 1 python bench.py --kernel-case 4 16 4096 64 causal
+    # ncu --set full --clock-control none -k regex:causal_kernel -s 3 -c 1
+    #     python bench.py --kernel-case B H N D causal
+    # (dram__bytes_read.sum + dram__bytes_write.sum of the captured launch)
     ("causal_kernel<64,false>", "bf16_b4h16_n4096_d64"):
-        {"sources": "5dd173277415a42b", "bytes": 100742400 + 3939072},
+        {"sources": "4048ca60f9e1dcc1", "bytes": 100793344 + 4888832},
+    ("causal_kernel<128,false>", "bf16_b2h16_n32768_d128"):
+        {"sources": "4048ca60f9e1dcc1", "bytes": 874345728 + 308971264},
 }
 
 
@@ -355,7 +358,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
     res = {}
     Kx, Wx = max(3, args.steps // 2), max(3, args.warmup)
 
-    def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2):
+    def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2, kernel=None):
         w = wl.WORKLOADS[wkey]
         try:
             if inputs is None:
@@ -371,7 +374,8 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
             r = {"tokens_per_s": round(w.B * w.N * world / (ms * 1e-3), 1),
                  "ms_per_step": round(ms, 4), "steps": Kx,
                  "roofline": roofline_hbm(forward_bytes(w.B, w.H, w.N, w.d, elem),
-                                          ms, peaks["hbm_gbs"])}
+                                          ms, peaks["hbm_gbs"],
+                                          known_traffic(kernel, w) if kernel else None)}
             if causal and elem == 2:
                 C = 128
                 r["tensor"] = tensor_fraction(chunk_flops(w.B, w.H, w.N, w.d, C),
@@ -382,7 +386,8 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
             res[name] = {"error": f"{type(e).__name__}: {e}"}
 
     fwd_path(f"{MAIN} noncausal", MAIN, False, inputs=(q, k, v))
-    fwd_path("bf16_b2h16_n32768_d128 causal", "bf16_b2h16_n32768_d128", True)
+    fwd_path("bf16_b2h16_n32768_d128 causal", "bf16_b2h16_n32768_d128", True,
+             kernel="causal_kernel<128,false>")
     wd = wl.WORKLOADS["bf16_decay_b4h8_n16384_d128"]
     fwd_path("bf16_decay_b4h8_n16384_d128 causal", wd.name, True,
              decay=list(wd.decay))

@@ -35,8 +35,13 @@
 // loads them with evict-last).
 //
 // Warp roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-9 feature-map transform (T), warps 10-13 score and output
-// epilogues (E), warps 14-17 state epilogue and look-back (S).  All waits
+// owner, warps 2-9 feature-map transform, warps 10-13 score epilogue (mask,
+// decay, bf16 P~ in TMEM), warps 14-17 state and output epilogue (bf16
+// [S | z] operand, look-back; O / den, TMA store).  P and (without decay) O
+// have two TMEM buffers, and the MMA issuer issues P of chunk j+1 ahead of
+// P~V of chunk j when it is ready, so the tensor pipe can run
+// ... SU(j) P(j+1) P~V(j) QS(j+1) SU(j+1) ... without waiting for an
+// epilogue to drain a buffer.  All waits
 // are bounded; a wait that runs out sets the device status word to
 // LA_ERR_TIMEOUT and an abort flag, after which every wait passes through so
 // that the kernel finishes (with invalid output) instead of hanging.
@@ -56,15 +61,18 @@ using namespace la::tcc;
 
 constexpr int C = 128;           // chunk length (tokens) = MMA M
 constexpr int DV = 64;           // value columns per work item
-constexpr int kWarpT = 2, kNumT = 8, kWarpE = 10, kWarpS = 14;
-constexpr int kThreads = (kWarpS + 4) * 32;  // 576
+constexpr int kWarpT = 2, kNumT = 8, kWarpE1 = 10, kWarpE2 = 14;
+constexpr int kThreads = (kWarpE2 + 4) * 32;  // 576
 constexpr int kTThreads = kNumT * 32;
-constexpr int BAR_T = 1, BAR_E = 2, BAR_S = 3;
-// TMEM columns
-// P (128), O | den (80), inter-chunk O | den with decay (80), S | z (80)
-constexpr uint32_t TM_P = 0, TM_O = 128, TM_OQS = 208, TM_S = 288;
+constexpr int BAR_T = 1, BAR_E1 = 2, BAR_E2 = 3;
+// TMEM columns: P in two buffers (2 x 128); O | den (80) in two buffers
+// without decay, or O | den and the inter-chunk O | den (80 each) with
+// decay; S | z (80).  496 of 512 columns either way.
+constexpr uint32_t TM_P = 0, TM_O = 256, TM_OQS = 336, TM_S = 416;
 constexpr uint32_t TM_COLS = 512;
 constexpr int NX = DV + 16;  // extended N of the wide products
+template <bool kDecay>
+struct OBufs { static constexpr int n = kDecay ? 1 : 2; };
 
 struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
@@ -97,17 +105,25 @@ struct Layout {
     static constexpr bool VHAT_IN_Q = DK == 128;
     static constexpr int OFF_VHAT_OWN = OFF_ONESX + ONESX;
     static constexpr int VHAT_OWN = (kDecay && !VHAT_IN_Q) ? 2 * 16384 : 0;
-    static constexpr int OFF_SMALL = OFF_VHAT_OWN + VHAT_OWN;
+    // output staging: a buffer of its own where shared memory allows (a
+    // stage is then free once its last product completes), else the stage's
+    // Q slot, dead by the time the chunk's output is ready
+    static constexpr bool OWN_OST = DK == 128 || kDecay;
+    static constexpr int OFF_OST = OFF_VHAT_OWN + VHAT_OWN;
+    static constexpr int OST = OWN_OST ? C * DV * 2 : 0;
+    static constexpr int OFF_SMALL = OFF_OST + OST;
     static constexpr int STATE = DK * DV + DK;
 };
 
 struct Small {
     float gtab[32];  // E: g^0 .. g^31 of the current head
     uint64_t full[4], empty[4], xf[4];
-    uint64_t pfull, pt_ready, o_full, o_empty, pv_done, s_full, sb_ready;
+    uint64_t pfull[2], pt_ready[2], pv_done[2], o_full[2], o_empty[2];
+    uint64_t s_full, sb_ready;
     uint64_t qs_done, vhat_ready;
     uint64_t item_full[2], item_empty[2];
     int ring[2];
+    int lb_flag[32], lb_n;  // look-back decision of the current item
     uint32_t tmem_base;
 };
 
@@ -198,15 +214,59 @@ __device__ __forceinline__ uint32_t vhat_base(uint8_t *smem, int st) {
                         : smem_u32(smem + L::OFF_VHAT_OWN);
 }
 
+// P = phi(Q) phi(K)^T of job `jj` (stage jj % STAGES) into P buffer b of
+// B-chunk number `nbq`, once the chunk is transformed and the buffer's
+// previous P~V has completed.
+template <int DK, bool kDecay>
+__device__ __forceinline__ void issue_p(uint8_t *smem, Small &sm, const Ctx &cx,
+                                        uint32_t tmem, int jj, int nbq) {
+    using L = Layout<DK, kDecay>;
+    constexpr uint32_t idP = idesc_bf16(128, 128, 0, 0);
+    const int st = jj % L::STAGES, b = nbq & 1;
+    wait_bar(&sm.xf[st], (jj / L::STAGES) & 1, cx);
+    wait_bar(&sm.pv_done[b], ((nbq >> 1) & 1) ^ 1, cx);
+    tc_fence_after();
+    const uint32_t qb = smem_u32(smem + st * L::STAGE + L::OFF_Q);
+    const uint32_t kb = smem_u32(smem + st * L::STAGE + L::OFF_K);
+    for (int ks = 0; ks < DK / 16; ++ks) {
+        const uint32_t off = kmajor_off(ks, 16384);
+        mma_ss(tmem + TM_P + 128u * b, sdesc_sw128(qb + off, 16, 1024),
+               sdesc_sw128(kb + off, 16, 1024), idP, ks > 0 ? 1u : 0u);
+    }
+    mma_commit(&sm.pfull[b]);
+}
+
+// Issues P of B chunk qi+1 now if its feature maps and P buffer are ready;
+// otherwise it is issued (blocking) at the top of the next chunk, so the
+// state-dependent products of chunk qi never wait on the transform.
+template <int DK, bool kDecay>
+__device__ __forceinline__ void try_issue_next_p(uint8_t *smem, Small &sm,
+                                                 const Ctx &cx, uint32_t tmem,
+                                                 int jj, int nbq, int qi,
+                                                 int nB, int &p_next) {
+    using L = Layout<DK, kDecay>;
+    if (p_next != qi + 1 || qi + 1 >= nB) return;
+    const int st1 = (jj + 1) % L::STAGES, b1 = (nbq + 1) & 1;
+    if (mbar_try_wait(&sm.xf[st1], ((jj + 1) / L::STAGES) & 1) &&
+        mbar_try_wait(&sm.pv_done[b1], (((nbq + 1) >> 1) & 1) ^ 1)) {
+        issue_p<DK, kDecay>(smem, sm, cx, tmem, jj + 1, nbq + 1);
+        ++p_next;
+    }
+}
+
 template <int DK, bool kDecay>
 __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                            const Ctx &cx, uint32_t tmem) {
     using L = Layout<DK, kDecay>;
-    constexpr uint32_t idP = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t idPV = idesc_bf16(128, NX, 0, 1);  // Pt [V | 1]
     constexpr uint32_t idQS = idesc_bf16(128, NX, 0, 1);  // phi(Q) [S | z]
     constexpr uint32_t idSU = idesc_bf16(128, NX, 1, 1);  // phi(K)^T [V | 1]
     constexpr uint32_t lboA = DK == 128 ? 16384 : 0;      // d=64: rows 64..127 alias
+    constexpr int NOB = OBufs<kDecay>::n;
+    // chunk order: P~V first where the look-back and state epilogue are the
+    // longer latency (d = 64); phi(Q) [S | z] first where the feature-map
+    // ring is (d = 128, two stages) and with decay (one O buffer)
+    constexpr bool kPVFirst = !kDecay && DK == 64;
     const uint32_t sb = smem_u32(smem + L::OFF_SB);
     const uint32_t onesx = smem_u32(smem + L::OFF_ONESX);
     int j = 0, nb = 0, nsb = 0, tl = 0;
@@ -215,8 +275,9 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         if (it.hasA) {
-            wait_bar(&sm.sb_ready, nsb & 1, cx);
-            ++nsb;
+            // phase A: the segment's local state.  S's columns are free: the
+            // previous item read them before its last sb_ready.  Phase-A
+            // stages have no output, so both of their releases come from here.
             for (int c = it.c0; c < it.c1; ++c, ++j) {
                 const int st = j % L::STAGES;
                 wait_bar(&sm.xf[st], (j / L::STAGES) & 1, cx);
@@ -230,58 +291,99 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                            (c > it.c0 || ks > 0) ? 1u : 0u);
                 if (c == it.c1 - 1) mma_commit(&sm.s_full);
                 mma_commit(&sm.empty[st]);
+                mma_commit(&sm.empty[st]);
             }
         }
-        for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
-            const int st = j % L::STAGES;
-            wait_bar(&sm.xf[st], (j / L::STAGES) & 1, cx);
-            wait_bar(&sm.pv_done, (nb & 1) ^ 1, cx);
-            tc_fence_after();
+        // phase B.  The state after the item's last chunk is never read, so
+        // that chunk has no state update.
+        const int nB = it.c1 - it.c0;
+        int p_next = 0;  // first B chunk of the item whose P is not issued
+        for (int qi = 0; qi < nB; ++qi) {
+            const int jj = j + qi, nbq = nb + qi;
+            const int st = jj % L::STAGES, b = nbq & 1;
+            const bool su = qi + 1 < nB;
+            if (p_next == qi) {
+                issue_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq);
+                ++p_next;
+            }
             const uint32_t qb = smem_u32(smem + st * L::STAGE + L::OFF_Q);
             const uint32_t kb = smem_u32(smem + st * L::STAGE + L::OFF_K);
             const uint32_t vb = smem_u32(smem + st * L::STAGE + L::OFF_V);
-            // P = phi(Q) phi(K)^T
-            for (int ks = 0; ks < DK / 16; ++ks) {
-                const uint32_t off = kmajor_off(ks, 16384);
-                mma_ss(tmem + TM_P, sdesc_sw128(qb + off, 16, 1024),
-                       sdesc_sw128(kb + off, 16, 1024), idP, ks > 0 ? 1u : 0u);
-            }
-            mma_commit(&sm.pfull);
-            wait_bar(&sm.sb_ready, nsb & 1, cx);
-            ++nsb;
-            wait_bar(&sm.o_empty, (nb & 1) ^ 1, cx);
-            tc_fence_after();
-            // inter-chunk read: phi(Q) [S | z]
-            for (int ks = 0; ks < DK / 16; ++ks)
-                mma_ss(tmem + (kDecay ? TM_OQS : TM_O),
-                       sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
-                       sdesc_sw128(sb + ks * 2048, L::SBLK, 1024), idQS,
-                       ks > 0 ? 1u : 0u);
-            // state update: phi(K)^T [V | 1], or phi(K)^T [Vhat | w] (decay;
-            // Vhat is written once phi(Q) has been consumed)
-            uint32_t vsu = vb, lsu = onesx - vb;
-            if (kDecay) {
-                mma_commit(&sm.qs_done);
-                wait_bar(&sm.vhat_ready, nb & 1, cx);
+            const int ob = NOB == 2 ? (nbq & 1) : 0;
+            const uint32_t tob = TM_O + 80u * ob;
+            wait_bar(&sm.o_empty[ob], ((NOB == 2 ? (nbq >> 1) : nbq) & 1) ^ 1, cx);
+            if (kPVFirst) {
+                // The state-independent half first: P~V(j) and P(j+1) fill
+                // the tensor pipe while the state epilogue (or, for the
+                // item's first chunk, the look-back) prepares [S | z].
+                wait_bar(&sm.pt_ready[b], (nbq >> 1) & 1, cx);
                 tc_fence_after();
-                vsu = vhat_base<DK, kDecay>(smem, st);
-                lsu = 16384;
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_ts(tmem + tob, tmem + TM_P + 128u * b + ks * 8,
+                           sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV,
+                           ks > 0 ? 1u : 0u);
+                mma_commit(&sm.pv_done[b]);
+                try_issue_next_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
+                wait_bar(&sm.sb_ready, nsb & 1, cx);
+                ++nsb;
+                tc_fence_after();
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    mma_ss(tmem + tob, sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
+                           sdesc_sw128(sb + ks * 2048, L::SBLK, 1024), idQS, 1u);
+                if (su) {
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
+                               sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idSU, 1u);
+                    mma_commit(&sm.s_full);
+                }
+                mma_commit(&sm.o_full[ob]);
+            } else {
+                // The state-dependent half first: phi(Q) [S | z] and the
+                // state update run while the score epilogue works on P(j).
+                wait_bar(&sm.sb_ready, nsb & 1, cx);
+                ++nsb;
+                tc_fence_after();
+                // inter-chunk read (with decay into its own accumulator: it
+                // is scaled per row by g^(i+1) in the output epilogue)
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    mma_ss(tmem + (kDecay ? TM_OQS : tob),
+                           sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
+                           sdesc_sw128(sb + ks * 2048, L::SBLK, 1024), idQS,
+                           ks > 0 ? 1u : 0u);
+                // state update phi(K)^T [V | 1], or phi(K)^T [Vhat | w] with
+                // decay (Vhat is written once phi(Q) has been consumed)
+                uint32_t vsu = vb, lsu = onesx - vb;
+                if (kDecay) {
+                    mma_commit(&sm.qs_done);
+                    wait_bar(&sm.vhat_ready, nbq & 1, cx);
+                    tc_fence_after();
+                    vsu = vhat_base<DK, kDecay>(smem, st);
+                    lsu = 16384;
+                }
+                if (su) {
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
+                               sdesc_sw128(vsu + ks * 2048, lsu, 1024), idSU, 1u);
+                    mma_commit(&sm.s_full);
+                }
+                try_issue_next_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
+                wait_bar(&sm.pt_ready[b], (nbq >> 1) & 1, cx);
+                tc_fence_after();
+                // intra-chunk: P~ [V | 1] (P~ read from TMEM)
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_ts(tmem + tob, tmem + TM_P + 128u * b + ks * 8,
+                           sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV,
+                           (kDecay && ks == 0) ? 0u : 1u);
+                mma_commit(&sm.o_full[ob]);
+                mma_commit(&sm.pv_done[b]);
             }
-            for (int ks = 0; ks < C / 16; ++ks)
-                mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
-                       sdesc_sw128(vsu + ks * 2048, lsu, 1024), idSU, 1u);
-            mma_commit(&sm.s_full);
-            wait_bar(&sm.pt_ready, nb & 1, cx);
-            tc_fence_after();
-            // intra-chunk: Pt [V | 1] (Pt read from TMEM)
-            for (int ks = 0; ks < C / 16; ++ks)
-                mma_ts(tmem + TM_O, tmem + TM_P + ks * 8,
-                       sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV,
-                       (kDecay && ks == 0) ? 0u : 1u);
-            mma_commit(&sm.o_full);
-            mma_commit(&sm.pv_done);
+            // the stage: one release per consumer (the output epilogue
+            // releases it itself when the output is staged in its Q slot)
             mma_commit(&sm.empty[st]);
+            if (L::OWN_OST) mma_commit(&sm.empty[st]);
         }
+        j += nB;
+        nb += nB;
     }
 }
 
@@ -404,55 +506,48 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
     }
 }
 
-// ---------------------------------------------------------------- epilogue E
+// ---------------------------------------------------------------- score epilogue
 
+// Causal mask and decay on P (fp32, TMEM), rounded to bf16 in place (the A
+// operand of P~V).  One thread per row i (= TMEM lane).
 template <int DK, bool kDecay>
-__device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
-                         const Ctx &cx, const DecayArgs &dk, uint32_t tmem,
-                         const CUtensorMap *to) {
-    using L = Layout<DK, kDecay>;
+__device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
+                               const DecayArgs &dk, uint32_t tmem) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int et = threadIdx.x - kWarpE * 32;
+    const int et = threadIdx.x - kWarpE1 * 32;
     const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);
-    int j = 0, nb = 0, tl = 0;
+    int nb = 0, tl = 0;
     for (;;) {
-        const int t = pop_item(sm, tl, cx, BAR_E, 128, et == 0);
+        const int t = pop_item(sm, tl, cx, BAR_E1, 128, et == 0);
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         if (kDecay) {
             if (et < 32) sm.gtab[et] = gpow(lg, et);
-            named_bar_sync(BAR_E, 128);
+            named_bar_sync(BAR_E1, 128);
         }
-        const float wq = kDecay ? gpow(lg, row + 1) : 1.f;
-        if (it.hasA)
-            for (int c = it.c0; c < it.c1; ++c, ++j) {
-                const int st = j % L::STAGES;
-                wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
-                if (et == 0) mbar_arrive(&sm.empty[st]);
-            }
-        for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
-            const int st = j % L::STAGES;
-            // ---- scores: causal mask, decay, bf16 into TMEM (in place)
-            wait_bar(&sm.pfull, nb & 1, cx);
+        for (int c = it.c0; c < it.c1; ++c, ++nb) {
+            const int b = nb & 1;
+            const uint32_t tp = lb + TM_P + 128u * b;
+            wait_bar(&sm.pfull[b], (nb >> 1) & 1, cx);
             tc_fence_after();
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
+            for (int blk = 0; blk < 4; ++blk) {
                 uint32_t pk[16];
-                if (b > q) {
+                if (blk > q) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) pk[e] = 0u;
                 } else {
                     uint32_t v[32];
-                    tmem_ld32(lb + TM_P + 32 * b, v);
+                    tmem_ld32(tp + 32 * blk, v);
                     tmem_wait_ld();
                     reg_fence(v);
-                    if (b < q) {
+                    if (blk < q) {
                         if (kDecay) {
-                            // g^(row - j) = g^(row - 32b - 31) g^(31 - e)
-                            const float base = gpow(lg, row - 32 * b - 31);
+                            // g^(row - j) = g^(row - 32 blk - 31) g^(31 - e)
+                            const float base = gpow(lg, row - 32 * blk - 31);
 #pragma unroll
                             for (int e = 0; e < 32; e += 2)
                                 pk[e >> 1] = pack_bf16x2(
@@ -478,71 +573,101 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
                         }
                     }
                 }
-                tmem_st16(lb + TM_P + 16 * b, pk);
+                tmem_st16(tp + 16 * blk, pk);
             }
             tmem_wait_st();
             tc_fence_before();
-            named_bar_sync(BAR_E, 128);
-            if (et == 0) mbar_arrive(&sm.pt_ready);
-
-            // ---- output: (O + g^(i+1) O_inter) / (den + g^(i+1) den_inter)
-            wait_bar(&sm.o_full, nb & 1, cx);
-            tc_fence_after();
-            uint32_t dreg = tmem_ld1(lb + TM_O + DV);
-            uint32_t direg = kDecay ? tmem_ld1(lb + TM_OQS + DV) : 0u;
-            uint32_t packed[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t o[32];
-                tmem_ld32(lb + TM_O + 32 * h, o);
-                if (kDecay) {
-                    uint32_t oi[32];
-                    tmem_ld32(lb + TM_OQS + 32 * h, oi);
-                    tmem_wait_ld();
-                    reg_fence(o);
-                    reg_fence(oi);
-                    reg_fence(dreg);
-                    reg_fence(direg);
-                    const float inv = 1.f / fmaf(wq, u2f(direg), u2f(dreg));
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2)
-                        packed[16 * h + (e >> 1)] =
-                            pack_bf16x2(fmaf(wq, u2f(oi[e]), u2f(o[e])) * inv,
-                                        fmaf(wq, u2f(oi[e + 1]), u2f(o[e + 1])) * inv);
-                } else {
-                    tmem_wait_ld();
-                    reg_fence(o);
-                    reg_fence(dreg);
-                    const float inv = 1.f / u2f(dreg);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2)
-                        packed[16 * h + (e >> 1)] =
-                            pack_bf16x2(u2f(o[e]) * inv, u2f(o[e + 1]) * inv);
-                }
-            }
-            tc_fence_before();
-            named_bar_sync(BAR_E, 128);
-            if (et == 0) mbar_arrive(&sm.o_empty);
-            uint8_t *stage_o = smem + st * L::STAGE + L::OFF_Q;  // Q slot is dead
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(stage_o + sw128_offset(row, ch * 8)) =
-                    make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2],
-                               packed[4 * ch + 3]);
-            fence_async_shared();
-            named_bar_sync(BAR_E, 128);
-            if (et == 0) {
-                tma_store_3d(to, stage_o, 64 * it.half, c * C, it.bh);
-                tma_store_commit();
-                tma_store_wait_read<0>();
-                mbar_arrive(&sm.empty[st]);
-            }
+            mbar_arrive(&sm.pt_ready[b]);  // 128 arrivals, one per row
         }
     }
-    if (et == 0) tma_store_wait_all<0>();
 }
 
-// ---------------------------------------------------------------- state S
+// One chunk's output: (O + g^(i+1) O_inter) / (den + g^(i+1) den_inter),
+// bf16 into the stage's (dead) Q slot, TMA store.  With several stages the
+// stage is released when the next store is issued (the store has read it by
+// then), so the store never stalls this warpgroup.
+template <int DK, bool kDecay>
+__device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
+                                             const Ctx &cx, uint32_t lb,
+                                             int row, int et, float wq,
+                                             const Item &it, int c, int j,
+                                             int nb, int &pend,
+                                             const CUtensorMap *to) {
+    using L = Layout<DK, kDecay>;
+    constexpr bool kDefer = !L::OWN_OST && L::STAGES >= 3;
+    const int st = j % L::STAGES;
+    const int ob = OBufs<kDecay>::n == 2 ? (nb & 1) : 0;
+    const uint32_t tob = TM_O + 80u * ob;
+    uint8_t *stage_o = L::OWN_OST ? smem + L::OFF_OST : smem + st * L::STAGE + L::OFF_Q;
+    if (L::OWN_OST) {  // the previous chunk's store must have read the buffer
+        if (et == 0) tma_store_wait_read<0>();
+        named_bar_sync(BAR_E2, 128);
+    }
+    wait_bar(&sm.o_full[ob], (OBufs<kDecay>::n == 2 ? (nb >> 1) : nb) & 1, cx);
+    tc_fence_after();
+    uint32_t dreg = tmem_ld1(lb + tob + DV);
+    uint32_t direg = kDecay ? tmem_ld1(lb + TM_OQS + DV) : 0u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t o[32];
+        tmem_ld32(lb + tob + 32 * h, o);
+        float inv;
+        if (kDecay) {
+            uint32_t oi[32];
+            tmem_ld32(lb + TM_OQS + 32 * h, oi);
+            tmem_wait_ld();
+            reg_fence(o);
+            reg_fence(oi);
+            reg_fence(dreg);
+            reg_fence(direg);
+            inv = 1.f / fmaf(wq, u2f(direg), u2f(dreg));
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                o[e] = __float_as_uint(fmaf(wq, u2f(oi[e]), u2f(o[e])));
+        } else {
+            tmem_wait_ld();
+            reg_fence(o);
+            reg_fence(dreg);
+            inv = 1.f / u2f(dreg);
+        }
+        if (h == 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.o_empty[ob]);  // 128 arrivals: O has been read
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+            *reinterpret_cast<uint4 *>(stage_o + sw128_offset(row, 32 * h + ch * 8)) =
+                make_uint4(pack_bf16x2(u2f(o[8 * ch]) * inv, u2f(o[8 * ch + 1]) * inv),
+                           pack_bf16x2(u2f(o[8 * ch + 2]) * inv, u2f(o[8 * ch + 3]) * inv),
+                           pack_bf16x2(u2f(o[8 * ch + 4]) * inv, u2f(o[8 * ch + 5]) * inv),
+                           pack_bf16x2(u2f(o[8 * ch + 6]) * inv, u2f(o[8 * ch + 7]) * inv));
+    }
+    fence_async_shared();
+    named_bar_sync(BAR_E2, 128);
+    if (et == 0) {
+        tma_store_3d(to, stage_o, 64 * it.half, c * C, it.bh);
+        tma_store_commit();
+        if (L::OWN_OST) {
+            // the stage was released by the MMA issuer
+        } else if (kDefer) {
+            if (pend >= 0) {
+                tma_store_wait_read<1>();
+                mbar_arrive(&sm.empty[pend]);
+            }
+            pend = st;
+        } else {
+            tma_store_wait_read<0>();
+            mbar_arrive(&sm.empty[st]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- output + state
+
+// Output epilogue (O / den, bf16, TMA store) and state epilogue (bf16 [S | z]
+// operand of the next chunk, decay rescale, segment publication and
+// look-back) on one warpgroup.  Per chunk j the state of chunk j+1 is
+// prepared first (it gates the next phi(Q) [S | z]), then chunk j's output.
 
 // Writes bf16 values of one 32-column half of S row `a` into block 0 of the
 // [S | z] operand (MN-major, K = a rows).
@@ -572,45 +697,226 @@ __device__ __forceinline__ void tmem_put_z(uint32_t taddr, float z) {
     tmem_st16(taddr, v);
 }
 
+// State-epilogue thread mapping.  For d = 64 the state accumulator's lanes
+// 64..127 hold a copy of rows 0..63 (the A operand's rows alias), so lanes
+// 0..63 take columns 0..31 and lanes 64..127 columns 32..63 of the same
+// rows, and every thread of the warpgroup has work; for d = 128 each lane is
+// one row and takes both 32-column halves.  z goes with column half 0.
+template <int DK>
+struct SMap {
+    static constexpr int NH = DK == 64 ? 1 : 2;  // halves per thread
+    int a, h0;
+    bool hasz;
+    __device__ __forceinline__ explicit SMap(int lane)
+        : a(DK == 64 ? (lane & 63) : lane), h0(DK == 64 ? (lane >> 6) : 0),
+          hasz(DK == 64 ? lane < 64 : true) {}
+};
+
+// Decoupled look-back, step 1 (one warp): lane k watches segment seg-1-k.
+// The predecessors to combine run back from seg-1 to the nearest one that
+// has published its inclusive prefix (or to segment 0), and each of them
+// must have published at least its local aggregate.  The count and each
+// one's flag are left in shared memory for the warpgroup.  A chain longer
+// than 32 waits for one of the 32 nearest to publish its inclusive prefix
+// (each does, in segment order, so the wait ends).  With `wait` false it
+// looks once and leaves -1 if the chain is not decided yet.
+__device__ __forceinline__ void resolve_lookback(Small &sm, const Params &p,
+                                                 const Item &it, const Ctx &cx,
+                                                 int lane, bool wait) {
+    if (it.seg == 0) {
+        if (lane == 0) sm.lb_n = 0;
+        return;
+    }
+    const int k = it.seg - 1 - lane;
+    const int *fp = p.flags + item_index(it.bh, k < 0 ? 0 : k, it.half, p);
+    const long long dl = clock64() + cx.timeout;
+    int f = FLAG_INCL, n = 0;
+    for (;;) {
+        f = k < 0 ? FLAG_INCL : load_flag(fp);
+        const unsigned stop = __ballot_sync(~0u, f >= FLAG_INCL);
+        const unsigned ready = __ballot_sync(~0u, f >= FLAG_AGG);
+        if (stop) {
+            const int ls = __ffs(stop) - 1;
+            const unsigned need = (2u << ls) - 1u;  // lanes 0..ls
+            if ((ready & need) == need) {
+                n = it.seg - 1 - ls < 0 ? ls : ls + 1;
+                break;
+            }
+        }
+        if (!wait) {
+            n = -1;
+            break;
+        }
+        const bool ab = __any_sync(~0u, *cx.abort != 0);
+        const bool late = __shfl_sync(~0u, (int)(clock64() > dl), 0) != 0;
+        if (ab || late) {
+            if (late && !ab && lane == 0)
+                raise_timeout(cx, 0x80000u | ((uint32_t)(reinterpret_cast<uintptr_t>(fp) >> 2) & 0x7FFFFu));
+            break;
+        }
+        __nanosleep(64);
+    }
+    if (lane < n) sm.lb_flag[lane] = f;
+    if (lane == 0) sm.lb_n = n;
+}
+
+// Look-back, step 2 (every thread): its 32 columns (half h) of row a of
+// sum_m g^(L m) state(seg-1-m) over the decided predecessors, and z[a].
 template <int DK, bool kDecay>
-__device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
-                           const Ctx &cx, const DecayArgs &dk, uint32_t tmem) {
+__device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
+                                             const Item &it, int nlb, int a,
+                                             int h, bool zh, float gL,
+                                             float (&acc)[32], float &accz) {
     using L = Layout<DK, kDecay>;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+    accz = 0.f;
+    float w = 1.f;
+    for (int m = 0; m < nlb; ++m) {
+        const int pi = item_index(it.bh, it.seg - 1 - m, it.half, p);
+        const float *src =
+            (sm.lb_flag[m] == FLAG_INCL ? p.incl : p.agg) + (size_t)pi * L::STATE;
+        const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV + 32 * h);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 u = __ldcg(s4 + e);
+            acc[4 * e] = fmaf(w, u.x, acc[4 * e]);
+            acc[4 * e + 1] = fmaf(w, u.y, acc[4 * e + 1]);
+            acc[4 * e + 2] = fmaf(w, u.z, acc[4 * e + 2]);
+            acc[4 * e + 3] = fmaf(w, u.w, acc[4 * e + 3]);
+        }
+        if (zh) accz = fmaf(w, __ldcg(src + DK * DV + a), accz);
+        w *= gL;
+    }
+}
+
+// A thread's fp32 slot for half hh of its look-back sum, parked in the
+// [S | z] operand buffer (idle between an item's start and its phase B):
+// one 128-byte row of the buffer, the one the thread itself rewrites in
+// bf16 afterwards where possible (d = 128: block hh, row a; d = 64: block
+// 1 - h0, row a, shared with the row's other thread, so there the rewrite
+// waits for a barrier).  16-byte pieces rotate with the row (no bank
+// conflicts).
+template <int DK>
+__device__ __forceinline__ float4 *lb_slot(uint8_t *sb, int a, int h0, int hh) {
+    const int blk = DK == 128 ? hh : 1 - h0;
+    return reinterpret_cast<float4 *>(sb + blk * (DK * 128) + a * 128);
+}
+
+// Row a of block 1 of the [S | z] operand: z[a] in column 0, zero elsewhere.
+__device__ __forceinline__ void store_zrow(uint8_t *sb_z, int a, float z) {
+    uint4 *row = reinterpret_cast<uint4 *>(sb_z + a * 128);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+    store_zb(sb_z, a, z);
+}
+
+template <int DK, bool kDecay>
+__device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
+                             const Ctx &cx, const DecayArgs &dk, uint32_t tmem,
+                             const CUtensorMap *to) {
+    using L = Layout<DK, kDecay>;
+    using SM = SMap<DK>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;
-    const int a = q * 32 + lane;  // key-feature row of S (= TMEM lane)
-    const int et = threadIdx.x - kWarpS * 32;
-    const bool act = a < DK;      // warp-uniform
-    const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);
+    const int et = threadIdx.x - kWarpE2 * 32;
+    const int ln = q * 32 + lane;  // the TMEM lane this thread may access
+    const SM sm_map(ln);
+    const int a = sm_map.a, h0 = sm_map.h0;
+    const bool hasz = sm_map.hasz;
+    const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);  // lanes of this warp
     uint8_t *sb = smem + L::OFF_SB;
     uint8_t *sbz = sb + L::SBLK;
-    int tl = 0, ns = 0;
-    bool pending = false;
+    const int row = ln;  // output row i
+    int tl = 0, ns = 0, j = 0, nb = 0, pend = -1;
     for (;;) {
-        const int t = pop_item(sm, tl, cx, BAR_S, 128, et == 0);
+        const int t = pop_item(sm, tl, cx, BAR_E2, 128, et == 0);
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         const float gL = gpow(lg, p.seg_chunks * C);
-        if (pending) {
-            wait_bar(&sm.s_full, ns & 1, cx);
-            ++ns;
-            pending = false;
-        }
-        tc_fence_after();
+        const float wq = kDecay ? gpow(lg, row + 1) : 1.f;
         float *agg = p.agg + (size_t)t * L::STATE;
         float *incl = p.incl + (size_t)t * L::STATE;
+        const int n0 = min(C, p.N - it.c0 * C);
+        const float f0 = gpow(lg, n0);
+        // Look-back, first try: if the predecessors have already published,
+        // sum their states now, while phase A runs, into the threads' slots.
+        bool early = false;
+        float accz_e = 0.f;
         if (it.hasA) {
-            // S's TMEM columns are free for this item's phase A
-            tc_fence_before();
-            named_bar_sync(BAR_S, 128);
-            if (et == 0) mbar_arrive(&sm.sb_ready);
+            if (warp == kWarpE2) resolve_lookback(sm, p, it, cx, lane, false);
+            named_bar_sync(BAR_E2, 128);
+            const int nlb = sm.lb_n;
+            early = nlb >= 0;
+            if (early) {
+#pragma unroll 1
+                for (int hh = 0; hh < SM::NH; ++hh) {
+                    float acc[32], accz;
+                    lookback_sum<DK, kDecay>(sm, p, it, nlb, a, h0 + hh,
+                                             hasz && hh == 0, gL, acc, accz);
+                    if (hh == 0) accz_e = accz;
+                    float4 *slot = lb_slot<DK>(sb, a, h0, hh);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        slot[e ^ (a & 7)] = make_float4(acc[4 * e], acc[4 * e + 1],
+                                                        acc[4 * e + 2], acc[4 * e + 3]);
+                }
+            }
+            j += it.c1 - it.c0;  // the phase-A jobs (released by the MMA issuer)
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
             tc_fence_after();
-            if (act) {
+        }
+        if (early) {
+            // inclusive prefix = g^L S_start + local state, and the phase-B
+            // start state; the prefix is published without an aggregate
+#pragma unroll 1
+            for (int hh = 0; hh < SM::NH; ++hh) {
+                const int h = h0 + hh;
+                const bool zh = hasz && hh == 0;
+                float acc[32];
+                const float4 *slot = lb_slot<DK>(sb, a, h0, hh);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int e = 0; e < 8; ++e) {
+                    const float4 u = slot[e ^ (a & 7)];
+                    acc[4 * e] = u.x;
+                    acc[4 * e + 1] = u.y;
+                    acc[4 * e + 2] = u.z;
+                    acc[4 * e + 3] = u.w;
+                }
+                uint32_t v[32];
+                tmem_ld32(lb + TM_S + 32 * h, v);
+                tmem_wait_ld();
+                reg_fence(v);
+                float4 *dst = reinterpret_cast<float4 *>(incl + a * DV + 32 * h);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(fmaf(gL, acc[4 * e], u2f(v[4 * e])),
+                                         fmaf(gL, acc[4 * e + 1], u2f(v[4 * e + 1])),
+                                         fmaf(gL, acc[4 * e + 2], u2f(v[4 * e + 2])),
+                                         fmaf(gL, acc[4 * e + 3], u2f(v[4 * e + 3])));
+                if (zh) {
+                    uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                    tmem_wait_ld();
+                    reg_fence(zl);
+                    incl[DK * DV + a] = fmaf(gL, accz_e, u2f(zl));
+                    tmem_put_z(lb + TM_S + DV, f0 * accz_e);
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f0 * acc[e]);
+                tmem_st32(lb + TM_S + 32 * h, v);
+                if (DK == 64) named_bar_sync(BAR_E2, 128);  // every slot read
+                store_sb_half(sb, a, h, acc);
+                tmem_wait_st();
+            }
+            if (hasz) store_zrow(sbz, a, accz_e);
+        } else {
+            if (it.hasA) {
+                // publish the segment's local state (its aggregate)
+#pragma unroll
+                for (int hh = 0; hh < SM::NH; ++hh) {
+                    const int h = h0 + hh;
                     uint32_t v[32];
                     tmem_ld32(lb + TM_S + 32 * h, v);
                     tmem_wait_ld();
@@ -621,49 +927,29 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                         dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
                                              u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
                 }
-                uint32_t zl = tmem_ld1(lb + TM_S + DV);
-                tmem_wait_ld();
-                reg_fence(zl);
-                agg[DK * DV + a] = u2f(zl);
-            }
-            __threadfence();
-            named_bar_sync(BAR_S, 128);
-            if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
-        }
-        // look-back over this segment's predecessors, one 32-column half of
-        // S at a time; then the inclusive prefix and the phase-B start state
-        const int n0 = min(C, p.N - it.c0 * C);
-        const float f0 = gpow(lg, n0);
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-            float acc[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-            float accz = 0.f;
-            float w = 1.f;
-            for (int s2 = it.seg - 1; s2 >= 0; --s2) {
-                const int pi = item_index(it.bh, s2, it.half, p);
-                const int f = poll_flag_at_least(p.flags + pi, FLAG_AGG, FLAG_INCL, cx);
-                const float *src =
-                    (f == FLAG_INCL ? p.incl : p.agg) + (size_t)pi * L::STATE;
-                if (act) {
-                    const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV + 32 * h);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 u = __ldcg(s4 + e);
-                        acc[4 * e] = fmaf(w, u.x, acc[4 * e]);
-                        acc[4 * e + 1] = fmaf(w, u.y, acc[4 * e + 1]);
-                        acc[4 * e + 2] = fmaf(w, u.z, acc[4 * e + 2]);
-                        acc[4 * e + 3] = fmaf(w, u.w, acc[4 * e + 3]);
-                    }
-                    if (h == 0) accz = fmaf(w, __ldcg(src + DK * DV + a), accz);
+                if (hasz) {
+                    uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                    tmem_wait_ld();
+                    reg_fence(zl);
+                    agg[DK * DV + a] = u2f(zl);
                 }
-                if (f == FLAG_INCL) break;
-                w *= gL;
+                __threadfence();
+                named_bar_sync(BAR_E2, 128);
+                if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
             }
-            if (act) {
+            // look-back, waiting for the predecessors
+            if (warp == kWarpE2) resolve_lookback(sm, p, it, cx, lane, true);
+            named_bar_sync(BAR_E2, 128);
+            const int nlb = sm.lb_n;
+#pragma unroll 1
+            for (int hh = 0; hh < SM::NH; ++hh) {
+                const int h = h0 + hh;
+                const bool zh = hasz && hh == 0;
+                float acc[32], accz;
+                lookback_sum<DK, kDecay>(sm, p, it, nlb, a, h, zh, gL, acc, accz);
                 if (it.hasA) {
-                    // inclusive prefix = g^L S_start + local state
+                    // inclusive prefix = g^L S_start + local state (published
+                    // below, once phase B has its start state)
                     uint32_t v[32];
                     tmem_ld32(lb + TM_S + 32 * h, v);
                     tmem_wait_ld();
@@ -675,7 +961,7 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                                              fmaf(gL, acc[4 * e + 1], u2f(v[4 * e + 1])),
                                              fmaf(gL, acc[4 * e + 2], u2f(v[4 * e + 2])),
                                              fmaf(gL, acc[4 * e + 3], u2f(v[4 * e + 3])));
-                    if (h == 0) {
+                    if (zh) {
                         uint32_t zl = tmem_ld1(lb + TM_S + DV);
                         tmem_wait_ld();
                         reg_fence(zl);
@@ -689,32 +975,34 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                 for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f0 * acc[e]);
                 tmem_st32(lb + TM_S + 32 * h, v);
                 store_sb_half(sb, a, h, acc);
-                if (h == 0) {
+                if (zh) {
                     tmem_put_z(lb + TM_S + DV, f0 * accz);
                     store_zb(sbz, a, accz);
                 }
                 tmem_wait_st();
             }
         }
-        if (it.hasA) {
-            __threadfence();
-            named_bar_sync(BAR_S, 128);
-            if (et == 0) publish_flag(p.flags + t, FLAG_INCL);
-        }
         fence_async_shared();
         tc_fence_before();
-        named_bar_sync(BAR_S, 128);
+        named_bar_sync(BAR_E2, 128);
         if (et == 0) mbar_arrive(&sm.sb_ready);
-        pending = true;
-        for (int c = it.c0 + 1; c < it.c1; ++c) {
-            wait_bar(&sm.s_full, ns & 1, cx);
-            ++ns;
-            tc_fence_after();
-            const int n = min(C, p.N - c * C);
-            const float f = gpow(lg, n);
-            if (act) {
+        if (it.hasA) {
+            __threadfence();
+            named_bar_sync(BAR_E2, 128);
+            if (et == 0) publish_flag(p.flags + t, FLAG_INCL);
+        }
+        for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
+            if (c + 1 < it.c1) {
+                // state epilogue: [S | z] of chunk c+1 as the bf16 operand,
+                // and with decay the rescale g^n of the accumulator
+                wait_bar(&sm.s_full, ns & 1, cx);
+                ++ns;
+                tc_fence_after();
+                const int n = min(C, p.N - (c + 1) * C);
+                const float f = gpow(lg, n);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int hh = 0; hh < SM::NH; ++hh) {
+                    const int h = h0 + hh;
                     uint32_t v[32];
                     tmem_ld32(lb + TM_S + 32 * h, v);
                     tmem_wait_ld();
@@ -729,23 +1017,30 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p,
                         tmem_st32(lb + TM_S + 32 * h, v);
                     }
                 }
-                uint32_t zr = tmem_ld1(lb + TM_S + DV);
-                tmem_wait_ld();
-                reg_fence(zr);
-                const float z = u2f(zr);
-                store_zb(sbz, a, z);
-                if (kDecay) {
-                    tmem_put_z(lb + TM_S + DV, f * z);
-                    tmem_wait_st();
+                if (hasz) {
+                    uint32_t zr = tmem_ld1(lb + TM_S + DV);
+                    tmem_wait_ld();
+                    reg_fence(zr);
+                    const float z = u2f(zr);
+                    store_zb(sbz, a, z);
+                    if (kDecay) tmem_put_z(lb + TM_S + DV, f * z);
                 }
+                if (kDecay) tmem_wait_st();
+                fence_async_shared();
+                tc_fence_before();
+                named_bar_sync(BAR_E2, 128);
+                if (et == 0) mbar_arrive(&sm.sb_ready);
             }
-            fence_async_shared();
-            tc_fence_before();
-            named_bar_sync(BAR_S, 128);
-            if (et == 0) mbar_arrive(&sm.sb_ready);
+            output_chunk<DK, kDecay>(smem, sm, cx, lb, row, et, wq, it, c, j, nb,
+                                     pend, to);
+        }
+        if (et == 0 && pend >= 0) {  // the item's last store: release its stage
+            tma_store_wait_read<0>();
+            mbar_arrive(&sm.empty[pend]);
+            pend = -1;
         }
     }
-    if (pending) wait_bar(&sm.s_full, ns & 1, cx);
+    if (et == 0) tma_store_wait_all<0>();
 }
 
 // ---------------------------------------------------------------- kernel
@@ -771,11 +1066,13 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
             mbar_init(&sm.empty[s], 2);
             mbar_init(&sm.xf[s], 1);
         }
-        mbar_init(&sm.pfull, 1);
-        mbar_init(&sm.pt_ready, 1);
-        mbar_init(&sm.o_full, 1);
-        mbar_init(&sm.o_empty, 1);
-        mbar_init(&sm.pv_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.pfull[b], 1);
+            mbar_init(&sm.pt_ready[b], 128);
+            mbar_init(&sm.pv_done[b], 1);
+            mbar_init(&sm.o_full[b], 1);
+            mbar_init(&sm.o_empty[b], 128);
+        }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.sb_ready, 1);
         mbar_init(&sm.qs_done, 1);
@@ -816,12 +1113,12 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
         if (lane == 0) producer<DK, kDecay>(smem, sm, p, cx, &tq, &tk, &tv);
     } else if (warp == 1) {
         if (lane == 0) mma_issuer<DK, kDecay>(smem, sm, p, cx, tmem);
-    } else if (warp < kWarpE) {
+    } else if (warp < kWarpE1) {
         transform<DK, kDecay>(smem, sm, p, cx, dk);
-    } else if (warp < kWarpS) {
-        epilogue<DK, kDecay>(smem, sm, p, cx, dk, tmem, &to);
+    } else if (warp < kWarpE2) {
+        score_epilogue<DK, kDecay>(sm, p, cx, dk, tmem);
     } else {
-        state_role<DK, kDecay>(smem, sm, p, cx, dk, tmem);
+        output_state<DK, kDecay>(smem, sm, p, cx, dk, tmem, &to);
     }
 
     tc_fence_before();
@@ -836,7 +1133,9 @@ constexpr size_t smem_bytes() {
 }
 
 static_assert(smem_bytes<128, true>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<128, false>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<64, true>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<64, false>() <= 232448, "shared memory budget");
 
 }  // namespace causal_tc
 

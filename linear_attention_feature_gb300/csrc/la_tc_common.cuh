@@ -46,17 +46,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Reads a published-state flag (acquire, device scope).
+__device__ __forceinline__ int load_flag(const int *f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
 // Bounded poll until *f >= want; returns the value seen (or `give_up` once
 // aborted or timed out).
 __device__ __forceinline__ int poll_flag_at_least(const int *f, int want,
                                                   int give_up, const Ctx &cx) {
     const long long dl = clock64() + cx.timeout;
     for (;;) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
-                     : "=r"(v)
-                     : "l"(f)
-                     : "memory");
+        const int v = load_flag(f);
         if (v >= want) return v;
         if (*cx.abort) return give_up;
         if (clock64() > dl) {
