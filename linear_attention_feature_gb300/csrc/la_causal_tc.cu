@@ -1127,6 +1127,19 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
     if (warp == 1) tmem_dealloc(tmem, TM_COLS);
 }
 
+// Automatic segment length.  Without decay: the wave rule (per-item
+// overhead about three chunk times, measured).  With decay the per-chunk
+// time grows once a wave's phase-A loads of K and V no longer stay in L2
+// until phase B re-reads them, so segments stay short: about three items
+// per SM, 2..8 chunks.
+template <bool kDecay>
+int auto_segment_chunks(long long heads, int nchunks, int sms) {
+    if (!kDecay) return tchost::wave_segment_chunks(heads, nchunks, sms, 3);
+    const long long units = heads * nchunks;
+    const long long want = (units + 3LL * sms - 1) / (3LL * sms);
+    return (int)(want < 2 ? 2 : (want > 8 ? 8 : want));
+}
+
 template <int DK, bool kDecay>
 constexpr size_t smem_bytes() {
     return (size_t)Layout<DK, kDecay>::OFF_SMALL + sizeof(Small) + 1024;
@@ -1167,13 +1180,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.N = N;
     p.nchunks = (N + C - 1) / C;
     p.nhalf = DK / DV;
-    if (seg_chunks <= 0) {
-        // ~3 items per SM, segments of 2..8 chunks (the phase-A loads of K
-        // and V then stay in L2 until phase B re-reads them)
-        long long units = (long long)BH * p.nchunks * p.nhalf;
-        long long want = (units + 3LL * sms - 1) / (3LL * sms);
-        seg_chunks = (int)(want < 2 ? 2 : (want > 8 ? 8 : want));
-    }
+    if (seg_chunks <= 0) seg_chunks = auto_segment_chunks<kDecay>(BH * p.nhalf, p.nchunks, sms);
     p.seg_chunks = seg_chunks;
     p.nseg = (p.nchunks + seg_chunks - 1) / seg_chunks;
     long long items = (long long)BH * p.nseg * p.nhalf;
@@ -1305,9 +1312,7 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     p.N = N;
     p.nchunks = (N + C - 1) / C;
     p.nhalf = DK / DV;
-    long long units = (long long)BH * p.nchunks * p.nhalf;
-    long long want = (units + 3LL * sms - 1) / (3LL * sms);
-    int seg = (int)(want < 2 ? 2 : (want > 8 ? 8 : want));
+    int seg = auto_segment_chunks<kDecay>(BH * p.nhalf, p.nchunks, sms);
     // lengthen segments until the workspace fits the static scratch
     size_t off_agg = 0, off_incl = 0, total = 0;
     long long items = 0;

@@ -504,11 +504,9 @@ TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
     p.nchunks = (N + C - 1) / C;
     p.nhalf = DK / DV;
     const long long heads = (long long)BH * p.nhalf;
-    const long long units = heads * p.nchunks;
-    // about two items per SM in each pass
-    int per = (int)((units + 2LL * sms - 1) / (2LL * sms));
-    if (per < 1) per = 1;
-    if (seg_chunks > 0) per = seg_chunks;
+    // segment length by the wave rule (per-item overhead about three chunk
+    // times, measured)
+    int per = seg_chunks > 0 ? seg_chunks : tchost::wave_segment_chunks(heads, p.nchunks, sms, 3);
     p.seg1 = p.grp2 = per;
     p.nseg1 = p.ngrp2 = (p.nchunks + per - 1) / per;
     const long long items = heads * p.nseg1;

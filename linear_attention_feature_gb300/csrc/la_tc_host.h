@@ -67,5 +67,26 @@ inline cudaError_t sm_count(int *out) {
     return cudaSuccess;
 }
 
+// Chunks per sequence segment for the persistent tensor-core kernels.  A
+// work item is one segment of one head (and value half), and the one-CTA-
+// per-SM grid takes items in waves of `sms`.  The length chosen minimises
+//   ceil(items / sms) * (segment length + overhead),
+// with `overhead` the per-item cost (state publication, look-back) in chunk
+// times; a head in one segment has none.  Longer segments win ties.
+inline int wave_segment_chunks(long long heads, int nchunks, int sms, int overhead) {
+    int best = nchunks;
+    long long best_cost = -1;
+    for (int len = nchunks; len >= 1; --len) {
+        const long long nseg = (nchunks + len - 1) / len;
+        const long long waves = (heads * nseg + sms - 1) / sms;
+        const long long cost = waves * (len + (nseg > 1 ? overhead : 0));
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = len;
+        }
+    }
+    return best;
+}
+
 }  // namespace tchost
 }  // namespace la
