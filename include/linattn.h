@@ -17,8 +17,9 @@
  * scaling and no epsilon in the denominator (phi > 0 makes it positive).
  *
  * Conventions shared by every entry point
- *   - All tensor pointers are DEVICE pointers owned by the caller; the
- *     library never frees or retains them after the call is enqueued.
+ *   - All tensor pointers are DEVICE pointers owned by the caller (except
+ *     la_forward_host's, which are host pointers); the library never frees
+ *     or retains them after the call is enqueued.
  *   - Sequences are row-major contiguous [B][H][N][d] (d fastest); decode
  *     inputs are [B][H][d]; states S are [B][H][d][d] with S[a][c],
  *     a = key-feature index, c = value index; normalisers z are [B][H][d].
@@ -35,6 +36,8 @@
  */
 #ifndef LINATTN_H
 #define LINATTN_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -102,6 +105,49 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
                         void *out, int B, int H, int N, int d, int causal,
                         const float *decay, la_dtype dtype, int path,
                         int segment_chunks, la_stream_t stream);
+
+/*
+ * la_forward_host -- la_forward on HOST buffers (the one entry point whose
+ * tensors are host pointers).  The pages define only the operation (as for
+ * la_forward); moving the data to and from the GPU has no counterpart there.
+ * The call copies q, k, v to a caller-provided device workspace, runs the
+ * forward there and copies out back, split into at most 4 groups of heads so
+ * that the host-to-device copy of one group, the kernels of the one before
+ * and the device-to-host copy of the one before that overlap (two copy
+ * streams owned by the library, one per direction, created on first use).
+ *
+ *   q, k, v   [B][H][N][d] host, dtype `dtype`, read only.  Page-locked
+ *             memory (cudaHostAlloc, cudaHostRegister, torch pin_memory)
+ *             gives asynchronous full-speed copies; pageable memory works,
+ *             but the driver stages its copies and the call then blocks.
+ *   out       [B][H][N][d] host, written; may not alias q, k or v.
+ *   B, H, N, d, causal, decay, dtype   as la_forward (decay is a host
+ *             array of H floats, read during the call).
+ *   workspace device buffer, 256-byte aligned, of at least
+ *             la_forward_host_workspace_bytes(B, H, N, d, dtype) bytes,
+ *             owned by the caller; it holds the device copies of q, k, v and
+ *             out and must not be used by anything else until `stream` has
+ *             passed the call.
+ *   stream    the copies start after the work already enqueued on `stream`;
+ *             `stream` continues only after the last output copy, so out is
+ *             complete once `stream` reaches work enqueued after the call
+ *             (e.g. cudaStreamSynchronize(stream)).
+ *
+ * Errors: validation as la_forward (LA_ERR_INVALID_ARG also for a missing,
+ * unaligned or too small workspace); a failure part-way through returns its
+ * status with `stream` still ordered after the copies already enqueued, and
+ * out unspecified.  Calls on one device are serialised on the host while
+ * they enqueue (the copy streams and their events are shared).
+ */
+la_status la_forward_host(const void *q, const void *k, const void *v,
+                          void *out, int B, int H, int N, int d, int causal,
+                          const float *decay, la_dtype dtype, void *workspace,
+                          size_t workspace_bytes, la_stream_t stream);
+
+/* Device workspace bytes la_forward_host needs for this problem (0 for an
+ * invalid shape or dtype). */
+size_t la_forward_host_workspace_bytes(int B, int H, int N, int d,
+                                       la_dtype dtype);
 
 /*
  * la_decode_step -- one recurrent decode step per head: with

@@ -14,7 +14,8 @@ import os
 
 from . import build as _build
 
-__all__ = ["forward", "decode_step", "check_device_status",
+__all__ = ["forward", "forward_host", "host_workspace_bytes", "decode_step",
+           "check_device_status",
            "kernel_launch_count", "LinAttnError",
            "load_library", "LA_F32", "LA_BF16", "STATUS", "EXPORTED"]
 
@@ -25,7 +26,8 @@ STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED",
 EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_check_device_status", "la_status_string", "la_last_error",
             "la_abi_version", "la_kernel_launch_count",
-            "la_forward_causal_noalloc")
+            "la_forward_causal_noalloc", "la_forward_host",
+            "la_forward_host_workspace_bytes")
 
 _lib = None
 
@@ -51,6 +53,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.la_forward.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V]
     lib.la_forward_ex.argtypes = [V, V, V, V, I, I, I, I, I, F, I, I, I, V]
     lib.la_decode_step.argtypes = [V, V, V, V, V, V, I, I, I, I, V]
+    lib.la_forward_host.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V,
+                                    ctypes.c_size_t, V]
+    lib.la_forward_host_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.la_forward_host_workspace_bytes.restype = ctypes.c_size_t
     lib.la_check_device_status.argtypes = [V]
     lib.la_status_string.argtypes = [I]
     lib.la_status_string.restype = ctypes.c_char_p
@@ -59,7 +65,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.la_abi_version.argtypes = []
     lib.la_kernel_launch_count.argtypes = []
     lib.la_kernel_launch_count.restype = ctypes.c_ulonglong
-    for n in ("la_forward", "la_forward_ex", "la_decode_step",
+    for n in ("la_forward", "la_forward_ex", "la_decode_step", "la_forward_host",
               "la_check_device_status", "la_abi_version"):
         getattr(lib, n).restype = I
     if path is None:
@@ -179,3 +185,55 @@ def check_device_status(stream=None, device=None):
     with torch.cuda.device(dev):
         st = load_library().la_check_device_status(_stream_ptr(stream, dev))
     _raise_if(st)
+
+
+def host_workspace_bytes(shape, dtype) -> int:
+    """Device workspace bytes that forward_host needs for [B, H, N, d]."""
+    torch = _torch()
+    code = LA_BF16 if dtype == torch.bfloat16 else LA_F32 if dtype == torch.float32 else -1
+    if code < 0:
+        raise TypeError(f"unsupported dtype {dtype} (float32 or bfloat16)")
+    B, H, N, d = (int(x) for x in shape)
+    return int(load_library().la_forward_host_workspace_bytes(B, H, N, d, code))
+
+
+def forward_host(q, k, v, causal: bool = True, decay=None, out=None, *,
+                 workspace=None, device=None, stream=None):
+    """forward() on HOST tensors q, k, v [B, H, N, d] (page-locked for full
+    speed): the library copies them to the GPU, runs the forward and copies
+    the result into `out` (a host tensor, allocated page-locked if None),
+    pipelined over groups of heads.  `workspace` is a uint8 CUDA tensor of at
+    least host_workspace_bytes(q.shape, q.dtype) bytes (allocated if None).
+    The call is asynchronous: `out` is complete once `stream` (default: the
+    current stream of `device`) has passed it, e.g. after
+    torch.cuda.current_stream().synchronize()."""
+    torch = _torch()
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("forward_host takes contiguous host tensors")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if out.is_cuda or not out.is_contiguous() or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must be a contiguous host tensor like q")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = host_workspace_bytes(q.shape, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    B, H, N, d = q.shape
+    lib = load_library()
+    with torch.cuda.device(workspace.device):
+        st = lib.la_forward_host(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            B, H, N, d, int(bool(causal)), _decay_arg(decay, H),
+            _dtype_code(q), ctypes.c_void_p(workspace.data_ptr()),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+            _stream_ptr(stream, workspace.device))
+    _raise_if(st)
+    return out

@@ -8,6 +8,7 @@
 
 #include "la_internal.h"
 #include "la_tc.h"
+#include "la_tc_host.h"
 
 namespace la {
 
@@ -115,6 +116,26 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
                         void *out, int B, int H, int N, int d, int causal,
                         const float *decay, la_dtype dtype, int path,
                         int segment_chunks, la_stream_t stream) {
+    return la::forward_with_workspace(q, k, v, out, B, H, N, d, causal, decay,
+                                      dtype, path, segment_chunks, nullptr, 0,
+                                      stream);
+}
+
+__attribute__((visibility("default")))
+la_status la_forward(const void *q, const void *k, const void *v, void *out,
+                     int B, int H, int N, int d, int causal,
+                     const float *decay, la_dtype dtype, la_stream_t stream) {
+    return la_forward_ex(q, k, v, out, B, H, N, d, causal, decay, dtype, 0, 0,
+                         stream);
+}
+
+}  // extern "C"
+
+la_status la::forward_with_workspace(const void *q, const void *k, const void *v,
+                                     void *out, int B, int H, int N, int d,
+                                     int causal, const float *decay,
+                                     la_dtype dtype, int path, int segment_chunks,
+                                     void *ws, size_t ws_bytes, la_stream_t stream) {
     DecayArgs dk;
     la_status st = validate_forward(q, k, v, out, B, H, N, d, causal, decay,
                                     dtype, &dk);
@@ -138,7 +159,7 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
         int *status = device_status_word(&ce);
         if (!status) return cuda_fail(ce, "la_forward: status word");
         TcResult r = tc_forward(q, k, v, out, sh, causal, dk, segment_chunks,
-                                status, s);
+                                status, ws, ws_bytes, s);
         if (r.status != LA_OK) {
             if (r.status == LA_ERR_CUDA) return cuda_fail(r.cuda, r.where);
             return fail(r.status, r.where);
@@ -151,13 +172,16 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
     return LA_OK;
 }
 
-__attribute__((visibility("default")))
-la_status la_forward(const void *q, const void *k, const void *v, void *out,
-                     int B, int H, int N, int d, int causal,
-                     const float *decay, la_dtype dtype, la_stream_t stream) {
-    return la_forward_ex(q, k, v, out, B, H, N, d, causal, decay, dtype, 0, 0,
-                         stream);
+size_t la::forward_workspace_bytes(int B, int H, int N, int d, int causal,
+                                   bool decay, la_dtype dtype) {
+    FwdShape sh{B, H, N, d};
+    if (dtype != LA_BF16 || (d != 64 && d != 128)) return 0;  // CUDA-core path
+    int sms = 0;
+    if (tchost::sm_count(&sms) != cudaSuccess || sms <= 0) sms = 1;
+    return tc_workspace_bytes(sh, causal, decay, 0, sms);
 }
+
+extern "C" {
 
 __attribute__((visibility("default")))
 la_status la_decode_step(float *S, float *z, const void *q, const void *k,

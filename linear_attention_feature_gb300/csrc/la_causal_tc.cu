@@ -1156,12 +1156,40 @@ namespace {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Work decomposition and workspace layout of one causal launch.
+struct CausalPlan {
+    int seg_chunks, nseg, nchunks, nhalf;
+    long long items;
+    size_t off_flags, off_agg, off_incl, total;
+};
+
+template <int DK, bool kDecay>
+CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms) {
+    using namespace causal_tc;
+    using L = Layout<DK, kDecay>;
+    CausalPlan pl{};
+    pl.nchunks = (sh.N + C - 1) / C;
+    pl.nhalf = DK / DV;
+    if (seg_chunks <= 0)
+        seg_chunks = auto_segment_chunks<kDecay>(sh.BH() * pl.nhalf, pl.nchunks, sms);
+    pl.seg_chunks = seg_chunks;
+    pl.nseg = (pl.nchunks + seg_chunks - 1) / seg_chunks;
+    pl.items = sh.BH() * pl.nseg * pl.nhalf;
+    // workspace: control words, flags, published states
+    pl.off_flags = 256;
+    pl.off_agg = align_up(pl.off_flags + sizeof(int) * (size_t)pl.items, 256);
+    const size_t state_bytes = (pl.nseg > 1) ? sizeof(float) * L::STATE * (size_t)pl.items : 0;
+    pl.off_incl = align_up(pl.off_agg + state_bytes, 256);
+    pl.total = pl.off_incl + state_bytes;
+    return pl;
+}
+
 template <int DK, bool kDecay>
 TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
                          const FwdShape &sh, const DecayArgs &dk, int seg_chunks,
-                         int *status, cudaStream_t stream) {
+                         int *status, void *ws_in, size_t ws_bytes,
+                         cudaStream_t stream) {
     using namespace causal_tc;
-    using L = Layout<DK, kDecay>;
     const int BH = (int)sh.BH(), N = sh.N;
     CUtensorMap tq, tk, tv, to;
     cudaError_t e;
@@ -1173,53 +1201,51 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     int sms = 0;
     if ((e = tchost::sm_count(&sms)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: device query"};
+    const CausalPlan pl = plan_causal<DK, kDecay>(sh, seg_chunks, sms);
+    if (pl.items > (1LL << 30))
+        return {LA_ERR_UNSUPPORTED, cudaSuccess, "la_forward: too many work items"};
 
     Params p{};
     p.BH = BH;
     p.H = sh.H;
     p.N = N;
-    p.nchunks = (N + C - 1) / C;
-    p.nhalf = DK / DV;
-    if (seg_chunks <= 0) seg_chunks = auto_segment_chunks<kDecay>(BH * p.nhalf, p.nchunks, sms);
-    p.seg_chunks = seg_chunks;
-    p.nseg = (p.nchunks + seg_chunks - 1) / seg_chunks;
-    long long items = (long long)BH * p.nseg * p.nhalf;
-    if (items > (1LL << 30))
-        return {LA_ERR_UNSUPPORTED, cudaSuccess, "la_forward: too many work items"};
-    p.items = (int)items;
+    p.nchunks = pl.nchunks;
+    p.nhalf = pl.nhalf;
+    p.seg_chunks = pl.seg_chunks;
+    p.nseg = pl.nseg;
+    p.items = (int)pl.items;
     p.timeout = 1LL << 32;
 
-    // workspace: control words, flags, published states
-    const size_t off_flags = 256;
-    const size_t off_agg = align_up(off_flags + sizeof(int) * items, 256);
-    const size_t state_bytes = (p.nseg > 1) ? sizeof(float) * L::STATE * items : 0;
-    const size_t off_incl = align_up(off_agg + state_bytes, 256);
-    const size_t total = off_incl + state_bytes;
-    void *ws = nullptr;
-    if ((e = cudaMallocAsync(&ws, total, stream)) != cudaSuccess)
+    // the caller's workspace when given, else a stream-ordered allocation
+    void *ws = ws_in;
+    if (ws) {
+        if (ws_bytes < pl.total)
+            return {LA_ERR_INVALID_ARG, cudaSuccess, "la_forward: workspace too small"};
+    } else if ((e = cudaMallocAsync(&ws, pl.total, stream)) != cudaSuccess) {
         return {LA_ERR_NO_MEMORY, e, "la_forward: workspace allocation"};
+    }
     char *w8 = static_cast<char *>(ws);
     p.ctrl = reinterpret_cast<int *>(w8);
-    p.flags = reinterpret_cast<int *>(w8 + off_flags);
-    p.agg = reinterpret_cast<float *>(w8 + off_agg);
-    p.incl = reinterpret_cast<float *>(w8 + off_incl);
+    p.flags = reinterpret_cast<int *>(w8 + pl.off_flags);
+    p.agg = reinterpret_cast<float *>(w8 + pl.off_agg);
+    p.incl = reinterpret_cast<float *>(w8 + pl.off_incl);
     p.status = status;
-    e = cudaMemsetAsync(ws, 0, off_agg, stream);
+    e = tc_zero_words(ws, pl.off_agg, stream);
     if (e == cudaSuccess) {
         const size_t smem = smem_bytes<DK, kDecay>();
         auto kern = causal_kernel<DK, kDecay>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e == cudaSuccess) {
-            const int grid = (int)(items < sms ? items : sms);
+            const int grid = (int)(pl.items < sms ? pl.items : sms);
             kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p, dk);
             e = cudaGetLastError();
         }
     }
-    cudaError_t ef = cudaFreeAsync(ws, stream);
+    cudaError_t ef = ws_in ? cudaSuccess : cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return {LA_ERR_CUDA, e, "la_forward: causal kernel launch"};
     if (ef != cudaSuccess) return {LA_ERR_CUDA, ef, "la_forward: workspace free"};
-    note_launches(1);
+    note_launches(2);  // workspace clear + forward
     return {LA_OK, cudaSuccess, ""};
 }
 
@@ -1227,12 +1253,21 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
 
 TcResult launch_causal_tc(const void *q, const void *k, const void *v,
                           void *out, const FwdShape &sh, const DecayArgs &dk,
-                          int seg_chunks, int *status, cudaStream_t stream) {
+                          int seg_chunks, int *status, void *ws, size_t ws_bytes,
+                          cudaStream_t stream) {
     if (sh.d == 128)
-        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, stream)
-                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, stream);
-    return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, stream)
-                  : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, stream);
+        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream)
+                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream);
+    return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream)
+                  : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream);
+}
+
+size_t causal_tc_workspace_bytes(const FwdShape &sh, bool decay, int seg_chunks, int sms) {
+    if (sh.d == 128)
+        return decay ? plan_causal<128, true>(sh, seg_chunks, sms).total
+                     : plan_causal<128, false>(sh, seg_chunks, sms).total;
+    return decay ? plan_causal<64, true>(sh, seg_chunks, sms).total
+                 : plan_causal<64, false>(sh, seg_chunks, sms).total;
 }
 
 }  // namespace la
@@ -1340,7 +1375,7 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     p.incl = reinterpret_cast<float *>(scratch + off_incl);
     p.status = status;
     // the counter and flags must start at zero; the states need no clearing
-    if ((e = cudaMemsetAsync(scratch, 0, off_agg, stream)) != cudaSuccess)
+    if ((e = tc_zero_words(scratch, off_agg, stream)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: clearing flags"};
     const size_t smem = smem_bytes<DK, kDecay>();
     auto kern = causal_kernel<DK, kDecay>;
@@ -1351,7 +1386,7 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p, dk);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel launch"};
-    note_launches(1);
+    note_launches(2);  // flag clear + forward
     return {LA_OK, cudaSuccess, ""};
 }
 

@@ -50,4 +50,17 @@ void note_launches(int n);
 // Records the detail returned by la_last_error() on the calling thread.
 void set_last_error(const char *msg);
 
+// la_forward_ex with an optional caller-owned scratch for the tensor-core
+// kernels (ws = NULL: they allocate it stream-ordered themselves).
+la_status forward_with_workspace(const void *q, const void *k, const void *v,
+                                 void *out, int B, int H, int N, int d,
+                                 int causal, const float *decay, la_dtype dtype,
+                                 int path, int segment_chunks, void *ws,
+                                 size_t ws_bytes, la_stream_t stream);
+
+// Scratch bytes forward_with_workspace needs (automatic path and segment
+// length; 0 where the CUDA-core kernels run, which need none).
+size_t forward_workspace_bytes(int B, int H, int N, int d, int causal,
+                               bool decay, la_dtype dtype);
+
 }  // namespace la

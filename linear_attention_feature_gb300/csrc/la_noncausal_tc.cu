@@ -481,12 +481,41 @@ namespace {
 
 inline size_t nc_align(size_t x) { return (x + 255) / 256 * 256; }
 
+// Work decomposition and workspace layout of one non-causal launch.
+struct NcPlan {
+    int per, nseg, nchunks, nhalf;
+    long long heads, items;
+    size_t off_cnt, off_flag, off_part, off_fin, total;
+};
+
+template <int DK>
+NcPlan plan_noncausal(const FwdShape &sh, int seg_chunks, int sms) {
+    using namespace noncausal_tc;
+    using L = Layout<DK>;
+    NcPlan pl{};
+    pl.nchunks = (sh.N + C - 1) / C;
+    pl.nhalf = DK / DV;
+    pl.heads = sh.BH() * pl.nhalf;
+    // segment length by the wave rule (per-item overhead about three chunk
+    // times, measured)
+    pl.per = seg_chunks > 0 ? seg_chunks
+                            : tchost::wave_segment_chunks(pl.heads, pl.nchunks, sms, 3);
+    pl.nseg = (pl.nchunks + pl.per - 1) / pl.per;
+    pl.items = pl.heads * pl.nseg;
+    pl.off_cnt = 256;
+    pl.off_flag = nc_align(pl.off_cnt + sizeof(int) * (size_t)pl.heads);
+    pl.off_part = nc_align(pl.off_flag + sizeof(int) * (size_t)pl.heads);
+    pl.off_fin = nc_align(pl.off_part + sizeof(float) * L::STATE * (size_t)pl.items);
+    pl.total = pl.off_fin + sizeof(float) * L::STATE * (size_t)pl.heads;
+    return pl;
+}
+
 template <int DK>
 TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
                             void *out, const FwdShape &sh, int seg_chunks,
-                            int *status, cudaStream_t stream) {
+                            int *status, void *ws_in, size_t ws_bytes,
+                            cudaStream_t stream) {
     using namespace noncausal_tc;
-    using L = Layout<DK>;
     const int BH = (int)sh.BH(), N = sh.N;
     CUtensorMap tq, tk, tv, to;
     cudaError_t e;
@@ -498,54 +527,50 @@ TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
     int sms = 0;
     if ((e = tchost::sm_count(&sms)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: device query"};
+    const NcPlan pl = plan_noncausal<DK>(sh, seg_chunks, sms);
+    if (pl.items > (1LL << 29))
+        return {LA_ERR_UNSUPPORTED, cudaSuccess, "la_forward: too many work items"};
     Params p{};
     p.BH = BH;
     p.N = N;
-    p.nchunks = (N + C - 1) / C;
-    p.nhalf = DK / DV;
-    const long long heads = (long long)BH * p.nhalf;
-    // segment length by the wave rule (per-item overhead about three chunk
-    // times, measured)
-    int per = seg_chunks > 0 ? seg_chunks : tchost::wave_segment_chunks(heads, p.nchunks, sms, 3);
-    p.seg1 = p.grp2 = per;
-    p.nseg1 = p.ngrp2 = (p.nchunks + per - 1) / per;
-    const long long items = heads * p.nseg1;
-    if (items > (1LL << 29))
-        return {LA_ERR_UNSUPPORTED, cudaSuccess, "la_forward: too many work items"};
-    p.items1 = p.items2 = (int)items;
+    p.nchunks = pl.nchunks;
+    p.nhalf = pl.nhalf;
+    p.seg1 = p.grp2 = pl.per;
+    p.nseg1 = p.ngrp2 = pl.nseg;
+    p.items1 = p.items2 = (int)pl.items;
     p.timeout = 1LL << 32;
-    const size_t off_cnt = 256;
-    const size_t off_flag = nc_align(off_cnt + sizeof(int) * heads);
-    const size_t off_part = nc_align(off_flag + sizeof(int) * heads);
-    const size_t off_fin = nc_align(off_part + sizeof(float) * L::STATE * items);
-    const size_t total = off_fin + sizeof(float) * L::STATE * heads;
-    void *ws = nullptr;
-    if ((e = cudaMallocAsync(&ws, total, stream)) != cudaSuccess)
+    // the caller's workspace when given, else a stream-ordered allocation
+    void *ws = ws_in;
+    if (ws) {
+        if (ws_bytes < pl.total)
+            return {LA_ERR_INVALID_ARG, cudaSuccess, "la_forward: workspace too small"};
+    } else if ((e = cudaMallocAsync(&ws, pl.total, stream)) != cudaSuccess) {
         return {LA_ERR_NO_MEMORY, e, "la_forward: workspace allocation"};
+    }
     char *w8 = static_cast<char *>(ws);
     p.ctrl = reinterpret_cast<int *>(w8);
-    p.cnt = reinterpret_cast<int *>(w8 + off_cnt);
-    p.fflag = reinterpret_cast<int *>(w8 + off_flag);
-    p.part = reinterpret_cast<float *>(w8 + off_part);
-    p.fin = reinterpret_cast<float *>(w8 + off_fin);
+    p.cnt = reinterpret_cast<int *>(w8 + pl.off_cnt);
+    p.fflag = reinterpret_cast<int *>(w8 + pl.off_flag);
+    p.part = reinterpret_cast<float *>(w8 + pl.off_part);
+    p.fin = reinterpret_cast<float *>(w8 + pl.off_fin);
     p.status = status;
-    e = cudaMemsetAsync(ws, 0, off_part, stream);
+    e = tc_zero_words(ws, pl.off_part, stream);
     if (e == cudaSuccess) {
         const size_t smem = smem_bytes<DK>();
         auto kern = noncausal_kernel<DK>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e == cudaSuccess) {
-            const long long all = 2 * items;
+            const long long all = 2 * pl.items;
             const int grid = (int)(all < sms ? all : sms);
             kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p);
             e = cudaGetLastError();
         }
     }
-    cudaError_t ef = cudaFreeAsync(ws, stream);
+    cudaError_t ef = ws_in ? cudaSuccess : cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return {LA_ERR_CUDA, e, "la_forward: non-causal kernel launch"};
     if (ef != cudaSuccess) return {LA_ERR_CUDA, ef, "la_forward: workspace free"};
-    note_launches(1);
+    note_launches(2);  // workspace clear + forward
     return {LA_OK, cudaSuccess, ""};
 }
 
@@ -553,10 +578,16 @@ TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
 
 TcResult launch_noncausal_tc(const void *q, const void *k, const void *v,
                              void *out, const FwdShape &sh, int seg_chunks,
-                             int *status, cudaStream_t stream) {
+                             int *status, void *ws, size_t ws_bytes,
+                             cudaStream_t stream) {
     if (sh.d == 128)
-        return launch_noncausal_t<128>(q, k, v, out, sh, seg_chunks, status, stream);
-    return launch_noncausal_t<64>(q, k, v, out, sh, seg_chunks, status, stream);
+        return launch_noncausal_t<128>(q, k, v, out, sh, seg_chunks, status, ws, ws_bytes, stream);
+    return launch_noncausal_t<64>(q, k, v, out, sh, seg_chunks, status, ws, ws_bytes, stream);
+}
+
+size_t noncausal_tc_workspace_bytes(const FwdShape &sh, int seg_chunks, int sms) {
+    return sh.d == 128 ? plan_noncausal<128>(sh, seg_chunks, sms).total
+                       : plan_noncausal<64>(sh, seg_chunks, sms).total;
 }
 
 }  // namespace la

@@ -20,11 +20,39 @@ bool tc_supported(const FwdShape &sh, la_dtype dtype, int causal,
 
 TcResult tc_forward(const void *q, const void *k, const void *v, void *out,
                     const FwdShape &sh, int causal, const DecayArgs &dk,
-                    int segment_chunks, int *status, cudaStream_t stream) {
+                    int segment_chunks, int *status, void *ws, size_t ws_bytes,
+                    cudaStream_t stream) {
     if (causal)
         return launch_causal_tc(q, k, v, out, sh, dk, segment_chunks, status,
-                                stream);
-    return launch_noncausal_tc(q, k, v, out, sh, segment_chunks, status, stream);
+                                ws, ws_bytes, stream);
+    return launch_noncausal_tc(q, k, v, out, sh, segment_chunks, status, ws,
+                               ws_bytes, stream);
+}
+
+size_t tc_workspace_bytes(const FwdShape &sh, int causal, bool decay,
+                          int segment_chunks, int sms) {
+    if (sh.BH() == 0 || sh.N == 0) return 0;
+    return causal ? causal_tc_workspace_bytes(sh, decay, segment_chunks, sms)
+                  : noncausal_tc_workspace_bytes(sh, segment_chunks, sms);
+}
+
+namespace {
+
+__global__ void zero_words_kernel(uint4 *p, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+}  // namespace
+
+cudaError_t tc_zero_words(void *p, size_t bytes, cudaStream_t stream) {
+    const size_t n = bytes / 16;
+    if (n == 0) return cudaSuccess;
+    const size_t want = (n + 255) / 256;
+    const int blocks = (int)(want < 152 ? want : 152);
+    zero_words_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint4 *>(p), n);
+    return cudaGetLastError();
 }
 
 }  // namespace la

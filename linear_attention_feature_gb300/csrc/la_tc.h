@@ -19,18 +19,38 @@ bool tc_supported(const FwdShape &sh, la_dtype dtype, int causal,
 
 // Enqueues the tensor-core forward on `stream`.  `segment_chunks` = 0 picks
 // the segment length automatically.  `status` is the device status word.
+// `ws` (ws_bytes >= tc_workspace_bytes, 256-byte aligned) is the kernels'
+// scratch; NULL makes the launch allocate it stream-ordered
+// (cudaMallocAsync / cudaFreeAsync on `stream`).
 TcResult tc_forward(const void *q, const void *k, const void *v, void *out,
                     const FwdShape &sh, int causal, const DecayArgs &dk,
-                    int segment_chunks, int *status, cudaStream_t stream);
+                    int segment_chunks, int *status, void *ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
+// Scratch bytes one tensor-core forward needs on a device with `sms` SMs.
+size_t tc_workspace_bytes(const FwdShape &sh, int causal, bool decay,
+                          int segment_chunks, int sms);
+
+// Zeroes `bytes` (a multiple of 16, 16-byte aligned) of device memory with a
+// small kernel on `stream`.  The kernels' workspaces (ticket counters and
+// flags) are cleared this way rather than with cudaMemsetAsync: a memset can
+// be queued on a copy engine behind unrelated copies of other streams (for
+// example the input copies of la_forward_host), which would hold the kernel
+// back until they finish.
+cudaError_t tc_zero_words(void *p, size_t bytes, cudaStream_t stream);
 
 // Non-causal two-pass kernel (la_noncausal_tc.cu).
 TcResult launch_noncausal_tc(const void *q, const void *k, const void *v,
                              void *out, const FwdShape &sh, int seg_chunks,
-                             int *status, cudaStream_t stream);
+                             int *status, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+size_t noncausal_tc_workspace_bytes(const FwdShape &sh, int seg_chunks, int sms);
 
 // Chunkwise causal kernel (la_causal_tc.cu).
 TcResult launch_causal_tc(const void *q, const void *k, const void *v,
                           void *out, const FwdShape &sh, const DecayArgs &dk,
-                          int seg_chunks, int *status, cudaStream_t stream);
+                          int seg_chunks, int *status, void *ws, size_t ws_bytes,
+                          cudaStream_t stream);
+size_t causal_tc_workspace_bytes(const FwdShape &sh, bool decay, int seg_chunks, int sms);
 
 }  // namespace la

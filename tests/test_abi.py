@@ -1,7 +1,8 @@
 """The C-ABI library builds, loads and exports what include/linattn.h
 declares, and its host-side argument checks reject bad calls before anything
 touches a GPU (these tests need no GPU: every call here returns during
-validation, so no CUDA call is made)."""
+validation, so nothing is enqueued; the workspace-size query asks the CUDA
+runtime for the SM count and falls back to one SM without a device)."""
 import ctypes
 import os
 import re
@@ -128,3 +129,52 @@ def test_python_binding_refuses_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         la.load_library(str(tmp_path / "nope.so"))
+
+
+WS = ctypes.c_void_p(0x100000)  # 256-byte aligned, never dereferenced
+
+
+def fwd_host(lib, q=P, k=P2, v=P3, out=OUT, B=1, H=2, N=8, d=64, causal=1,
+             decay=None, dtype=1, ws=WS, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.la_forward_host_workspace_bytes(B, H, N, d, dtype)
+    return lib.la_forward_host(q, k, v, out, B, H, N, d, causal, decay, dtype,
+                               ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw, code, msg", [
+    (dict(q=None), INVALID, "null"),
+    (dict(out=None), INVALID, "null"),
+    (dict(B=-1, ws_bytes=0), INVALID, "negative"),
+    (dict(d=0, ws_bytes=0), INVALID, "d must"),
+    (dict(d=300, ws_bytes=0), INVALID, "d must"),
+    (dict(causal=2), INVALID, "causal"),
+    (dict(dtype=7, ws_bytes=0), INVALID, "dtype"),
+    (dict(out=P2), INVALID, "alias"),
+    (dict(causal=0, decay=floats(0.5, 0.5)), INVALID, "causal form only"),
+    (dict(decay=floats(0.5, 2.0)), INVALID, "[0, 1]"),
+    (dict(ws=None), INVALID, "workspace"),
+    (dict(ws_bytes=1024), INVALID, "workspace"),
+    (dict(ws=ctypes.c_void_p(0x100010)), INVALID, "aligned"),
+])
+def test_forward_host_rejects_bad_arguments(lib, kw, code, msg):
+    assert fwd_host(lib, **kw) == code
+    assert msg in lib.la_last_error().decode()
+
+
+def test_forward_host_workspace_size_and_empty_problems(lib):
+    # q, k, v, out (each rounded up to 256 bytes), plus the kernels' scratch
+    # on the tensor-core path (none on the CUDA-core path)
+    assert lib.la_forward_host_workspace_bytes(4, 16, 4096, 64, 1) > 4 * 4 * 16 * 4096 * 64 * 2
+    assert lib.la_forward_host_workspace_bytes(1, 1, 3, 3, 0) == 4 * 256
+    assert lib.la_forward_host_workspace_bytes(1, 1, 3, 0, 0) == 0
+    assert lib.la_forward_host_workspace_bytes(1, 1, 3, 3, 9) == 0
+    assert fwd_host(lib, B=0, ws=None, ws_bytes=0) == OK
+    assert fwd_host(lib, N=0, ws=None, ws_bytes=0) == OK
+
+
+def test_forward_host_python_binding_refuses_strided_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 4)
+    with pytest.raises(ValueError, match="contiguous host"):
+        la.forward_host(q.transpose(2, 3), q.clone(), q.clone())
