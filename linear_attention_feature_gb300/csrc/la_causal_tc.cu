@@ -10,12 +10,13 @@
 //   O      = Pt V + diag(g^(i+1)) phi(Q) S         (tcgen05; Pt read from TMEM)
 //   den    = Pt 1 + diag(g^(i+1)) phi(Q) z
 //   out_i  = O_i / den_i
-//   S     <- g^n S + phi(K)^T Vhat,  Vhat_t = g^(n-1-t) v_t   (n = chunk length)
-//   z     <- g^n z + phi(K)^T w,     w_t = g^(n-1-t)
+//   S     <- g^n S + Khat^T V,  Khat_t = g^(n-1-t) phi(k_t)   (n = chunk length)
+//   z     <- g^n z + Khat^T 1
 // A tcgen05.mma costs about the same for any N up to 128, so the normaliser
 // rides along as a 65th column of the wide products: phi(Q) [S | z],
-// Pt [V | 1] and phi(K)^T [Vhat | w] are single N = 80 MMAs (the extra
-// 64-column operand block holds z, ones or w in its first column).  S and z
+// Pt [V | 1] and Khat^T [V | 1] are single N = 80 MMAs (the extra 64-column
+// operand block holds z or ones in its first column).  With decay the K rows
+// are rescaled into Khat in place once P has read them.  S and z
 // are carried in TMEM in fp32 and copied to shared memory in bf16 as the B
 // operand of the next chunk's phi(Q) [S | z], so numerator and denominator
 // are formed from the same bf16 operands.  The feature
@@ -86,7 +87,7 @@ struct Params {
 template <int DK, bool kDecay>
 struct Layout {
     static constexpr int KB = DK / 64;
-    static constexpr int STAGES = DK == 128 ? 2 : (kDecay ? 3 : 4);
+    static constexpr int STAGES = DK == 128 ? 2 : 4;
     static constexpr int TILE = DK * C * 2;   // a Q or K tile (bf16)
     static constexpr int VTILE = C * DV * 2;  // a V (or O) tile half
     static constexpr int STAGE = 2 * TILE + VTILE;
@@ -100,16 +101,11 @@ struct Layout {
     // second N block of the V operand (reached through the descriptor LBO)
     static constexpr int OFF_ONESX = OFF_SB + SB;
     static constexpr int ONESX = 16384;
-    // [Vhat | w] with decay: for d = 128 it lives in the stage's Q slot once
-    // phi(Q) is consumed; for d = 64 in its own buffer
-    static constexpr bool VHAT_IN_Q = DK == 128;
-    static constexpr int OFF_VHAT_OWN = OFF_ONESX + ONESX;
-    static constexpr int VHAT_OWN = (kDecay && !VHAT_IN_Q) ? 2 * 16384 : 0;
     // output staging: a buffer of its own where shared memory allows (a
     // stage is then free once its last product completes), else the stage's
     // Q slot, dead by the time the chunk's output is ready
-    static constexpr bool OWN_OST = DK == 128 || kDecay;
-    static constexpr int OFF_OST = OFF_VHAT_OWN + VHAT_OWN;
+    static constexpr bool OWN_OST = DK == 128;
+    static constexpr int OFF_OST = OFF_ONESX + ONESX;
     static constexpr int OST = OWN_OST ? C * DV * 2 : 0;
     static constexpr int OFF_SMALL = OFF_OST + OST;
     static constexpr int STATE = DK * DV + DK;
@@ -120,7 +116,7 @@ struct Small {
     uint64_t full[4], empty[4], xf[4];
     uint64_t pfull[2], pt_ready[2], pv_done[2], o_full[2], o_empty[2];
     uint64_t s_full, sb_ready;
-    uint64_t qs_done, vhat_ready;
+    uint64_t khat_ready;  // with decay: the stage's K rows carry their weights
     uint64_t item_full[2], item_empty[2];
     int ring[2];
     int lb_flag[32], lb_n;  // look-back decision of the current item
@@ -206,13 +202,6 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
 }
 
 // ---------------------------------------------------------------- MMA issuer
-
-template <int DK, bool kDecay>
-__device__ __forceinline__ uint32_t vhat_base(uint8_t *smem, int st) {
-    using L = Layout<DK, kDecay>;
-    return L::VHAT_IN_Q ? smem_u32(smem + st * L::STAGE + L::OFF_Q)
-                        : smem_u32(smem + L::OFF_VHAT_OWN);
-}
 
 // P = phi(Q) phi(K)^T of job `jj` (stage jj % STAGES) into P buffer b of
 // B-chunk number `nbq`, once the chunk is transformed and the buffer's
@@ -350,20 +339,17 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                            sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
                            sdesc_sw128(sb + ks * 2048, L::SBLK, 1024), idQS,
                            ks > 0 ? 1u : 0u);
-                // state update phi(K)^T [V | 1], or phi(K)^T [Vhat | w] with
-                // decay (Vhat is written once phi(Q) has been consumed)
-                uint32_t vsu = vb, lsu = onesx - vb;
+                // state update phi(K)^T [V | 1]; with decay Khat^T [V | 1],
+                // Khat_t = g^(n-1-t) phi(k_t), the K rows being rescaled in
+                // place once P(j) has read them
                 if (kDecay) {
-                    mma_commit(&sm.qs_done);
-                    wait_bar(&sm.vhat_ready, nbq & 1, cx);
+                    wait_bar(&sm.khat_ready, nbq & 1, cx);
                     tc_fence_after();
-                    vsu = vhat_base<DK, kDecay>(smem, st);
-                    lsu = 16384;
                 }
                 if (su) {
                     for (int ks = 0; ks < C / 16; ++ks)
                         mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
-                               sdesc_sw128(vsu + ks * 2048, lsu, 1024), idSU, 1u);
+                               sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idSU, 1u);
                     mma_commit(&sm.s_full);
                 }
                 try_issue_next_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
@@ -429,6 +415,22 @@ __device__ __forceinline__ void transform_row_scaled(uint8_t *tile, int row,
     }
 }
 
+// Row `row` of a [128][DK] swizzled bf16 tile times w (this thread's half).
+template <int DK>
+__device__ __forceinline__ void scale_row(uint8_t *tile, int row, int part,
+                                          uint32_t w2) {
+    constexpr int NCH = DK / 16;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int cc = part * NCH + i;
+        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
+        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
+        *reinterpret_cast<uint4 *>(tile + off) =
+            make_uint4(bf2_mul(x.x, w2), bf2_mul(x.y, w2), bf2_mul(x.z, w2),
+                       bf2_mul(x.w, w2));
+    }
+}
+
 template <int DK, bool kDecay>
 __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                           const Ctx &cx, const DecayArgs &dk) {
@@ -472,35 +474,15 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
             if (kDecay) {
-                // [Vhat | w] with w_t = g^(n-1-t): written once phi(Q) [S | z]
-                // (which reads the Q slot) and the previous state update
-                // (which read the previous [Vhat | w]) have completed
-                wait_bar(&sm.qs_done, nb & 1, cx);
-                uint8_t *vh = smem + (L::VHAT_IN_Q ? st * L::STAGE + L::OFF_Q
-                                                   : L::OFF_VHAT_OWN);
-                const uint8_t *vt = smem + st * L::STAGE + L::OFF_V;
+                // Khat_t = g^(n-1-t) phi(k_t) in place, once P(j) (the only
+                // reader of the unweighted rows) has completed; rows past N
+                // are already zero
+                wait_bar(&sm.pfull[nb & 1], (nb >> 1) & 1, cx);
                 const float w = row < n ? gpow(lg, n - 1 - row) : 0.f;
-                const uint32_t w2 = bf2_splat(w);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t off = sw128_offset(row, (part * 4 + i) * 8);
-                    const uint4 x = *reinterpret_cast<const uint4 *>(vt + off);
-                    *reinterpret_cast<uint4 *>(vh + off) =
-                        make_uint4(bf2_mul(x.x, w2), bf2_mul(x.y, w2),
-                                   bf2_mul(x.z, w2), bf2_mul(x.w, w2));
-                }
-                // w block: column 0 = w_t, the rest zero
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int ch = part * 4 + i;
-                    const uint32_t off = sw128_offset(row, ch * 8);
-                    const uint32_t lo = (ch == 0) ? (w2 & 0xFFFFu) : 0u;
-                    *reinterpret_cast<uint4 *>(vh + 16384 + off) =
-                        make_uint4(lo, 0u, 0u, 0u);
-                }
+                scale_row<DK>(kt, row, part, bf2_splat(w));
                 fence_async_shared();
                 named_bar_sync(BAR_T, kTThreads);
-                if (et == 0) mbar_arrive(&sm.vhat_ready);
+                if (et == 0) mbar_arrive(&sm.khat_ready);
             }
         }
     }
@@ -1075,8 +1057,7 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
         }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.sb_ready, 1);
-        mbar_init(&sm.qs_done, 1);
-        mbar_init(&sm.vhat_ready, 1);
+        mbar_init(&sm.khat_ready, 1);
         for (int r = 0; r < 2; ++r) {
             mbar_init(&sm.item_full[r], 1);
             mbar_init(&sm.item_empty[r], 4);
