@@ -9,11 +9,10 @@
 // counter:
 //   pass 1 (head, segment, value half): S_seg | z_seg = phi(K)^T [V | 1] over
 //     a run of 128-token chunks (tcgen05, N = 80, the ones column gives z),
-//     written as an fp32 partial; the last segment of a head to finish (an
-//     atomic count) adds the partials in segment order -- so the result does
-//     not depend on timing -- and publishes the head's final [S | z].
-//   pass 2 (head, chunk group, value half): waits (bounded) for its head's
-//     final state, stages it in bf16 as the B operand, then per chunk
+//     written as an fp32 partial and counted in (an atomic per head).
+//   pass 2 (head, chunk group, value half): waits (bounded) until all of its
+//     head's partials are counted in, adds them in segment order -- so the
+//     result does not depend on timing -- into the bf16 B operand, then per chunk
 //     O | den = phi(Q) [S | z] (one N = 80 MMA per 16 features) into a
 //     double-buffered TMEM accumulator, out = O / den, TMA store.
 // Pass-1 tickets all precede pass-2 tickets and pass-1 items never wait, so
@@ -48,8 +47,7 @@ struct Params {
     int seg1, nseg1, items1;  // pass 1: chunks per segment, segments, items
     int grp2, ngrp2, items2;  // pass 2: chunks per group, groups, items
     float *part;              // [items1][STATE]
-    float *fin;               // [BH * nhalf][STATE]
-    int *cnt, *fflag;         // [BH * nhalf]
+    int *cnt;                 // [BH * nhalf] partials counted in
     int *ctrl;                // [0] ticket counter, [1] abort flag
     int *status;
     long long timeout;
@@ -76,7 +74,6 @@ struct Small {
     uint64_t s_full, s_free, sb_ready, o_full[2], o_empty[2];
     uint64_t item_full[2], item_empty[2];
     int ring[2];
-    int last;
     uint32_t tmem_base;
 };
 
@@ -256,7 +253,7 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
     const bool act = row < DK;      // warp-uniform
     const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);
     uint8_t *sb = smem + L::OFF_SB;
-    int j = 0, n1 = 0, nb = 0, tl = 0;
+    int j = 0, n1 = 0, nb = 0, tl = 0, pend = -1;
     for (;;) {
         const int t = pop_item(sm, tl, cx, BAR_E, 128, et == 0);
         if (t < 0) break;
@@ -294,63 +291,53 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
             named_bar_sync(BAR_E, 128);
             if (et == 0) {
                 mbar_arrive(&sm.s_free);
-                const int done = atomicAdd(p.cnt + it.hh, 1);
-                sm.last = (done == p.nseg1 - 1);
-                __threadfence();
-            }
-            named_bar_sync(BAR_E, 128);
-            if (sm.last) {
-                // the head's final [S | z]: partials added in segment order
-                float *fin = p.fin + (size_t)it.hh * L::STATE;
-                if (act) {
-                    for (int h = 0; h < 2; ++h) {
-                        float acc[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-                        float accz = 0.f;
-                        for (int s2 = 0; s2 < p.nseg1; ++s2) {
-                            const int pi = (s2 * p.BH + it.bh) * p.nhalf + it.half;
-                            const float *src = p.part + (size_t)pi * L::STATE;
-                            const float4 *s4 =
-                                reinterpret_cast<const float4 *>(src + row * DV + 32 * h);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float4 u = __ldcg(s4 + e);
-                                acc[4 * e] += u.x;
-                                acc[4 * e + 1] += u.y;
-                                acc[4 * e + 2] += u.z;
-                                acc[4 * e + 3] += u.w;
-                            }
-                            if (h == 0) accz += __ldcg(src + DK * DV + row);
-                        }
-                        float4 *d4 = reinterpret_cast<float4 *>(fin + row * DV + 32 * h);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            d4[e] = make_float4(acc[4 * e], acc[4 * e + 1],
-                                                acc[4 * e + 2], acc[4 * e + 3]);
-                        if (h == 0) fin[DK * DV + row] = accz;
-                    }
-                }
-                __threadfence();
-                named_bar_sync(BAR_E, 128);
-                if (et == 0) publish_flag(p.fflag + it.hh, 1);
+                atomicAdd(p.cnt + it.hh, 1);  // after the fence: the partial is visible
             }
             continue;
         }
-        // pass 2: stage the head's final [S | z] in bf16
-        poll_flag_at_least(p.fflag + it.hh, 1, 1, cx);
-        const float *fin = p.fin + (size_t)it.hh * L::STATE;
-        if (act) {
+        // pass 2: the head's [S | z] = sum of its partials in segment order,
+        // staged in bf16.  For d = 64 two threads share a row (32 columns
+        // each); for d = 128 each thread takes a row, both halves.
+        if (warp == kWarpE) poll_flag_at_least(p.cnt + it.hh, p.nseg1, p.nseg1, cx);
+        named_bar_sync(BAR_E, 128);
+        {
+            constexpr int NH = DK == 64 ? 1 : 2;
+            const int a = DK == 64 ? (et & 63) : et;
+            const int h0 = DK == 64 ? (et >> 6) : 0;
+#pragma unroll 1
+            for (int hh = 0; hh < NH; ++hh) {
+                const int h = h0 + hh;
+                const bool zh = h == 0;
+                float acc[32];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const float4 a0 = __ldcg(reinterpret_cast<const float4 *>(fin + row * DV + 8 * ch));
-                const float4 a1 = __ldcg(reinterpret_cast<const float4 *>(fin + row * DV + 8 * ch + 4));
-                *reinterpret_cast<uint4 *>(sb + sw128_offset(row, ch * 8)) =
-                    make_uint4(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w),
-                               pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
+                for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                float accz = 0.f;
+#pragma unroll 2
+                for (int s2 = 0; s2 < p.nseg1; ++s2) {
+                    const int pi = (s2 * p.BH + it.bh) * p.nhalf + it.half;
+                    const float *src = p.part + (size_t)pi * L::STATE;
+                    const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV + 32 * h);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 u = __ldcg(s4 + e);
+                        acc[4 * e] += u.x;
+                        acc[4 * e + 1] += u.y;
+                        acc[4 * e + 2] += u.z;
+                        acc[4 * e + 3] += u.w;
+                    }
+                    if (zh) accz += __ldcg(src + DK * DV + a);
+                }
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4 *>(sb + sw128_offset(a, 32 * h + ch * 8)) =
+                        make_uint4(pack_bf16x2(acc[8 * ch], acc[8 * ch + 1]),
+                                   pack_bf16x2(acc[8 * ch + 2], acc[8 * ch + 3]),
+                                   pack_bf16x2(acc[8 * ch + 4], acc[8 * ch + 5]),
+                                   pack_bf16x2(acc[8 * ch + 6], acc[8 * ch + 7]));
+                if (zh)
+                    *reinterpret_cast<__nv_bfloat16 *>(sb + L::SBLK + sw128_offset(a, 0)) =
+                        __float2bfloat16_rn(accz);
             }
-            *reinterpret_cast<__nv_bfloat16 *>(sb + L::SBLK + sw128_offset(row, 0)) =
-                __float2bfloat16_rn(__ldcg(fin + DK * DV + row));
         }
         fence_async_shared();
         named_bar_sync(BAR_E, 128);
@@ -377,8 +364,7 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
                         pack_bf16x2(u2f(o[e]) * inv, u2f(o[e + 1]) * inv);
             }
             tc_fence_before();
-            named_bar_sync(BAR_E, 128);
-            if (et == 0) mbar_arrive(&sm.o_empty[ob]);
+            mbar_arrive(&sm.o_empty[ob]);  // 128 arrivals: this row is read
             uint8_t *stage_o = smem + st * L::STAGE + L::OFF_V;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
@@ -390,9 +376,19 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
             if (et == 0) {
                 tma_store_3d(to, stage_o, 64 * it.half, c * C, it.bh);
                 tma_store_commit();
-                tma_store_wait_read<0>();
-                mbar_arrive(&sm.empty[st]);
+                // release the previous chunk's stage once its store has
+                // read it (one store stays in flight)
+                if (pend >= 0) {
+                    tma_store_wait_read<1>();
+                    mbar_arrive(&sm.empty[pend]);
+                }
+                pend = st;
             }
+        }
+        if (et == 0 && pend >= 0) {  // the item's last store
+            tma_store_wait_read<0>();
+            mbar_arrive(&sm.empty[pend]);
+            pend = -1;
         }
     }
     if (et == 0) tma_store_wait_all<0>();
@@ -423,7 +419,7 @@ noncausal_kernel(const __grid_constant__ CUtensorMap tq,
         mbar_init(&sm.sb_ready, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.o_full[b], 1);
-            mbar_init(&sm.o_empty[b], 1);
+            mbar_init(&sm.o_empty[b], 128);
             mbar_init(&sm.item_full[b], 1);
             mbar_init(&sm.item_empty[b], 3);  // MMA, transform, epilogue
         }
@@ -485,7 +481,7 @@ inline size_t nc_align(size_t x) { return (x + 255) / 256 * 256; }
 struct NcPlan {
     int per, nseg, nchunks, nhalf;
     long long heads, items;
-    size_t off_cnt, off_flag, off_part, off_fin, total;
+    size_t off_cnt, off_part, total;
 };
 
 template <int DK>
@@ -502,11 +498,10 @@ NcPlan plan_noncausal(const FwdShape &sh, int seg_chunks, int sms) {
                             : tchost::wave_segment_chunks(pl.heads, pl.nchunks, sms, 3);
     pl.nseg = (pl.nchunks + pl.per - 1) / pl.per;
     pl.items = pl.heads * pl.nseg;
+    // workspace: control words, per-head counts (zeroed), partial states
     pl.off_cnt = 256;
-    pl.off_flag = nc_align(pl.off_cnt + sizeof(int) * (size_t)pl.heads);
-    pl.off_part = nc_align(pl.off_flag + sizeof(int) * (size_t)pl.heads);
-    pl.off_fin = nc_align(pl.off_part + sizeof(float) * L::STATE * (size_t)pl.items);
-    pl.total = pl.off_fin + sizeof(float) * L::STATE * (size_t)pl.heads;
+    pl.off_part = nc_align(pl.off_cnt + sizeof(int) * (size_t)pl.heads);
+    pl.total = pl.off_part + sizeof(float) * L::STATE * (size_t)pl.items;
     return pl;
 }
 
@@ -550,9 +545,7 @@ TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
     char *w8 = static_cast<char *>(ws);
     p.ctrl = reinterpret_cast<int *>(w8);
     p.cnt = reinterpret_cast<int *>(w8 + pl.off_cnt);
-    p.fflag = reinterpret_cast<int *>(w8 + pl.off_flag);
     p.part = reinterpret_cast<float *>(w8 + pl.off_part);
-    p.fin = reinterpret_cast<float *>(w8 + pl.off_fin);
     p.status = status;
     e = tc_zero_words(ws, pl.off_part, stream);
     if (e == cudaSuccess) {
