@@ -199,13 +199,15 @@ def timed_steps(fn, K, W, world, flush=None):
 # one ncu capture of a kernel, keyed by kernel and workload, valid only while
 # the kernel's sources hash to the recorded digest (else reported as null).
 KNOWN_TRAFFIC = {
-    # ncu --set full --clock-control none -k regex:causal_kernel -s 3 -c 1
-    #     python bench.py --kernel-case B H N D causal
+    # ncu --set full --clock-control none -k regex:<kernel> -s 3 -c 1
+    #     python bench.py --kernel-case B H N D causal|noncausal
     # (dram__bytes_read.sum + dram__bytes_write.sum of the captured launch)
     ("causal_kernel<64,false>", "bf16_b4h16_n4096_d64"):
-        {"sources": "4048ca60f9e1dcc1", "bytes": 100793344 + 4888832},
+        {"sources": "353a2e93a1511e26", "bytes": 100781568 + 5092864},
     ("causal_kernel<128,false>", "bf16_b2h16_n32768_d128"):
-        {"sources": "4048ca60f9e1dcc1", "bytes": 874345728 + 308971264},
+        {"sources": "353a2e93a1511e26", "bytes": 1304689920 + 233806592},
+    ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
+        {"sources": "353a2e93a1511e26", "bytes": 100716288 + 3066880},
 }
 
 
@@ -384,7 +386,8 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
         except Exception as e:  # keep the main line; report the failure
             res[name] = {"error": f"{type(e).__name__}: {e}"}
 
-    fwd_path(f"{MAIN} noncausal", MAIN, False, inputs=(q, k, v))
+    fwd_path(f"{MAIN} noncausal", MAIN, False, inputs=(q, k, v),
+             kernel="noncausal_kernel<64>")
     fwd_path("bf16_b2h16_n32768_d128 causal", "bf16_b2h16_n32768_d128", True,
              kernel="causal_kernel<128,false>")
     wd = wl.WORKLOADS["bf16_decay_b4h8_n16384_d128"]
