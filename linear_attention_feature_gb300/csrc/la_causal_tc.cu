@@ -112,7 +112,7 @@ struct Layout {
 };
 
 struct Small {
-    float gtab[32];  // E: g^0 .. g^31 of the current head
+    float gtab[32];  // score epilogue: g^0 .. g^31 of the current head
     uint64_t full[4], empty[4], xf[4];
     uint64_t pfull[2], pt_ready[2], pv_done[2], o_full[2], o_empty[2];
     uint64_t s_full, sb_ready;
@@ -543,13 +543,13 @@ __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
                     } else {
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            // g^(lane - e) only where e <= lane: for g = 0 a
-                            // negative power is +inf, and 0 * inf is NaN
+                            // diagonal block: g^(i - j) = g^(lane - e), from
+                            // the head's table, only where e <= lane
                             float x0 = 0.f, x1 = 0.f;
                             if (e <= lane)
-                                x0 = kDecay ? u2f(v[e]) * gpow(lg, lane - e) : u2f(v[e]);
+                                x0 = kDecay ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
                             if (e + 1 <= lane)
-                                x1 = kDecay ? u2f(v[e + 1]) * gpow(lg, lane - e - 1)
+                                x1 = kDecay ? u2f(v[e + 1]) * sm.gtab[lane - e - 1]
                                             : u2f(v[e + 1]);
                             pk[e >> 1] = pack_bf16x2(x0, x1);
                         }
