@@ -64,10 +64,12 @@ def _load():
     lib.ora_noncausal.argtypes = [P, P, P, P, L, L, L, I, I, I]
     lib.ora_recurrent_step.argtypes = [P, P, P, P, P, P, L, ctypes.c_double, I, I]
     lib.ora_causal.argtypes = [P, P, P, P, L, L, L, P, I, I, I]
+    lib.ora_causal_state.argtypes = [P, P, P, P, L, L, L, P, I]
     lib.ora_decode_step.argtypes = [P, P, P, P, P, P, L, L, P, I]
     lib.ora_quadratic.argtypes = [P, P, P, P, L, L, L, P, I, I, P]
     lib.ora_chunked.argtypes = [P, P, P, P, L, L, L, P, L, L]
     for name in ("ora_noncausal_state", "ora_state_read", "ora_noncausal",
+                 "ora_causal_state",
                  "ora_recurrent_step", "ora_causal", "ora_decode_step",
                  "ora_quadratic", "ora_chunked"):
         getattr(lib, name).restype = I
@@ -174,6 +176,20 @@ def causal(q, k, v, decay=None, *, fmap=FMAP_ELU1, normalise=True,
                               _ptr(g) if g is not None else None, fmap,
                               int(normalise), int(nthreads)), "causal")
     return out
+
+
+def causal_state(k, v, decay=None, *, fmap=FMAP_ELU1):
+    """Final (S, z) of the causal recurrence after all N tokens of k, v
+    [..., N, d], with optional per-head decay: S [..., d, d], z [..., d]."""
+    k, v = _f64(k), _f64(v)
+    BH, N, d = _seq_shape(k)
+    g = _decay_per_head(decay, k.shape, BH)
+    S = np.empty(k.shape[:-2] + (d, d))
+    z = np.empty(k.shape[:-2] + (d,))
+    _check(_load().ora_causal_state(_ptr(k), _ptr(v), _ptr(S), _ptr(z), BH, N, d,
+                                    _ptr(g) if g is not None else None, fmap),
+           "causal_state")
+    return S, z
 
 
 def recurrent_step(S, z, q, k, v, g=1.0, *, fmap=FMAP_ELU1, normalise=True):

@@ -227,6 +227,31 @@ int ora_causal(const double *q, const double *k, const double *v, double *out,
     return c.err;
 }
 
+/* Final state of the causal recurrence after all N tokens -- the state a
+ * decode continues from ("Linear Attention", the running statistics S_n and
+ * z_n; with the forget-gate passage's scalar g):
+ *   S_0 = 0, z_0 = 0;  S_t = g S_{t-1} + phi(k_t) v_t^T,  z_t = g z_{t-1} + phi(k_t).
+ * S [BH][d][d] (S[a][c]: a key feature, c value column), z [BH][d]. */
+int ora_causal_state(const double *k, const double *v, double *S, double *z,
+                     long BH, long N, long d, const double *g, int fmap) {
+    if (!k || !v || !S || !z || BH < 0 || N < 0 || d <= 0) return -1;
+    for (long h = 0; h < BH; ++h) {
+        const double gh = g ? g[h] : 1.0;
+        double *Sh = S + h * d * d, *zh = z + h * d;
+        for (long i = 0; i < d * d; ++i) Sh[i] = 0.0;
+        for (long a = 0; a < d; ++a) zh[a] = 0.0;
+        for (long t = 0; t < N; ++t) {
+            const double *kt = k + (h * N + t) * d, *vt = v + (h * N + t) * d;
+            for (long a = 0; a < d; ++a) {
+                const double pk = feat(kt[a], fmap);
+                zh[a] = gh * zh[a] + pk;
+                for (long c = 0; c < d; ++c) Sh[a * d + c] = gh * Sh[a * d + c] + pk * vt[c];
+            }
+        }
+    }
+    return 0;
+}
+
 /* Recurrent decode step: one new token per head on a caller-owned state
  * (S [BH][d][d], z [BH][d], updated in place), then the read.  O(d^2) work
  * and memory per token ("Linear Attention", inference cost per token). */

@@ -174,6 +174,52 @@ def test_decode_steps_equal_causal(decay):
         np.testing.assert_allclose(y, yc[:, :, t], rtol=1e-13, atol=1e-13)
 
 
+# --------------------------------------------------------------------------
+# final state of the causal recurrence (the state a decode continues from)
+
+
+@pytest.mark.parametrize("decay", [None, [0.96875, 0.5]])
+def test_causal_state_closed_form(decay):
+    # S_N = sum_t g^(N-1-t) phi(k_t) v_t^T (0-based t), z_N likewise:
+    # written here with numpy's exp, independently of the oracle's phi
+    B, H, N, d = 2, 2, 11, 5
+    k, v = _rand((B, H, N, d), 30), _rand((B, H, N, d), 31)
+    S, z = oracle.causal_state(k, v, decay)
+    pk = np.where(k > 0, k + 1.0, np.exp(k))
+    g = np.ones(H) if decay is None else np.asarray(decay)
+    w = g[None, :, None] ** (N - 1 - np.arange(N))[None, None, :]  # [1, H, N]
+    S_ref = np.einsum("bhn,bhna,bhnc->bhac", np.broadcast_to(w, (B, H, N)), pk, v)
+    z_ref = np.einsum("bhn,bhna->bha", np.broadcast_to(w, (B, H, N)), pk)
+    np.testing.assert_allclose(S, S_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(z, z_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_causal_state_special_cases():
+    k, v = _rand((1, 2, 9, 4), 32), _rand((1, 2, 9, 4), 33)
+    # no decay: the whole-sequence sums of the non-causal form
+    S, z = oracle.causal_state(k, v)
+    Sn, zn = oracle.noncausal_state(k, v)
+    np.testing.assert_allclose(S, Sn, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(z, zn, rtol=1e-14, atol=1e-14)
+    # g = 0 keeps only the last token
+    S0, z0 = oracle.causal_state(k, v, [0.0, 0.0])
+    pk = np.where(k[..., -1, :] > 0, k[..., -1, :] + 1.0, np.exp(k[..., -1, :]))
+    np.testing.assert_allclose(S0, pk[..., :, None] * v[..., -1, None, :], rtol=1e-15)
+    np.testing.assert_allclose(z0, pk, rtol=1e-15)
+    # empty sequence: the zero state
+    Se, ze = oracle.causal_state(k[..., :0, :], v[..., :0, :])
+    assert not Se.any() and not ze.any()
+
+
+@pytest.mark.parametrize("decay", [None, [0.9, 0.6]])
+def test_causal_state_is_what_the_last_output_reads(decay):
+    q, k, v = (_rand((1, 2, 14, 6), s) for s in (34, 35, 36))
+    S, z = oracle.causal_state(k, v, decay)
+    y_last = oracle.state_read(S, z, q[..., -1:, :])[..., 0, :]
+    np.testing.assert_allclose(y_last, oracle.causal(q, k, v, decay)[..., -1, :],
+                               rtol=1e-12, atol=1e-12)
+
+
 @pytest.mark.parametrize("block", [1, 2, 3, 16, 64])
 @pytest.mark.parametrize("segments", [1, 3])
 @pytest.mark.parametrize("decay", [None, [0.96875, 0.5]])
