@@ -359,7 +359,8 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
     res = {}
     Kx, Wx = max(3, args.steps // 2), max(3, args.warmup)
 
-    def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2, kernel=None):
+    def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2, kernel=None,
+                 state=False):
         w = wl.WORKLOADS[wkey]
         try:
             if inputs is None:
@@ -368,13 +369,21 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
                 qq, kk, vv = inputs
             oo = torch.empty_like(qq)
             fn = lambda: la.forward(qq, kk, vv, causal=causal, decay=decay, out=oo)  # noqa
+            extra = 0
+            if state:
+                # forward plus the final state (the prefill of a decode)
+                Ss = torch.empty(w.B, w.H, w.d, w.d, device=dev)
+                zs = torch.empty(w.B, w.H, w.d, device=dev)
+                fn = lambda: la.forward_causal_state(qq, kk, vv, decay=decay, out=oo,  # noqa
+                                                     S=Ss, z=zs)
+                extra = 4 * w.B * w.H * (w.d * w.d + w.d)
             replay, _ = capture(fn)
             steps = timed_steps(replay, Kx, Wx, world, flush)
             la.check_device_status()
             ms = max_over_ranks(sum(steps) / Kx, world)
             r = {"tokens_per_s": round(w.B * w.N * world / (ms * 1e-3), 1),
                  "ms_per_step": round(ms, 4), "steps": Kx,
-                 "roofline": roofline_hbm(forward_bytes(w.B, w.H, w.N, w.d, elem),
+                 "roofline": roofline_hbm(forward_bytes(w.B, w.H, w.N, w.d, elem) + extra,
                                           ms, peaks["hbm_gbs"],
                                           known_traffic(kernel, w) if kernel else None)}
             if causal and elem == 2:
@@ -394,11 +403,21 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
     fwd_path("bf16_decay_b4h8_n16384_d128 causal", wd.name, True,
              decay=list(wd.decay))
     fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
+    fwd_path(f"{MAIN} causal with final state", MAIN, True, inputs=(q, k, v),
+             state=True)
     try:
         res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,
                                                 args)
     except Exception as e:
         res["decode_b256h32_d128"] = {"error": f"{type(e).__name__}: {e}"}
+    try:
+        # the same decode with the per-head decay g_h = 1 - 2^(-5-h)
+        wdec = wl.WORKLOADS["decode_b256h32_d128"]
+        res["decode_b256h32_d128 decay"] = run_decode(
+            la, wl, dev, peaks, world, rank, args,
+            decay=list(wl.decay_schedule(wdec.H)))
+    except Exception as e:
+        res["decode_b256h32_d128 decay"] = {"error": f"{type(e).__name__}: {e}"}
     return res
 
 
@@ -408,7 +427,7 @@ def decode_bytes(BH, d, elem):
     return BH * (2 * (d * d + d) * 4 + 4 * d * elem)
 
 
-def run_decode(la, wl, dev, peaks, world, rank, args):
+def run_decode(la, wl, dev, peaks, world, rank, args, decay=None):
     import torch
     w = wl.WORKLOADS["decode_b256h32_d128"]
     B, H, d = w.B, w.H, w.d
@@ -421,15 +440,16 @@ def run_decode(la, wl, dev, peaks, world, rank, args):
     z = torch.zeros(B, H, d, device=dev)
     o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
     for t in range(P):  # prefill from the 1024 seeded tokens (untimed)
-        la.decode_step(S, z, q[t], k[t], v[t], out=o)
+        la.decode_step(S, z, q[t], k[t], v[t], out=o, decay=decay)
     # the T timed steps, captured once as one graph of T launches
-    replay, _ = capture(lambda: [la.decode_step(S, z, q[t], k[t], v[t], out=o)
+    replay, _ = capture(lambda: [la.decode_step(S, z, q[t], k[t], v[t], out=o,
+                                                decay=decay)
                                   for t in range(P, P + T)])
     # capturing ran the steps once: restore the prefilled state
     S.zero_()
     z.zero_()
     for t in range(P):
-        la.decode_step(S, z, q[t], k[t], v[t], out=o)
+        la.decode_step(S, z, q[t], k[t], v[t], out=o, decay=decay)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()

@@ -74,7 +74,8 @@ typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
  *   q, k, v  [B][H][N][d] device, dtype `dtype`, read only.
  *   out      [B][H][N][d] device, dtype `dtype`, written; may not alias
  *            q, k or v.
- *   B, H, N  >= 0 (B*H*N == 0 is a no-op returning LA_OK); d in 1..LA_MAX_D.
+ *   B, H, N  >= 0 (B*H*N == 0 is a no-op returning LA_OK, and then q, k,
+ *            v, out may be NULL); d in 1..LA_MAX_D.
  *   causal   0 or 1.
  *   decay    HOST array of H floats g_h in [0, 1] (read during the call, not
  *            retained), or NULL for g = 1.  Only valid with causal == 1:
@@ -167,6 +168,40 @@ size_t la_forward_host_workspace_bytes(int B, int H, int N, int d,
 la_status la_decode_step(float *S, float *z, const void *q, const void *k,
                          const void *v, void *out, int B, int H, int d,
                          la_dtype dtype, la_stream_t stream);
+
+/*
+ * la_decode_step_ex -- la_decode_step with a per-head decay g:
+ * S <- g S + phi_k v^T, z <- g z + phi_k, then out = phi(q)^T S / phi(q)^T z
+ * (the recurrence with the forget-gate passage's scalar g; "Story of
+ * Attention - Part 5", section 4, recurrent form S_t = g S_{t-1} + k_t v_t^T).
+ *   decay    HOST array of H floats in [0, 1] (read during the call), or NULL
+ *            for g = 1 (then identical to la_decode_step).
+ * Other arguments, layouts and errors as la_decode_step; LA_ERR_UNSUPPORTED
+ * for a decay over more than LA_MAX_DECAY_HEADS heads.
+ */
+la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k,
+                            const void *v, void *out, int B, int H, int d,
+                            const float *decay, la_dtype dtype,
+                            la_stream_t stream);
+
+/*
+ * la_forward_causal_state -- the causal form of la_forward that also returns
+ * the final state: S_N = sum_t g^(N-1-t) phi(k_t) v_t^T and z_N likewise,
+ * i.e. the running statistics after the last token ("Linear Attention",
+ * running statistics; the state an RNN-style decode continues from).  It is
+ * the prefill half of a prefill -> decode hand-off: la_decode_step(_ex) on S
+ * and z then continues the same sequences.
+ *   q, k, v, out, B, H, N, d, decay, dtype   as la_forward with causal = 1.
+ *   S        [B][H][d][d] fp32 device, written (S[a][c]: a key feature, c
+ *            value column; the layout la_decode_step reads); 16-byte aligned.
+ *   z        [B][H][d] fp32 device, written.
+ * N == 0 writes the zero state.  Errors as la_forward, plus
+ * LA_ERR_INVALID_ARG for a NULL or unaligned S or a NULL z.
+ */
+la_status la_forward_causal_state(const void *q, const void *k, const void *v,
+                                  void *out, float *S, float *z, int B, int H,
+                                  int N, int d, const float *decay,
+                                  la_dtype dtype, la_stream_t stream);
 
 /* Size of the fixed device scratch used by la_forward_causal_noalloc. */
 #define LA_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -14,7 +14,8 @@ import os
 
 from . import build as _build
 
-__all__ = ["forward", "forward_host", "host_workspace_bytes", "decode_step",
+__all__ = ["forward", "forward_causal_state", "forward_host",
+           "host_workspace_bytes", "decode_step",
            "check_device_status",
            "kernel_launch_count", "LinAttnError",
            "load_library", "LA_F32", "LA_BF16", "STATUS", "EXPORTED"]
@@ -27,7 +28,8 @@ EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_check_device_status", "la_status_string", "la_last_error",
             "la_abi_version", "la_kernel_launch_count",
             "la_forward_causal_noalloc", "la_forward_host",
-            "la_forward_host_workspace_bytes")
+            "la_forward_host_workspace_bytes", "la_forward_causal_state",
+            "la_decode_step_ex")
 
 _lib = None
 
@@ -53,6 +55,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.la_forward.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V]
     lib.la_forward_ex.argtypes = [V, V, V, V, I, I, I, I, I, F, I, I, I, V]
     lib.la_decode_step.argtypes = [V, V, V, V, V, V, I, I, I, I, V]
+    lib.la_decode_step_ex.argtypes = [V, V, V, V, V, V, I, I, I, F, I, V]
+    lib.la_forward_causal_state.argtypes = [V, V, V, V, V, V, I, I, I, I, F, I, V]
     lib.la_forward_host.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V,
                                     ctypes.c_size_t, V]
     lib.la_forward_host_workspace_bytes.argtypes = [I, I, I, I, I]
@@ -66,6 +70,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.la_kernel_launch_count.argtypes = []
     lib.la_kernel_launch_count.restype = ctypes.c_ulonglong
     for n in ("la_forward", "la_forward_ex", "la_decode_step", "la_forward_host",
+              "la_decode_step_ex", "la_forward_causal_state",
               "la_check_device_status", "la_abi_version"):
         getattr(lib, n).restype = I
     if path is None:
@@ -145,9 +150,46 @@ def forward(q, k, v, causal: bool = True, decay=None, out=None, *,
     return out
 
 
-def decode_step(S, z, q, k, v, out=None, *, stream=None):
+def forward_causal_state(q, k, v, decay=None, out=None, S=None, z=None, *,
+                         stream=None):
+    """Causal forward that also returns the final state: (out, S, z) with
+    S [B, H, d, d] and z [B, H, d] in fp32 -- the state after the last token,
+    in the layout decode_step takes, so that a decode continues the
+    sequence."""
+    torch = _torch()
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if S is None:
+        S = torch.empty(B, H, d, d, dtype=torch.float32, device=q.device)
+    if z is None:
+        z = torch.empty(B, H, d, dtype=torch.float32, device=q.device)
+    if tuple(S.shape) != (B, H, d, d) or tuple(z.shape) != (B, H, d):
+        raise ValueError("S must be [B, H, d, d] and z [B, H, d]")
+    if S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("S and z must be float32")
+    _check_cuda(q, k, v, out, S, z)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_forward_causal_state(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(S.data_ptr()), ctypes.c_void_p(z.data_ptr()),
+            B, H, N, d, _decay_arg(decay, H), _dtype_code(q),
+            _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out, S, z
+
+
+def decode_step(S, z, q, k, v, out=None, *, decay=None, stream=None):
     """One decode step per head: S, z (fp32, [B, H, d, d] / [B, H, d]) are
-    updated in place; q, k, v [B, H, d]; returns out [B, H, d]."""
+    updated in place (S <- g S + phi(k) v^T, z <- g z + phi(k), with the
+    per-head decay g from `decay`, H floats in [0, 1], or 1); q, k, v
+    [B, H, d]; returns out [B, H, d]."""
     torch = _torch()
     if q.dim() != 3 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must share one [B, H, d] shape")
@@ -163,11 +205,12 @@ def decode_step(S, z, q, k, v, out=None, *, stream=None):
     _check_cuda(S, z, q, k, v, out)
     lib = load_library()
     with torch.cuda.device(q.device):
-        st = lib.la_decode_step(
+        st = lib.la_decode_step_ex(
             ctypes.c_void_p(S.data_ptr()), ctypes.c_void_p(z.data_ptr()),
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
-            B, H, d, _dtype_code(q), _stream_ptr(stream, q.device))
+            B, H, d, _decay_arg(decay, H), _dtype_code(q),
+            _stream_ptr(stream, q.device))
     _raise_if(st)
     return out
 

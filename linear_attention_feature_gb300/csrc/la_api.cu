@@ -74,17 +74,20 @@ la_status validate_forward(const void *q, const void *k, const void *v,
                            const void *out, int B, int H, int N, int d,
                            int causal, const float *decay, la_dtype dtype,
                            DecayArgs *dk) {
-    if (!q || !k || !v || !out)
-        return fail(LA_ERR_INVALID_ARG, "la_forward: null tensor pointer");
     if (B < 0 || H < 0 || N < 0)
         return fail(LA_ERR_INVALID_ARG, "la_forward: negative B, H or N");
+    // an empty problem reads and writes no tensor element, so its pointers
+    // may be NULL (zero-size framework tensors have no storage)
+    const bool empty = (long long)B * H * N == 0;
+    if (!empty && (!q || !k || !v || !out))
+        return fail(LA_ERR_INVALID_ARG, "la_forward: null tensor pointer");
     if (d < 1 || d > LA_MAX_D)
         return fail(LA_ERR_INVALID_ARG, "la_forward: d must be in 1..256");
     if (causal != 0 && causal != 1)
         return fail(LA_ERR_INVALID_ARG, "la_forward: causal must be 0 or 1");
     if (!valid_dtype(dtype))
         return fail(LA_ERR_INVALID_ARG, "la_forward: unknown dtype");
-    if (out == q || out == k || out == v)
+    if (!empty && (out == q || out == k || out == v))
         return fail(LA_ERR_INVALID_ARG, "la_forward: out aliases an input");
     dk->has = 0;
     dk->H = H > 0 ? H : 1;
@@ -118,7 +121,20 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
                         int segment_chunks, la_stream_t stream) {
     return la::forward_with_workspace(q, k, v, out, B, H, N, d, causal, decay,
                                       dtype, path, segment_chunks, nullptr, 0,
-                                      stream);
+                                      nullptr, nullptr, stream);
+}
+
+__attribute__((visibility("default")))
+la_status la_forward_causal_state(const void *q, const void *k, const void *v,
+                                  void *out, float *S, float *z, int B, int H,
+                                  int N, int d, const float *decay,
+                                  la_dtype dtype, la_stream_t stream) {
+    if (!S || !z)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_causal_state: null state pointer");
+    if ((reinterpret_cast<uintptr_t>(S) & 15u) != 0)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_causal_state: S must be 16-byte aligned");
+    return la::forward_with_workspace(q, k, v, out, B, H, N, d, 1, decay, dtype,
+                                      0, 0, nullptr, 0, S, z, stream);
 }
 
 __attribute__((visibility("default")))
@@ -135,7 +151,8 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
                                      void *out, int B, int H, int N, int d,
                                      int causal, const float *decay,
                                      la_dtype dtype, int path, int segment_chunks,
-                                     void *ws, size_t ws_bytes, la_stream_t stream) {
+                                     void *ws, size_t ws_bytes, float *S_out,
+                                     float *z_out, la_stream_t stream) {
     DecayArgs dk;
     la_status st = validate_forward(q, k, v, out, B, H, N, d, causal, decay,
                                     dtype, &dk);
@@ -145,9 +162,18 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
     if (segment_chunks < 0)
         return fail(LA_ERR_INVALID_ARG, "la_forward_ex: segment_chunks < 0");
     FwdShape sh{B, H, N, d};
-    if (sh.BH() == 0 || N == 0) return LA_OK;
+    if (sh.BH() == 0) return LA_OK;
     if (sh.BH() > 2147483647LL || (long long)N * d > (1LL << 40))
         return fail(LA_ERR_UNSUPPORTED, "la_forward: problem too large");
+    if (N == 0) {
+        // no tokens: the final state is the zero state
+        if (!S_out) return LA_OK;
+        cudaStream_t s0 = reinterpret_cast<cudaStream_t>(stream);
+        cudaError_t e0 = cudaMemsetAsync(S_out, 0, sizeof(float) * sh.BH() * d * d, s0);
+        if (e0 == cudaSuccess)
+            e0 = cudaMemsetAsync(z_out, 0, sizeof(float) * sh.BH() * d, s0);
+        return e0 == cudaSuccess ? LA_OK : cuda_fail(e0, "la_forward: zero state");
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     const bool tc_ok = tc_supported(sh, dtype, causal, q, k, v, out);
@@ -159,14 +185,15 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
         int *status = device_status_word(&ce);
         if (!status) return cuda_fail(ce, "la_forward: status word");
         TcResult r = tc_forward(q, k, v, out, sh, causal, dk, segment_chunks,
-                                status, ws, ws_bytes, s);
+                                status, ws, ws_bytes, S_out, z_out, s);
         if (r.status != LA_OK) {
             if (r.status == LA_ERR_CUDA) return cuda_fail(r.cuda, r.where);
             return fail(r.status, r.where);
         }
         return LA_OK;
     }
-    cudaError_t e = launch_simt_forward(q, k, v, out, sh, causal, dk, dtype, s);
+    cudaError_t e = launch_simt_forward(q, k, v, out, sh, causal, dk, dtype,
+                                        S_out, z_out, s);
     if (e != cudaSuccess) return cuda_fail(e, "la_forward (CUDA-core kernel)");
     note_launches(1);
     return LA_OK;
@@ -184,9 +211,10 @@ size_t la::forward_workspace_bytes(int B, int H, int N, int d, int causal,
 extern "C" {
 
 __attribute__((visibility("default")))
-la_status la_decode_step(float *S, float *z, const void *q, const void *k,
-                         const void *v, void *out, int B, int H, int d,
-                         la_dtype dtype, la_stream_t stream) {
+la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k,
+                            const void *v, void *out, int B, int H, int d,
+                            const float *decay, la_dtype dtype,
+                            la_stream_t stream) {
     if (!S || !z || !q || !k || !v || !out)
         return fail(LA_ERR_INVALID_ARG, "la_decode_step: null pointer");
     if (B < 0 || H < 0)
@@ -195,15 +223,38 @@ la_status la_decode_step(float *S, float *z, const void *q, const void *k,
         return fail(LA_ERR_INVALID_ARG, "la_decode_step: d must be in 1..256");
     if (!valid_dtype(dtype))
         return fail(LA_ERR_INVALID_ARG, "la_decode_step: unknown dtype");
+    DecayArgs dk;
+    dk.has = 0;
+    dk.H = H > 0 ? H : 1;
+    if (decay) {
+        if (H > LA_MAX_DECAY_HEADS)
+            return fail(LA_ERR_UNSUPPORTED,
+                        "la_decode_step: decay given for more than 1024 heads");
+        for (int h = 0; h < H; ++h) {
+            const float g = decay[h];
+            if (!(g >= 0.f && g <= 1.f))  // also rejects NaN
+                return fail(LA_ERR_INVALID_ARG,
+                            "la_decode_step: decay values must lie in [0, 1]");
+            dk.g[h] = g;
+        }
+        dk.has = 1;
+    }
     long long BH = (long long)B * H;
     if (BH == 0) return LA_OK;
     if (BH > 2147483647LL)
         return fail(LA_ERR_UNSUPPORTED, "la_decode_step: too many heads");
-    cudaError_t e = launch_decode_step(S, z, q, k, v, out, BH, d, dtype,
+    cudaError_t e = launch_decode_step(S, z, q, k, v, out, BH, d, dk, dtype,
                                        reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
     note_launches(1);
     return LA_OK;
+}
+
+__attribute__((visibility("default")))
+la_status la_decode_step(float *S, float *z, const void *q, const void *k,
+                         const void *v, void *out, int B, int H, int d,
+                         la_dtype dtype, la_stream_t stream) {
+    return la_decode_step_ex(S, z, q, k, v, out, B, H, d, nullptr, dtype, stream);
 }
 
 __attribute__((visibility("default")))

@@ -79,6 +79,7 @@ struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
     float *agg, *incl;  // [items][DK * DV + DK]: S rows (a-major), then z
     int *flags;         // [items]
+    float *S_out, *z_out;  // final state [BH][DK][DK] / [BH][DK], or NULL
     int *ctrl;          // [0] ticket counter, [1] abort flag
     int *status;        // device status word
     long long timeout;  // clock cycles per bounded wait
@@ -283,14 +284,16 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 mma_commit(&sm.empty[st]);
             }
         }
-        // phase B.  The state after the item's last chunk is never read, so
-        // that chunk has no state update.
+        // phase B.  The state after the item's last chunk is only read when
+        // it is the sequence's final state and the caller asked for it;
+        // otherwise that chunk has no state update.
         const int nB = it.c1 - it.c0;
+        const bool final_state = p.S_out && it.seg == p.nseg - 1;
         int p_next = 0;  // first B chunk of the item whose P is not issued
         for (int qi = 0; qi < nB; ++qi) {
             const int jj = j + qi, nbq = nb + qi;
             const int st = jj % L::STAGES, b = nbq & 1;
-            const bool su = qi + 1 < nB;
+            const bool su = qi + 1 < nB || final_state;
             if (p_next == qi) {
                 issue_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq);
                 ++p_next;
@@ -367,6 +370,12 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             // releases it itself when the output is staged in its Q slot)
             mma_commit(&sm.empty[st]);
             if (L::OWN_OST) mma_commit(&sm.empty[st]);
+        }
+        if (final_state) {
+            // S's columns are reused by the next item: wait until the
+            // output warpgroup has read the final state
+            wait_bar(&sm.sb_ready, nsb & 1, cx);
+            ++nsb;
         }
         j += nB;
         nb += nB;
@@ -1021,6 +1030,36 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             mbar_arrive(&sm.empty[pend]);
             pend = -1;
         }
+        if (p.S_out && it.seg == p.nseg - 1) {
+            // the state after the sequence's last token (a decode continues
+            // from it): this item's 64 value columns of S, and z once
+            wait_bar(&sm.s_full, ns & 1, cx);
+            ++ns;
+            tc_fence_after();
+#pragma unroll 1
+            for (int hh = 0; hh < SM::NH; ++hh) {
+                const int h = h0 + hh;
+                uint32_t v[32];
+                tmem_ld32(lb + TM_S + 32 * h, v);
+                tmem_wait_ld();
+                reg_fence(v);
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.S_out + ((size_t)it.bh * DK + a) * DK + 64 * it.half + 32 * h);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
+                                         u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+            }
+            if (hasz && it.half == 0) {
+                uint32_t zr = tmem_ld1(lb + TM_S + DV);
+                tmem_wait_ld();
+                reg_fence(zr);
+                p.z_out[(size_t)it.bh * DK + a] = u2f(zr);
+            }
+            tc_fence_before();
+            named_bar_sync(BAR_E2, 128);
+            if (et == 0) mbar_arrive(&sm.sb_ready);
+        }
     }
     if (et == 0) tma_store_wait_all<0>();
 }
@@ -1168,8 +1207,8 @@ CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms) {
 template <int DK, bool kDecay>
 TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
                          const FwdShape &sh, const DecayArgs &dk, int seg_chunks,
-                         int *status, void *ws_in, size_t ws_bytes,
-                         cudaStream_t stream) {
+                         int *status, void *ws_in, size_t ws_bytes, float *S_out,
+                         float *z_out, cudaStream_t stream) {
     using namespace causal_tc;
     const int BH = (int)sh.BH(), N = sh.N;
     CUtensorMap tq, tk, tv, to;
@@ -1196,6 +1235,8 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.nseg = pl.nseg;
     p.items = (int)pl.items;
     p.timeout = 1LL << 32;
+    p.S_out = S_out;
+    p.z_out = z_out;
 
     // the caller's workspace when given, else a stream-ordered allocation
     void *ws = ws_in;
@@ -1235,12 +1276,12 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
 TcResult launch_causal_tc(const void *q, const void *k, const void *v,
                           void *out, const FwdShape &sh, const DecayArgs &dk,
                           int seg_chunks, int *status, void *ws, size_t ws_bytes,
-                          cudaStream_t stream) {
+                          float *S_out, float *z_out, cudaStream_t stream) {
     if (sh.d == 128)
-        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream)
-                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream);
-    return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream)
-                  : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, stream);
+        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream)
+                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream);
+    return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream)
+                  : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream);
 }
 
 size_t causal_tc_workspace_bytes(const FwdShape &sh, bool decay, int seg_chunks, int sms) {

@@ -1,6 +1,8 @@
-// Recurrent decode step: S <- S + phi(k) v^T, z <- z + phi(k),
+// Recurrent decode step: S <- g S + phi(k) v^T, z <- g z + phi(k),
 // out = phi(q)^T S / phi(q)^T z  ("Linear Attention", running statistics and
-// the O(d^2)-per-token inference cost).
+// the O(d^2)-per-token inference cost; g the per-head decay of the
+// forget-gate passage, 1 without decay).  g = 1 multiplies by one exactly, so
+// the undecayed step is unchanged.
 //
 // The step is a pure stream over the fp32 d x d state (read once, written
 // once): 2 * 4 * d^2 bytes per head against ~4 d^2 flops, so it is bound by
@@ -38,7 +40,7 @@ template <typename T>
 __device__ __forceinline__ void decode_prologue(float *__restrict__ zh,
                                                 const T *__restrict__ qh,
                                                 const T *__restrict__ kh,
-                                                int d, float *sk, float *sq,
+                                                int d, float g, float *sk, float *sq,
                                                 float *swarp, float *sden) {
     const int tid = threadIdx.x;
     float part = 0.f;
@@ -47,7 +49,7 @@ __device__ __forceinline__ void decode_prologue(float *__restrict__ zh,
         float pq = phi(ld_in(qh + a));
         sk[a] = pk;
         sq[a] = pq;
-        float zn = zh[a] + pk;
+        float zn = fmaf(g, zh[a], pk);
         zh[a] = zn;
         part = fmaf(pq, zn, part);
     }
@@ -67,7 +69,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
                   const T *__restrict__ q, const T *__restrict__ k,
-                  const T *__restrict__ v, T *__restrict__ out) {
+                  const T *__restrict__ v, T *__restrict__ out, DecayArgs dk) {
     constexpr int NCG = D / 4;                 // column groups (float4 each)
     constexpr int NRG = kThreads / NCG;        // row groups
     constexpr int RPT = D / NRG;               // rows per thread
@@ -82,8 +84,9 @@ decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
     const int tid = threadIdx.x;
     const int cg = tid % NCG, rg = tid / NCG;
     float4 *__restrict__ Sh = reinterpret_cast<float4 *>(S + (size_t)bh * D * D);
+    const float g = decay_of(dk, (int)bh);
     decode_prologue<T>(z + (size_t)bh * D, q + (size_t)bh * D,
-                       k + (size_t)bh * D, D, sk, sq, swarp, &sden);
+                       k + (size_t)bh * D, D, g, sk, sq, swarp, &sden);
     const T *vh = v + (size_t)bh * D + 4 * cg;
     const float v0 = ld_in(vh), v1 = ld_in(vh + 1), v2 = ld_in(vh + 2),
                 v3 = ld_in(vh + 3);
@@ -100,10 +103,10 @@ decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
         for (int r = 0; r < BATCH; ++r) {
             const int a = rg + (r0 + r) * NRG;
             const float pk = sk[a], pq = sq[a];
-            s[r].x = fmaf(pk, v0, s[r].x);
-            s[r].y = fmaf(pk, v1, s[r].y);
-            s[r].z = fmaf(pk, v2, s[r].z);
-            s[r].w = fmaf(pk, v3, s[r].w);
+            s[r].x = fmaf(pk, v0, g * s[r].x);
+            s[r].y = fmaf(pk, v1, g * s[r].y);
+            s[r].z = fmaf(pk, v2, g * s[r].z);
+            s[r].w = fmaf(pk, v3, g * s[r].w);
             __stcs(Sh + (size_t)a * NCG + cg, s[r]);
             acc.x = fmaf(pq, s[r].x, acc.x);
             acc.y = fmaf(pq, s[r].y, acc.y);
@@ -135,19 +138,21 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 decode_generic_kernel(float *__restrict__ S, float *__restrict__ z,
                       const T *__restrict__ q, const T *__restrict__ k,
-                      const T *__restrict__ v, T *__restrict__ out, int d) {
+                      const T *__restrict__ v, T *__restrict__ out, int d,
+                      DecayArgs dk) {
     __shared__ float sk[LA_MAX_D], sq[LA_MAX_D];
     __shared__ float swarp[kThreads / 32], sden;
     const long long bh = blockIdx.x;
     float *Sh = S + (size_t)bh * d * d;
+    const float g = decay_of(dk, (int)bh);
     decode_prologue<T>(z + (size_t)bh * d, q + (size_t)bh * d,
-                       k + (size_t)bh * d, d, sk, sq, swarp, &sden);
+                       k + (size_t)bh * d, d, g, sk, sq, swarp, &sden);
     __syncthreads();
     for (int c = threadIdx.x; c < d; c += kThreads) {
         const float vc = ld_in(v + (size_t)bh * d + c);
         float acc = 0.f;
         for (int a = 0; a < d; ++a) {
-            float s = fmaf(sk[a], vc, Sh[(size_t)a * d + c]);
+            float s = fmaf(sk[a], vc, g * Sh[(size_t)a * d + c]);
             Sh[(size_t)a * d + c] = s;
             acc = fmaf(sq[a], s, acc);
         }
@@ -158,20 +163,20 @@ decode_generic_kernel(float *__restrict__ S, float *__restrict__ z,
 template <typename T>
 cudaError_t launch_t(float *S, float *z, const void *q, const void *k,
                      const void *v, void *out, long long BH, int d,
-                     cudaStream_t stream) {
+                     const DecayArgs &dk, cudaStream_t stream) {
     const T *qq = static_cast<const T *>(q), *kk = static_cast<const T *>(k),
             *vv = static_cast<const T *>(v);
     T *oo = static_cast<T *>(out);
     const bool aligned = (reinterpret_cast<uintptr_t>(S) & 15u) == 0;
     dim3 grid((unsigned)BH);
     if (aligned && d == 128)
-        decode_vec_kernel<T, 128><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo);
+        decode_vec_kernel<T, 128><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk);
     else if (aligned && d == 64)
-        decode_vec_kernel<T, 64><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo);
+        decode_vec_kernel<T, 64><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk);
     else if (aligned && d == 256)
-        decode_vec_kernel<T, 256><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo);
+        decode_vec_kernel<T, 256><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk);
     else
-        decode_generic_kernel<T><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, d);
+        decode_generic_kernel<T><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, d, dk);
     return cudaGetLastError();
 }
 
@@ -179,10 +184,10 @@ cudaError_t launch_t(float *S, float *z, const void *q, const void *k,
 
 cudaError_t launch_decode_step(float *S, float *z, const void *q,
                                const void *k, const void *v, void *out,
-                               long long BH, int d, la_dtype dtype,
-                               cudaStream_t stream) {
-    if (dtype == LA_F32) return launch_t<float>(S, z, q, k, v, out, BH, d, stream);
-    return launch_t<__nv_bfloat16>(S, z, q, k, v, out, BH, d, stream);
+                               long long BH, int d, const DecayArgs &dk,
+                               la_dtype dtype, cudaStream_t stream) {
+    if (dtype == LA_F32) return launch_t<float>(S, z, q, k, v, out, BH, d, dk, stream);
+    return launch_t<__nv_bfloat16>(S, z, q, k, v, out, BH, d, dk, stream);
 }
 
 }  // namespace la

@@ -28,16 +28,18 @@ struct FwdShape {
 };
 
 // ---- CUDA-core (fp32 FMA) forward: any d in 1..LA_MAX_D, fp32 or bf16 ----
+// S_out / z_out (causal only, may be NULL): the final state [BH][d][d] /
+// [BH][d] in fp32.
 cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
                                 void *out, const FwdShape &sh, int causal,
                                 const DecayArgs &decay, la_dtype dtype,
-                                cudaStream_t stream);
+                                float *S_out, float *z_out, cudaStream_t stream);
 
 // ---- recurrent decode step ----
 cudaError_t launch_decode_step(float *S, float *z, const void *q,
                                const void *k, const void *v, void *out,
-                               long long BH, int d, la_dtype dtype,
-                               cudaStream_t stream);
+                               long long BH, int d, const DecayArgs &decay,
+                               la_dtype dtype, cudaStream_t stream);
 
 // Address of the current device's two status words (kernels set word 0 to a
 // non-zero la_status when a bounded wait gives up, and word 1 to where).
@@ -52,11 +54,13 @@ void set_last_error(const char *msg);
 
 // la_forward_ex with an optional caller-owned scratch for the tensor-core
 // kernels (ws = NULL: they allocate it stream-ordered themselves).
+// S_out / z_out (causal only, may be NULL): also write the final state.
 la_status forward_with_workspace(const void *q, const void *k, const void *v,
                                  void *out, int B, int H, int N, int d,
                                  int causal, const float *decay, la_dtype dtype,
                                  int path, int segment_chunks, void *ws,
-                                 size_t ws_bytes, la_stream_t stream);
+                                 size_t ws_bytes, float *S_out, float *z_out,
+                                 la_stream_t stream);
 
 // Scratch bytes forward_with_workspace needs (automatic path and segment
 // length; 0 where the CUDA-core kernels run, which need none).

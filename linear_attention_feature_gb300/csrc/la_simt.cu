@@ -42,7 +42,8 @@ template <typename T, bool kCausal>
 __global__ void __launch_bounds__(kThreads)
 simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, T *__restrict__ out, int N,
-                    int d, DecayArgs decay) {
+                    int d, DecayArgs decay, float *__restrict__ S_out,
+                    float *__restrict__ z_out) {
     extern __shared__ float smem[];
     const int cb = blockIdx.x;
     const long long bh = blockIdx.y;
@@ -170,13 +171,22 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
         }
         __syncthreads();
     }
+    // the state after the last token, for a decode to continue from
+    if (S_out) {
+        for (int e = tid; e < d * kCB; e += kThreads) {
+            const int a = e / kCB, c = e % kCB;
+            if (c < cw) S_out[((size_t)bh * d + a) * d + c0 + c] = S[e];
+        }
+        if (cb == 0)
+            for (int a = tid; a < d; a += kThreads) z_out[(size_t)bh * d + a] = z[a];
+    }
     }
 }
 
 template <typename T, bool kCausal>
 cudaError_t launch_t(const void *q, const void *k, const void *v, void *out,
-                     const FwdShape &sh, const DecayArgs &decay,
-                     cudaStream_t stream) {
+                     const FwdShape &sh, const DecayArgs &decay, float *S_out,
+                     float *z_out, cudaStream_t stream) {
     const int d = sh.d;
     size_t smem_floats = (size_t)d * kCB + d + 2 * (size_t)kT * d +
                          (size_t)kT * kCB + kT * kT + kT + (kT + 1);
@@ -188,7 +198,8 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, void *out,
     dim3 grid((d + kCB - 1) / kCB, (unsigned)sh.BH());
     kern<<<grid, kThreads, smem, stream>>>(
         static_cast<const T *>(q), static_cast<const T *>(k),
-        static_cast<const T *>(v), static_cast<T *>(out), sh.N, d, decay);
+        static_cast<const T *>(v), static_cast<T *>(out), sh.N, d, decay, S_out,
+        z_out);
     return cudaGetLastError();
 }
 
@@ -197,13 +208,13 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, void *out,
 cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
                                 void *out, const FwdShape &sh, int causal,
                                 const DecayArgs &decay, la_dtype dtype,
-                                cudaStream_t stream) {
+                                float *S_out, float *z_out, cudaStream_t stream) {
     if (dtype == LA_F32)
-        return causal ? launch_t<float, true>(q, k, v, out, sh, decay, stream)
-                      : launch_t<float, false>(q, k, v, out, sh, decay, stream);
+        return causal ? launch_t<float, true>(q, k, v, out, sh, decay, S_out, z_out, stream)
+                      : launch_t<float, false>(q, k, v, out, sh, decay, nullptr, nullptr, stream);
     return causal
-               ? launch_t<__nv_bfloat16, true>(q, k, v, out, sh, decay, stream)
-               : launch_t<__nv_bfloat16, false>(q, k, v, out, sh, decay, stream);
+               ? launch_t<__nv_bfloat16, true>(q, k, v, out, sh, decay, S_out, z_out, stream)
+               : launch_t<__nv_bfloat16, false>(q, k, v, out, sh, decay, nullptr, nullptr, stream);
 }
 
 }  // namespace la

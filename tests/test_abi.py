@@ -91,10 +91,12 @@ def test_forward_rejects_bad_arguments(lib, kw, code, msg):
 
 
 def test_forward_empty_problems_are_noops(lib):
-    # nothing is enqueued, so no GPU is needed
+    # nothing is enqueued, so no GPU is needed; an empty problem touches no
+    # tensor element, so NULL pointers (zero-size tensors) are accepted
     assert fwd(lib, B=0) == OK
     assert fwd(lib, H=0) == OK
     assert fwd(lib, N=0) == OK
+    assert fwd(lib, N=0, q=None, k=None, v=None, out=None) == OK
 
 
 def test_forward_rejects_decay_for_too_many_heads(lib):
@@ -178,3 +180,30 @@ def test_forward_host_python_binding_refuses_strided_tensors(lib):
     q = torch.zeros(1, 1, 4, 4)
     with pytest.raises(ValueError, match="contiguous host"):
         la.forward_host(q.transpose(2, 3), q.clone(), q.clone())
+
+
+def test_forward_causal_state_rejects_bad_arguments(lib):
+    f = lib.la_forward_causal_state
+    SA = ctypes.c_void_p(0x200000)   # 16-byte aligned, never dereferenced
+    ZA = ctypes.c_void_p(0x300000)
+    assert f(P, P2, P3, OUT, None, ZA, 1, 2, 8, 64, None, 1, None) == INVALID
+    assert "null state" in lib.la_last_error().decode()
+    assert f(P, P2, P3, OUT, SA, None, 1, 2, 8, 64, None, 1, None) == INVALID
+    assert f(P, P2, P3, OUT, ctypes.c_void_p(0x200004), ZA, 1, 2, 8, 64, None, 1,
+             None) == INVALID
+    assert "aligned" in lib.la_last_error().decode()
+    assert f(None, P2, P3, OUT, SA, ZA, 1, 2, 8, 64, None, 1, None) == INVALID
+    assert f(P, P2, P3, OUT, SA, ZA, 1, 2, 8, 300, None, 1, None) == INVALID
+    assert f(P, P2, P3, OUT, SA, ZA, 1, 2, 8, 64, floats(0.5, 1.5), 1, None) == INVALID
+    assert f(P, P2, P3, OUT, SA, ZA, 0, 2, 8, 64, None, 1, None) == OK  # no heads
+
+
+def test_decode_step_ex_rejects_bad_decay(lib):
+    f = lib.la_decode_step_ex
+    assert f(P, P, P, P, P, OUT, 1, 2, 64, floats(0.5, -0.1), 1, None) == INVALID
+    assert "[0, 1]" in lib.la_last_error().decode()
+    assert f(P, P, P, P, P, OUT, 1, 2, 64, floats(float("nan"), 0.5), 1, None) == INVALID
+    H = 1025
+    dec = (ctypes.c_float * H)(*([0.5] * H))
+    assert f(P, P, P, P, P, OUT, 1, H, 64, dec, 1, None) == UNSUPPORTED
+    assert f(P, P, P, P, P, OUT, 0, 2, 64, floats(0.5, 0.5), 1, None) == OK
