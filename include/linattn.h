@@ -58,6 +58,15 @@ typedef enum {
 
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 
+/* Method variant for la_forward_variant / la_decode_step_variant. */
+typedef enum { LA_PHI_ELU1 = 0, LA_PHI_IDENTITY = 1 } la_feature_map;
+typedef struct {
+    int feature_map; /* LA_PHI_ELU1: phi(x) = elu(x) + 1 (the default);
+                        LA_PHI_IDENTITY: phi(x) = x                         */
+    int normalise;   /* 1: divide by phi(q)^T z (the default); 0: no
+                        denominator                                         */
+} la_variant;
+
 /* Largest head dimension accepted by any entry point. */
 #define LA_MAX_D 256
 /* Largest number of heads for which a per-head decay can be given. */
@@ -202,6 +211,31 @@ la_status la_forward_causal_state(const void *q, const void *k, const void *v,
                                   void *out, float *S, float *z, int B, int H,
                                   int N, int d, const float *decay,
                                   la_dtype dtype, la_stream_t stream);
+
+/*
+ * la_forward_variant / la_decode_step_variant -- la_forward_ex (automatic
+ * kernel and segment choice) and la_decode_step_ex with the feature map and
+ * the normaliser selectable.  With {LA_PHI_IDENTITY, 0} and a decay this is
+ * retention ("Story of Attention - Part 5", section 4: recurrent form
+ * S_t = g S_{t-1} + k_t v_t^T, o_t = q_t S_t; parallel form (Q K^T (.) D) V
+ * with D_ij = g^(i-j) for i >= j); with {LA_PHI_ELU1, 0} linear attention
+ * without the denominator.
+ *   variant  NULL for {LA_PHI_ELU1, 1} (then identical to la_forward_ex /
+ *            la_decode_step_ex); LA_ERR_INVALID_ARG for a feature_map other
+ *            than the two above or a normalise other than 0 or 1.
+ * Without the normaliser z is still carried (and, for the decode step,
+ * updated) but not used.  Other arguments and errors as la_forward and
+ * la_decode_step_ex.
+ */
+la_status la_forward_variant(const void *q, const void *k, const void *v,
+                             void *out, int B, int H, int N, int d, int causal,
+                             const float *decay, la_dtype dtype,
+                             const la_variant *variant, la_stream_t stream);
+la_status la_decode_step_variant(float *S, float *z, const void *q,
+                                 const void *k, const void *v, void *out, int B,
+                                 int H, int d, const float *decay,
+                                 la_dtype dtype, const la_variant *variant,
+                                 la_stream_t stream);
 
 /* Size of the fixed device scratch used by la_forward_causal_noalloc. */
 #define LA_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -14,7 +14,7 @@ import os
 
 from . import build as _build
 
-__all__ = ["forward", "forward_causal_state", "forward_host",
+__all__ = ["forward", "forward_variant", "forward_causal_state", "forward_host",
            "host_workspace_bytes", "decode_step",
            "check_device_status",
            "kernel_launch_count", "LinAttnError",
@@ -29,7 +29,19 @@ EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_abi_version", "la_kernel_launch_count",
             "la_forward_causal_noalloc", "la_forward_host",
             "la_forward_host_workspace_bytes", "la_forward_causal_state",
-            "la_decode_step_ex")
+            "la_decode_step_ex", "la_forward_variant", "la_decode_step_variant")
+
+FEATURE_MAPS = {"elu1": 0, "identity": 1}
+
+
+class _Variant(ctypes.Structure):
+    _fields_ = [("feature_map", ctypes.c_int), ("normalise", ctypes.c_int)]
+
+
+def _variant(feature_map, normalise):
+    if feature_map not in FEATURE_MAPS:
+        raise ValueError(f"feature_map must be one of {sorted(FEATURE_MAPS)}")
+    return ctypes.byref(_Variant(FEATURE_MAPS[feature_map], int(bool(normalise))))
 
 _lib = None
 
@@ -57,6 +69,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.la_decode_step.argtypes = [V, V, V, V, V, V, I, I, I, I, V]
     lib.la_decode_step_ex.argtypes = [V, V, V, V, V, V, I, I, I, F, I, V]
     lib.la_forward_causal_state.argtypes = [V, V, V, V, V, V, I, I, I, I, F, I, V]
+    VP = ctypes.POINTER(_Variant)
+    lib.la_forward_variant.argtypes = [V, V, V, V, I, I, I, I, I, F, I, VP, V]
+    lib.la_decode_step_variant.argtypes = [V, V, V, V, V, V, I, I, I, F, I, VP, V]
     lib.la_forward_host.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V,
                                     ctypes.c_size_t, V]
     lib.la_forward_host_workspace_bytes.argtypes = [I, I, I, I, I]
@@ -71,6 +86,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.la_kernel_launch_count.restype = ctypes.c_ulonglong
     for n in ("la_forward", "la_forward_ex", "la_decode_step", "la_forward_host",
               "la_decode_step_ex", "la_forward_causal_state",
+              "la_forward_variant", "la_decode_step_variant",
               "la_check_device_status", "la_abi_version"):
         getattr(lib, n).restype = I
     if path is None:
@@ -150,6 +166,32 @@ def forward(q, k, v, causal: bool = True, decay=None, out=None, *,
     return out
 
 
+def forward_variant(q, k, v, causal: bool = True, decay=None, out=None, *,
+                    feature_map: str = "elu1", normalise: bool = True,
+                    stream=None):
+    """forward() with the feature map ("elu1" or "identity") and the
+    normaliser selectable.  feature_map="identity", normalise=False with a
+    decay is retention: o_i = sum_{j<=i} g^(i-j) (q_i . k_j) v_j."""
+    torch = _torch()
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda(q, k, v, out)
+    B, H, N, d = q.shape
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_forward_variant(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            B, H, N, d, int(bool(causal)), _decay_arg(decay, H), _dtype_code(q),
+            _variant(feature_map, normalise), _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out
+
+
 def forward_causal_state(q, k, v, decay=None, out=None, S=None, z=None, *,
                          stream=None):
     """Causal forward that also returns the final state: (out, S, z) with
@@ -185,11 +227,13 @@ def forward_causal_state(q, k, v, decay=None, out=None, S=None, z=None, *,
     return out, S, z
 
 
-def decode_step(S, z, q, k, v, out=None, *, decay=None, stream=None):
+def decode_step(S, z, q, k, v, out=None, *, decay=None, feature_map="elu1",
+                normalise=True, stream=None):
     """One decode step per head: S, z (fp32, [B, H, d, d] / [B, H, d]) are
     updated in place (S <- g S + phi(k) v^T, z <- g z + phi(k), with the
     per-head decay g from `decay`, H floats in [0, 1], or 1); q, k, v
-    [B, H, d]; returns out [B, H, d]."""
+    [B, H, d]; returns out [B, H, d].  feature_map / normalise as in
+    forward_variant."""
     torch = _torch()
     if q.dim() != 3 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must share one [B, H, d] shape")
@@ -205,12 +249,12 @@ def decode_step(S, z, q, k, v, out=None, *, decay=None, stream=None):
     _check_cuda(S, z, q, k, v, out)
     lib = load_library()
     with torch.cuda.device(q.device):
-        st = lib.la_decode_step_ex(
+        st = lib.la_decode_step_variant(
             ctypes.c_void_p(S.data_ptr()), ctypes.c_void_p(z.data_ptr()),
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
             B, H, d, _decay_arg(decay, H), _dtype_code(q),
-            _stream_ptr(stream, q.device))
+            _variant(feature_map, normalise), _stream_ptr(stream, q.device))
     _raise_if(st)
     return out
 

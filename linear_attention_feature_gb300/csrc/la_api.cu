@@ -121,7 +121,17 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
                         int segment_chunks, la_stream_t stream) {
     return la::forward_with_workspace(q, k, v, out, B, H, N, d, causal, decay,
                                       dtype, path, segment_chunks, nullptr, 0,
-                                      nullptr, nullptr, stream);
+                                      nullptr, nullptr, nullptr, stream);
+}
+
+__attribute__((visibility("default")))
+la_status la_forward_variant(const void *q, const void *k, const void *v,
+                             void *out, int B, int H, int N, int d, int causal,
+                             const float *decay, la_dtype dtype,
+                             const la_variant *variant, la_stream_t stream) {
+    return la::forward_with_workspace(q, k, v, out, B, H, N, d, causal, decay,
+                                      dtype, 0, 0, nullptr, 0, nullptr, nullptr,
+                                      variant, stream);
 }
 
 __attribute__((visibility("default")))
@@ -134,7 +144,7 @@ la_status la_forward_causal_state(const void *q, const void *k, const void *v,
     if ((reinterpret_cast<uintptr_t>(S) & 15u) != 0)
         return fail(LA_ERR_INVALID_ARG, "la_forward_causal_state: S must be 16-byte aligned");
     return la::forward_with_workspace(q, k, v, out, B, H, N, d, 1, decay, dtype,
-                                      0, 0, nullptr, 0, S, z, stream);
+                                      0, 0, nullptr, 0, S, z, nullptr, stream);
 }
 
 __attribute__((visibility("default")))
@@ -152,7 +162,12 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
                                      int causal, const float *decay,
                                      la_dtype dtype, int path, int segment_chunks,
                                      void *ws, size_t ws_bytes, float *S_out,
-                                     float *z_out, la_stream_t stream) {
+                                     float *z_out, const la_variant *variant,
+                                     la_stream_t stream) {
+    if (variant && ((variant->feature_map != LA_PHI_ELU1 &&
+                     variant->feature_map != LA_PHI_IDENTITY) ||
+                    (variant->normalise != 0 && variant->normalise != 1)))
+        return fail(LA_ERR_INVALID_ARG, "la_forward_variant: unknown variant");
     DecayArgs dk;
     la_status st = validate_forward(q, k, v, out, B, H, N, d, causal, decay,
                                     dtype, &dk);
@@ -162,6 +177,10 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
     if (segment_chunks < 0)
         return fail(LA_ERR_INVALID_ARG, "la_forward_ex: segment_chunks < 0");
     FwdShape sh{B, H, N, d};
+    if (variant) {
+        sh.phi = variant->feature_map == LA_PHI_ELU1 ? 1 : 0;
+        sh.norm = variant->normalise;
+    }
     if (sh.BH() == 0) return LA_OK;
     if (sh.BH() > 2147483647LL || (long long)N * d > (1LL << 40))
         return fail(LA_ERR_UNSUPPORTED, "la_forward: problem too large");
@@ -211,10 +230,17 @@ size_t la::forward_workspace_bytes(int B, int H, int N, int d, int causal,
 extern "C" {
 
 __attribute__((visibility("default")))
-la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k,
-                            const void *v, void *out, int B, int H, int d,
-                            const float *decay, la_dtype dtype,
-                            la_stream_t stream) {
+la_status la_decode_step_variant(float *S, float *z, const void *q,
+                                 const void *k, const void *v, void *out, int B,
+                                 int H, int d, const float *decay,
+                                 la_dtype dtype, const la_variant *variant,
+                                 la_stream_t stream) {
+    if (variant && ((variant->feature_map != LA_PHI_ELU1 &&
+                     variant->feature_map != LA_PHI_IDENTITY) ||
+                    (variant->normalise != 0 && variant->normalise != 1)))
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step_variant: unknown variant");
+    const int phi = (!variant || variant->feature_map == LA_PHI_ELU1) ? 1 : 0;
+    const int norm = variant ? variant->normalise : 1;
     if (!S || !z || !q || !k || !v || !out)
         return fail(LA_ERR_INVALID_ARG, "la_decode_step: null pointer");
     if (B < 0 || H < 0)
@@ -243,11 +269,20 @@ la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k,
     if (BH == 0) return LA_OK;
     if (BH > 2147483647LL)
         return fail(LA_ERR_UNSUPPORTED, "la_decode_step: too many heads");
-    cudaError_t e = launch_decode_step(S, z, q, k, v, out, BH, d, dk, dtype,
-                                       reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_decode_step(S, z, q, k, v, out, BH, d, dk, phi, norm,
+                                       dtype, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
     note_launches(1);
     return LA_OK;
+}
+
+__attribute__((visibility("default")))
+la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k,
+                            const void *v, void *out, int B, int H, int d,
+                            const float *decay, la_dtype dtype,
+                            la_stream_t stream) {
+    return la_decode_step_variant(S, z, q, k, v, out, B, H, d, decay, dtype,
+                                  nullptr, stream);
 }
 
 __attribute__((visibility("default")))

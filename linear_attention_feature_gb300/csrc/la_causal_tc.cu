@@ -80,6 +80,7 @@ struct Params {
     float *agg, *incl;  // [items][DK * DV + DK]: S rows (a-major), then z
     int *flags;         // [items]
     float *S_out, *z_out;  // final state [BH][DK][DK] / [BH][DK], or NULL
+    int phi, norm;         // elu(x) + 1 on q, k (else identity); divide by den
     int *ctrl;          // [0] ticket counter, [1] abort flag
     int *status;        // device status word
     long long timeout;  // clock cycles per bounded wait
@@ -385,30 +386,35 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
 // ---------------------------------------------------------------- transform
 
 // phi (bf16 pairs) over this thread's share of one row of a [128][DK]
-// swizzled tile, in place; rows with `zero` set become 0.
+// swizzled tile, in place (identity when `phi` is false); rows with `zero`
+// set become 0.
 template <int DK>
 __device__ __forceinline__ void transform_row(uint8_t *tile, int row, int part,
-                                              bool zero) {
+                                              bool zero, bool phi) {
     constexpr int NCH = DK / 16;  // 16-byte chunks per thread (half a row)
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
         const int cc = part * NCH + i;
         const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
         const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
-        uint4 y;
-        y.x = phi2(x.x);
-        y.y = phi2(x.y);
-        y.z = phi2(x.z);
-        y.w = phi2(x.w);
+        uint4 y = x;
+        if (phi) {
+            y.x = phi2(x.x);
+            y.y = phi2(x.y);
+            y.z = phi2(x.z);
+            y.w = phi2(x.w);
+        }
         if (zero) y = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4 *>(tile + off) = y;
     }
 }
 
-// Khat = w phi(K) in place (phase A weights relative to the segment end).
+// Khat = w phi(K) in place (phase A weights relative to the segment end);
+// w K with the identity feature map.
 template <int DK>
 __device__ __forceinline__ void transform_row_scaled(uint8_t *tile, int row,
-                                                     int part, uint32_t w2) {
+                                                     int part, uint32_t w2,
+                                                     bool phi) {
     constexpr int NCH = DK / 16;
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
@@ -416,10 +422,10 @@ __device__ __forceinline__ void transform_row_scaled(uint8_t *tile, int row,
         const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
         const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
         uint4 y;
-        y.x = bf2_mul(phi2(x.x), w2);
-        y.y = bf2_mul(phi2(x.y), w2);
-        y.z = bf2_mul(phi2(x.z), w2);
-        y.w = bf2_mul(phi2(x.w), w2);
+        y.x = bf2_mul(phi ? phi2(x.x) : x.x, w2);
+        y.y = bf2_mul(phi ? phi2(x.y) : x.y, w2);
+        y.z = bf2_mul(phi ? phi2(x.z) : x.z, w2);
+        y.w = bf2_mul(phi ? phi2(x.w) : x.w, w2);
         *reinterpret_cast<uint4 *>(tile + off) = y;
     }
 }
@@ -462,9 +468,9 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                 const int tok = c * C + row;
                 if (kDecay || tok >= p.N) {
                     const float w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
-                    transform_row_scaled<DK>(kt, row, part, bf2_splat(w));
+                    transform_row_scaled<DK>(kt, row, part, bf2_splat(w), p.phi);
                 } else {
-                    transform_row<DK>(kt, row, part, false);
+                    transform_row<DK>(kt, row, part, false, p.phi);
                 }
                 fence_async_shared();
                 named_bar_sync(BAR_T, kTThreads);
@@ -477,8 +483,8 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             uint8_t *qt = smem + st * L::STAGE + L::OFF_Q;
             uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
             const int n = min(C, p.N - c * C);
-            transform_row<DK>(qt, row, part, false);
-            transform_row<DK>(kt, row, part, row >= n);  // rows past N -> 0
+            transform_row<DK>(qt, row, part, false, p.phi);
+            transform_row<DK>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
@@ -582,7 +588,7 @@ __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
                                              const Ctx &cx, uint32_t lb,
                                              int row, int et, float wq,
                                              const Item &it, int c, int j,
-                                             int nb, int &pend,
+                                             int nb, int &pend, bool norm,
                                              const CUtensorMap *to) {
     using L = Layout<DK, kDecay>;
     constexpr bool kDefer = !L::OWN_OST && L::STAGES >= 3;
@@ -611,7 +617,7 @@ __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
             reg_fence(oi);
             reg_fence(dreg);
             reg_fence(direg);
-            inv = 1.f / fmaf(wq, u2f(direg), u2f(dreg));
+            inv = norm ? 1.f / fmaf(wq, u2f(direg), u2f(dreg)) : 1.f;
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 o[e] = __float_as_uint(fmaf(wq, u2f(oi[e]), u2f(o[e])));
@@ -619,7 +625,7 @@ __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
             tmem_wait_ld();
             reg_fence(o);
             reg_fence(dreg);
-            inv = 1.f / u2f(dreg);
+            inv = norm ? 1.f / u2f(dreg) : 1.f;
         }
         if (h == 1) {
             tc_fence_before();
@@ -1023,7 +1029,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 if (et == 0) mbar_arrive(&sm.sb_ready);
             }
             output_chunk<DK, kDecay>(smem, sm, cx, lb, row, et, wq, it, c, j, nb,
-                                     pend, to);
+                                     pend, p.norm != 0, to);
         }
         if (et == 0 && pend >= 0) {  // the item's last store: release its stage
             tma_store_wait_read<0>();
@@ -1237,6 +1243,8 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.timeout = 1LL << 32;
     p.S_out = S_out;
     p.z_out = z_out;
+    p.phi = sh.phi;
+    p.norm = sh.norm;
 
     // the caller's workspace when given, else a stream-ordered allocation
     void *ws = ws_in;
@@ -1391,6 +1399,8 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     p.nseg = (p.nchunks + seg - 1) / seg;
     p.items = (int)items;
     p.timeout = 1LL << 32;
+    p.phi = 1;
+    p.norm = 1;
     p.ctrl = reinterpret_cast<int *>(scratch);
     p.flags = reinterpret_cast<int *>(scratch + 256);
     p.agg = reinterpret_cast<float *>(scratch + off_agg);

@@ -2,7 +2,9 @@
 // out = phi(q)^T S / phi(q)^T z  ("Linear Attention", running statistics and
 // the O(d^2)-per-token inference cost; g the per-head decay of the
 // forget-gate passage, 1 without decay).  g = 1 multiplies by one exactly, so
-// the undecayed step is unchanged.
+// the undecayed step is unchanged.  The retention variant ("Story of
+// Attention - Part 5", section 4, recurrent form) uses the identity for phi
+// and no denominator.
 //
 // The step is a pure stream over the fp32 d x d state (read once, written
 // once): 2 * 4 * d^2 bytes per head against ~4 d^2 flops, so it is bound by
@@ -30,8 +32,9 @@ __device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) {
     *p = __float2bfloat16_rn(x);
 }
-__device__ __forceinline__ float phi(float x) {
-    return x > 0.f ? x + 1.f : expf(x);
+// elu(x) + 1, alpha = 1; the identity when `use_phi` is false
+__device__ __forceinline__ float fm(bool use_phi, float x) {
+    return use_phi ? (x > 0.f ? x + 1.f : expf(x)) : x;
 }
 
 // Shared prologue: phi(k), phi(q) into shared memory; z <- z + phi(k) and
@@ -40,13 +43,14 @@ template <typename T>
 __device__ __forceinline__ void decode_prologue(float *__restrict__ zh,
                                                 const T *__restrict__ qh,
                                                 const T *__restrict__ kh,
-                                                int d, float g, float *sk, float *sq,
+                                                int d, float g, bool use_phi,
+                                                float *sk, float *sq,
                                                 float *swarp, float *sden) {
     const int tid = threadIdx.x;
     float part = 0.f;
     for (int a = tid; a < d; a += kThreads) {
-        float pk = phi(ld_in(kh + a));
-        float pq = phi(ld_in(qh + a));
+        float pk = fm(use_phi, ld_in(kh + a));
+        float pq = fm(use_phi, ld_in(qh + a));
         sk[a] = pk;
         sq[a] = pq;
         float zn = fmaf(g, zh[a], pk);
@@ -69,7 +73,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
                   const T *__restrict__ q, const T *__restrict__ k,
-                  const T *__restrict__ v, T *__restrict__ out, DecayArgs dk) {
+                  const T *__restrict__ v, T *__restrict__ out, DecayArgs dk,
+                  int use_phi, int norm) {
     constexpr int NCG = D / 4;                 // column groups (float4 each)
     constexpr int NRG = kThreads / NCG;        // row groups
     constexpr int RPT = D / NRG;               // rows per thread
@@ -86,7 +91,7 @@ decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
     float4 *__restrict__ Sh = reinterpret_cast<float4 *>(S + (size_t)bh * D * D);
     const float g = decay_of(dk, (int)bh);
     decode_prologue<T>(z + (size_t)bh * D, q + (size_t)bh * D,
-                       k + (size_t)bh * D, D, g, sk, sq, swarp, &sden);
+                       k + (size_t)bh * D, D, g, use_phi != 0, sk, sq, swarp, &sden);
     const T *vh = v + (size_t)bh * D + 4 * cg;
     const float v0 = ld_in(vh), v1 = ld_in(vh + 1), v2 = ld_in(vh + 2),
                 v3 = ld_in(vh + 3);
@@ -123,7 +128,7 @@ decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
             float4 u = red[r][tid];
             t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
         }
-        const float inv = 1.f / sden;
+        const float inv = norm ? 1.f / sden : 1.f;
         T *o = out + (size_t)bh * D + 4 * tid;
         st_out(o, t.x * inv);
         st_out(o + 1, t.y * inv);
@@ -139,14 +144,14 @@ __global__ void __launch_bounds__(kThreads)
 decode_generic_kernel(float *__restrict__ S, float *__restrict__ z,
                       const T *__restrict__ q, const T *__restrict__ k,
                       const T *__restrict__ v, T *__restrict__ out, int d,
-                      DecayArgs dk) {
+                      DecayArgs dk, int use_phi, int norm) {
     __shared__ float sk[LA_MAX_D], sq[LA_MAX_D];
     __shared__ float swarp[kThreads / 32], sden;
     const long long bh = blockIdx.x;
     float *Sh = S + (size_t)bh * d * d;
     const float g = decay_of(dk, (int)bh);
     decode_prologue<T>(z + (size_t)bh * d, q + (size_t)bh * d,
-                       k + (size_t)bh * d, d, g, sk, sq, swarp, &sden);
+                       k + (size_t)bh * d, d, g, use_phi != 0, sk, sq, swarp, &sden);
     __syncthreads();
     for (int c = threadIdx.x; c < d; c += kThreads) {
         const float vc = ld_in(v + (size_t)bh * d + c);
@@ -156,27 +161,27 @@ decode_generic_kernel(float *__restrict__ S, float *__restrict__ z,
             Sh[(size_t)a * d + c] = s;
             acc = fmaf(sq[a], s, acc);
         }
-        st_out(out + (size_t)bh * d + c, acc / sden);
+        st_out(out + (size_t)bh * d + c, norm ? acc / sden : acc);
     }
 }
 
 template <typename T>
 cudaError_t launch_t(float *S, float *z, const void *q, const void *k,
                      const void *v, void *out, long long BH, int d,
-                     const DecayArgs &dk, cudaStream_t stream) {
+                     const DecayArgs &dk, int phi, int norm, cudaStream_t stream) {
     const T *qq = static_cast<const T *>(q), *kk = static_cast<const T *>(k),
             *vv = static_cast<const T *>(v);
     T *oo = static_cast<T *>(out);
     const bool aligned = (reinterpret_cast<uintptr_t>(S) & 15u) == 0;
     dim3 grid((unsigned)BH);
     if (aligned && d == 128)
-        decode_vec_kernel<T, 128><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk);
+        decode_vec_kernel<T, 128><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm);
     else if (aligned && d == 64)
-        decode_vec_kernel<T, 64><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk);
+        decode_vec_kernel<T, 64><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm);
     else if (aligned && d == 256)
-        decode_vec_kernel<T, 256><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk);
+        decode_vec_kernel<T, 256><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm);
     else
-        decode_generic_kernel<T><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, d, dk);
+        decode_generic_kernel<T><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, d, dk, phi, norm);
     return cudaGetLastError();
 }
 
@@ -185,9 +190,11 @@ cudaError_t launch_t(float *S, float *z, const void *q, const void *k,
 cudaError_t launch_decode_step(float *S, float *z, const void *q,
                                const void *k, const void *v, void *out,
                                long long BH, int d, const DecayArgs &dk,
-                               la_dtype dtype, cudaStream_t stream) {
-    if (dtype == LA_F32) return launch_t<float>(S, z, q, k, v, out, BH, d, dk, stream);
-    return launch_t<__nv_bfloat16>(S, z, q, k, v, out, BH, d, dk, stream);
+                               int phi, int norm, la_dtype dtype,
+                               cudaStream_t stream) {
+    if (dtype == LA_F32)
+        return launch_t<float>(S, z, q, k, v, out, BH, d, dk, phi, norm, stream);
+    return launch_t<__nv_bfloat16>(S, z, q, k, v, out, BH, d, dk, phi, norm, stream);
 }
 
 }  // namespace la

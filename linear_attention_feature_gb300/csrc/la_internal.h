@@ -21,9 +21,12 @@ __host__ __device__ inline float decay_of(const DecayArgs &dk, int bh) {
     return dk.has ? dk.g[bh % dk.H] : 1.0f;
 }
 
-// Common shape of a full-sequence call.
+// Common shape of a full-sequence call, with the method variant: phi = 1
+// applies elu(x) + 1 to q and k (0: identity), norm = 1 divides by the
+// normaliser phi(q)^T z (0: no denominator, as in retention).
 struct FwdShape {
     int B, H, N, d;
+    int phi = 1, norm = 1;
     long long BH() const { return (long long)B * H; }
 };
 
@@ -36,10 +39,12 @@ cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
                                 float *S_out, float *z_out, cudaStream_t stream);
 
 // ---- recurrent decode step ----
+// phi / norm as in FwdShape.
 cudaError_t launch_decode_step(float *S, float *z, const void *q,
                                const void *k, const void *v, void *out,
                                long long BH, int d, const DecayArgs &decay,
-                               la_dtype dtype, cudaStream_t stream);
+                               int phi, int norm, la_dtype dtype,
+                               cudaStream_t stream);
 
 // Address of the current device's two status words (kernels set word 0 to a
 // non-zero la_status when a bounded wait gives up, and word 1 to where).
@@ -55,12 +60,13 @@ void set_last_error(const char *msg);
 // la_forward_ex with an optional caller-owned scratch for the tensor-core
 // kernels (ws = NULL: they allocate it stream-ordered themselves).
 // S_out / z_out (causal only, may be NULL): also write the final state.
+// `variant` NULL: elu(x) + 1 with the normaliser.
 la_status forward_with_workspace(const void *q, const void *k, const void *v,
                                  void *out, int B, int H, int N, int d,
                                  int causal, const float *decay, la_dtype dtype,
                                  int path, int segment_chunks, void *ws,
                                  size_t ws_bytes, float *S_out, float *z_out,
-                                 la_stream_t stream);
+                                 const la_variant *variant, la_stream_t stream);
 
 // Scratch bytes forward_with_workspace needs (automatic path and segment
 // length; 0 where the CUDA-core kernels run, which need none).

@@ -48,6 +48,7 @@ struct Params {
     int grp2, ngrp2, items2;  // pass 2: chunks per group, groups, items
     float *part;              // [items1][STATE]
     int *cnt;                 // [BH * nhalf] partials counted in
+    int phi, norm;            // elu(x) + 1 on q, k (else identity); divide by den
     int *ctrl;                // [0] ticket counter, [1] abort flag
     int *status;
     long long timeout;
@@ -204,14 +205,14 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
 // place; rows past the sequence end become 0 when `zero` is set.
 template <int DK>
 __device__ __forceinline__ void transform_row(uint8_t *tile, int row, int part,
-                                              bool zero) {
+                                              bool zero, bool phi) {
     constexpr int NCH = DK / 16;
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
         const int cc = part * NCH + i;
         const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
         const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
-        uint4 y = make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w));
+        uint4 y = phi ? make_uint4(phi2(x.x), phi2(x.y), phi2(x.z), phi2(x.w)) : x;
         if (zero) y = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4 *>(tile + off) = y;
     }
@@ -234,7 +235,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             // phi(K) rows past the end must be 0 (they would add keys);
             // phi(Q) rows past the end produce outputs that are not stored
             transform_row<DK>(smem + st * L::STAGE + L::OFF_T, row, part,
-                              !it.pass2 && c * C + row >= p.N);
+                              !it.pass2 && c * C + row >= p.N, p.phi);
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
@@ -357,7 +358,7 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
                 tmem_wait_ld();
                 reg_fence(o);
                 reg_fence(dreg);
-                const float inv = 1.f / u2f(dreg);
+                const float inv = p.norm ? 1.f / u2f(dreg) : 1.f;
 #pragma unroll
                 for (int e = 0; e < 32; e += 2)
                     packed[16 * h + (e >> 1)] =
@@ -534,6 +535,8 @@ TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
     p.nseg1 = p.ngrp2 = pl.nseg;
     p.items1 = p.items2 = (int)pl.items;
     p.timeout = 1LL << 32;
+    p.phi = sh.phi;
+    p.norm = sh.norm;
     // the caller's workspace when given, else a stream-ordered allocation
     void *ws = ws_in;
     if (ws) {

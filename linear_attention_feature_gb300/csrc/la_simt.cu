@@ -33,9 +33,9 @@ __device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) {
     *p = __float2bfloat16_rn(x);
 }
 
-// elu(x) + 1, alpha = 1
-__device__ __forceinline__ float phi(float x) {
-    return x > 0.f ? x + 1.f : expf(x);
+// elu(x) + 1, alpha = 1; the identity when `use_phi` is false
+__device__ __forceinline__ float fm(bool use_phi, float x) {
+    return use_phi ? (x > 0.f ? x + 1.f : expf(x)) : x;
 }
 
 template <typename T, bool kCausal>
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads)
 simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, T *__restrict__ out, int N,
                     int d, DecayArgs decay, float *__restrict__ S_out,
-                    float *__restrict__ z_out) {
+                    float *__restrict__ z_out, int use_phi, int norm) {
     extern __shared__ float smem[];
     const int cb = blockIdx.x;
     const long long bh = blockIdx.y;
@@ -73,7 +73,7 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
         for (int t0 = 0; t0 < N; t0 += kT) {
             const int n = min(kT, N - t0);
             for (int i = tid; i < n * d; i += kThreads)
-                pk[i] = phi(ld_in(k + base + (size_t)t0 * d + i));
+                pk[i] = fm(use_phi, ld_in(k + base + (size_t)t0 * d + i));
             for (int i = tid; i < n * kCB; i += kThreads) {
                 int t = i / kCB, c = i % kCB;
                 pv[i] = c < cw ? ld_in(v + base + (size_t)(t0 + t) * d + c0 + c)
@@ -97,7 +97,7 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
         for (int t0 = 0; t0 < N; t0 += kT) {
             const int n = min(kT, N - t0);
             for (int i = tid; i < n * d; i += kThreads)
-                pq[i] = phi(ld_in(q + base + (size_t)t0 * d + i));
+                pq[i] = fm(use_phi, ld_in(q + base + (size_t)t0 * d + i));
             __syncthreads();
             for (int i = tid; i < n; i += kThreads) {
                 float s = 0.f;
@@ -110,7 +110,7 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
                 if (c >= cw) continue;
                 float s = 0.f;
                 for (int a = 0; a < d; ++a) s = fmaf(pq[t * d + a], S[a * kCB + c], s);
-                st_out(out + base + (size_t)(t0 + t) * d + c0 + c, s / den[t]);
+                st_out(out + base + (size_t)(t0 + t) * d + c0 + c, norm ? s / den[t] : s);
             }
             __syncthreads();
         }
@@ -118,8 +118,8 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
     for (int t0 = 0; t0 < N; t0 += kT) {
         const int n = min(kT, N - t0);
         for (int i = tid; i < n * d; i += kThreads) {
-            pq[i] = phi(ld_in(q + base + (size_t)t0 * d + i));
-            pk[i] = phi(ld_in(k + base + (size_t)t0 * d + i));
+            pq[i] = fm(use_phi, ld_in(q + base + (size_t)t0 * d + i));
+            pk[i] = fm(use_phi, ld_in(k + base + (size_t)t0 * d + i));
         }
         for (int i = tid; i < n * kCB; i += kThreads) {
             int t = i / kCB, c = i % kCB;
@@ -152,8 +152,8 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
             float s = 0.f, r = 0.f;
             for (int j = 0; j <= i; ++j) s = fmaf(A[i * kT + j], pv[j * kCB + c], s);
             for (int a = 0; a < d; ++a) r = fmaf(pq[i * d + a], S[a * kCB + c], r);
-            st_out(out + base + (size_t)(t0 + i) * d + c0 + c,
-                   (s + gp[i + 1] * r) / den[i]);
+            const float num = s + gp[i + 1] * r;
+            st_out(out + base + (size_t)(t0 + i) * d + c0 + c, norm ? num / den[i] : num);
         }
         __syncthreads();
         // state update
@@ -199,7 +199,7 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, void *out,
     kern<<<grid, kThreads, smem, stream>>>(
         static_cast<const T *>(q), static_cast<const T *>(k),
         static_cast<const T *>(v), static_cast<T *>(out), sh.N, d, decay, S_out,
-        z_out);
+        z_out, sh.phi, sh.norm);
     return cudaGetLastError();
 }
 

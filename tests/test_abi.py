@@ -207,3 +207,27 @@ def test_decode_step_ex_rejects_bad_decay(lib):
     dec = (ctypes.c_float * H)(*([0.5] * H))
     assert f(P, P, P, P, P, OUT, 1, H, 64, dec, 1, None) == UNSUPPORTED
     assert f(P, P, P, P, P, OUT, 0, 2, 64, floats(0.5, 0.5), 1, None) == OK
+
+
+_Var = la._Variant  # the binding's la_variant struct (ctypes type checks it)
+
+
+@pytest.mark.parametrize("fmap, norm", [(2, 1), (-1, 0), (0, 2), (1, -1)])
+def test_variant_entry_points_reject_unknown_variants(lib, fmap, norm):
+    var = ctypes.byref(_Var(fmap, norm))
+    assert lib.la_forward_variant(P, P2, P3, OUT, 1, 2, 8, 64, 1, None, 1, var,
+                                  None) == INVALID
+    assert "variant" in lib.la_last_error().decode()
+    assert lib.la_decode_step_variant(P, P, P, P, P, OUT, 1, 2, 64, None, 1, var,
+                                      None) == INVALID
+
+
+def test_variant_null_and_valid_variants_pass_validation(lib):
+    # NULL and the four valid variants get past validation: an empty problem
+    # then returns LA_OK without touching a GPU
+    for var in (None, ctypes.byref(_Var(0, 1)), ctypes.byref(_Var(1, 0)),
+                ctypes.byref(_Var(0, 0)), ctypes.byref(_Var(1, 1))):
+        assert lib.la_forward_variant(P, P2, P3, OUT, 0, 2, 8, 64, 1, None, 1, var,
+                                      None) == OK
+        assert lib.la_decode_step_variant(P, P, P, P, P, OUT, 0, 2, 64, None, 1, var,
+                                          None) == OK
