@@ -360,7 +360,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
     Kx, Wx = max(3, args.steps // 2), max(3, args.warmup)
 
     def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2, kernel=None,
-                 state=False):
+                 state=False, retention=False):
         w = wl.WORKLOADS[wkey]
         try:
             if inputs is None:
@@ -370,6 +370,11 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
             oo = torch.empty_like(qq)
             fn = lambda: la.forward(qq, kk, vv, causal=causal, decay=decay, out=oo)  # noqa
             extra = 0
+            if retention:
+                # identity feature map, no normaliser (retention)
+                fn = lambda: la.forward_variant(qq, kk, vv, causal=causal, decay=decay,  # noqa
+                                                out=oo, feature_map="identity",
+                                                normalise=False)
             if state:
                 # forward plus the final state (the prefill of a decode)
                 Ss = torch.empty(w.B, w.H, w.d, w.d, device=dev)
@@ -405,6 +410,8 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
     fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
     fwd_path(f"{MAIN} causal with final state", MAIN, True, inputs=(q, k, v),
              state=True)
+    fwd_path("bf16_decay_b4h8_n16384_d128 retention", wd.name, True,
+             decay=list(wd.decay), retention=True)
     try:
         res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,
                                                 args)

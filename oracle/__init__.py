@@ -65,11 +65,12 @@ def _load():
     lib.ora_recurrent_step.argtypes = [P, P, P, P, P, P, L, ctypes.c_double, I, I]
     lib.ora_causal.argtypes = [P, P, P, P, L, L, L, P, I, I, I]
     lib.ora_causal_state.argtypes = [P, P, P, P, L, L, L, P, I]
+    lib.ora_causal_gated.argtypes = [P, P, P, P, P, L, L, L, I, I, I]
     lib.ora_decode_step.argtypes = [P, P, P, P, P, P, L, L, P, I]
     lib.ora_quadratic.argtypes = [P, P, P, P, L, L, L, P, I, I, P]
     lib.ora_chunked.argtypes = [P, P, P, P, L, L, L, P, L, L]
     for name in ("ora_noncausal_state", "ora_state_read", "ora_noncausal",
-                 "ora_causal_state",
+                 "ora_causal_state", "ora_causal_gated",
                  "ora_recurrent_step", "ora_causal", "ora_decode_step",
                  "ora_quadratic", "ora_chunked"):
         getattr(lib, name).restype = I
@@ -175,6 +176,21 @@ def causal(q, k, v, decay=None, *, fmap=FMAP_ELU1, normalise=True,
     _check(_load().ora_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), BH, N, d,
                               _ptr(g) if g is not None else None, fmap,
                               int(normalise), int(nthreads)), "causal")
+    return out
+
+
+def causal_gated(q, k, v, alpha, *, fmap=FMAP_ELU1, normalise=True, nthreads=1):
+    """Causal recurrence with a scalar gate per token and head: alpha
+    [..., N] (the leading dimensions of q); inputs [..., N, d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    BH, N, d = _seq_shape(q)
+    a = np.ascontiguousarray(np.asarray(alpha, dtype=np.float64))
+    if a.shape != q.shape[:-1]:
+        raise ValueError("alpha must have the shape of q without its last axis")
+    out = np.empty_like(q)
+    _check(_load().ora_causal_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(out),
+                                    BH, N, d, fmap, int(normalise), int(nthreads)),
+           "causal_gated")
     return out
 
 

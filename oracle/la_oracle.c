@@ -227,6 +227,45 @@ int ora_causal(const double *q, const double *k, const double *v, double *out,
     return c.err;
 }
 
+/* Causal recurrence with a data-dependent scalar gate per token and head
+ * ("Linear Attention", GLA: S_t = G_t (.) S_{t-1} + k_t v_t^T with the gate
+ * produced from the input; "Story of Attention - Part 5", section 7, the
+ * scalar forget gate alpha_t of Gated DeltaNet), here with G_t = alpha_t
+ * and the normaliser gated like the state:
+ *   S_t = alpha_t S_{t-1} + phi(k_t) v_t^T,  z_t = alpha_t z_{t-1} + phi(k_t),
+ *   y_t = phi(q_t)^T S_t / phi(q_t)^T z_t   (update, then read).
+ * alpha [BH][N]. */
+typedef struct {
+    const double *q, *k, *v, *alpha;
+    double *out;
+    long N, d;
+    int fmap, normalise, err;
+} gated_ctx;
+
+static void gated_head(void *vctx, long h) {
+    gated_ctx *c = (gated_ctx *)vctx;
+    long N = c->N, d = c->d;
+    double *S = (double *)calloc((size_t)(d * d), sizeof(double));
+    double *z = (double *)calloc((size_t)d, sizeof(double));
+    if (!S || !z) { c->err = -2; free(S); free(z); return; }
+    for (long t = 0; t < N; ++t) {
+        long o = (h * N + t) * d;
+        ora_recurrent_step(S, z, c->q + o, c->k + o, c->v + o, c->out + o, d,
+                           c->alpha[h * N + t], c->fmap, c->normalise);
+    }
+    free(S);
+    free(z);
+}
+
+int ora_causal_gated(const double *q, const double *k, const double *v,
+                     const double *alpha, double *out, long BH, long N, long d,
+                     int fmap, int normalise, int nthreads) {
+    if (!q || !k || !v || !alpha || !out || BH < 0 || N < 0 || d <= 0) return -1;
+    gated_ctx c = {q, k, v, alpha, out, N, d, fmap, normalise, 0};
+    for_each_head(gated_head, &c, BH, nthreads);
+    return c.err;
+}
+
 /* Final state of the causal recurrence after all N tokens -- the state a
  * decode continues from ("Linear Attention", the running statistics S_n and
  * z_n; with the forget-gate passage's scalar g):

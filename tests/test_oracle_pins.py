@@ -175,6 +175,54 @@ def test_decode_steps_equal_causal(decay):
 
 
 # --------------------------------------------------------------------------
+# data-dependent scalar gate per token (GLA-style; Gated DeltaNet's alpha_t)
+
+
+def _gates(shape, seed, lo=0.5):
+    return np.random.default_rng(seed).uniform(lo, 1.0, shape)
+
+
+def test_gated_constant_gates_are_the_per_head_decay():
+    q, k, v = (_rand((2, 3, 12, 5), s) for s in (40, 41, 42))
+    dec = [0.9, 0.5, 1.0]
+    alpha = np.broadcast_to(np.asarray(dec)[None, :, None], (2, 3, 12))
+    np.testing.assert_allclose(oracle.causal_gated(q, k, v, alpha),
+                               oracle.causal(q, k, v, dec), rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("fmap, norm", [(oracle.FMAP_ELU1, True), (ID, False)])
+def test_gated_equals_masked_parallel_with_gate_products(fmap, norm):
+    # y_i = sum_{j<=i} w_ij v_j / sum_{j<=i} w_ij with
+    # w_ij = (phi(q_i) . phi(k_j)) prod_{t=j+1..i} alpha_t, written here with
+    # numpy (independently of the recurrence)
+    N, d = 15, 6
+    q, k, v = (_rand((1, 1, N, d), s) for s in (43, 44, 45))
+    a = _gates((1, 1, N), 46)
+    f = (lambda x: np.where(x > 0, x + 1.0, np.exp(x))) if fmap != ID else (lambda x: x)
+    fq, fk = f(q[0, 0]), f(k[0, 0])
+    W = np.zeros((N, N))
+    for i in range(N):
+        for j in range(i + 1):
+            W[i, j] = fq[i] @ fk[j] * np.prod(a[0, 0, j + 1:i + 1])
+    y = W @ v[0, 0]
+    if norm:
+        y = y / W.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(oracle.causal_gated(q, k, v, a, fmap=fmap, normalise=norm)[0, 0],
+                               y, rtol=1e-12, atol=1e-12)
+
+
+def test_gated_zero_gate_resets_the_state():
+    # alpha_t0 = 0 forgets everything before t0: from t0 on the outputs are
+    # those of a fresh sequence starting at t0
+    q, k, v = (_rand((1, 2, 20, 4), s) for s in (47, 48, 49))
+    a = _gates((1, 2, 20), 50)
+    a[..., 8] = 0.0
+    y = oracle.causal_gated(q, k, v, a)
+    y2 = oracle.causal_gated(q[..., 8:, :], k[..., 8:, :], v[..., 8:, :], a[..., 8:])
+    np.testing.assert_allclose(y[..., 8:, :], y2, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
 # final state of the causal recurrence (the state a decode continues from)
 
 
