@@ -237,6 +237,31 @@ la_status la_decode_step_variant(float *S, float *z, const void *q,
                                  la_dtype dtype, const la_variant *variant,
                                  la_stream_t stream);
 
+/*
+ * la_forward_gated / la_decode_step_gated -- the causal recurrence with a
+ * data-dependent scalar gate per token and head instead of a fixed decay:
+ * S_t = alpha_t S_{t-1} + phi(k_t) v_t^T, z_t = alpha_t z_{t-1} + phi(k_t),
+ * y_t = phi(q_t)^T S_t / phi(q_t)^T z_t ("Linear Attention", GLA's
+ * S_t = G_t (.) S_{t-1} + k_t v_t^T with G_t = alpha_t, the scalar forget
+ * gate alpha_t of "Story of Attention - Part 5", section 7).
+ *   gates    DEVICE fp32, [B][H][N] for la_forward_gated (alpha of every
+ *            token) or [B][H] for la_decode_step_gated (alpha of this step's
+ *            token), values in [0, 1].  The values are not checked (they live
+ *            on the device); outside [0, 1] the results are unspecified.
+ *   variant  as la_forward_variant (NULL: elu(x) + 1 with the normaliser).
+ * Other arguments as la_forward (causal) and la_decode_step.  The forward
+ * runs on the fp32 CUDA-core kernels for every dtype and head size; the
+ * decode step is the same kernel as la_decode_step.
+ */
+la_status la_forward_gated(const void *q, const void *k, const void *v,
+                           void *out, const float *gates, int B, int H, int N,
+                           int d, la_dtype dtype, const la_variant *variant,
+                           la_stream_t stream);
+la_status la_decode_step_gated(float *S, float *z, const void *q, const void *k,
+                               const void *v, void *out, const float *gates,
+                               int B, int H, int d, la_dtype dtype,
+                               const la_variant *variant, la_stream_t stream);
+
 /* Size of the fixed device scratch used by la_forward_causal_noalloc. */
 #define LA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

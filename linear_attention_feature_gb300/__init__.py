@@ -14,7 +14,8 @@ import os
 
 from . import build as _build
 
-__all__ = ["forward", "forward_variant", "forward_causal_state", "forward_host",
+__all__ = ["forward", "forward_variant", "forward_gated", "decode_step_gated",
+           "forward_causal_state", "forward_host",
            "host_workspace_bytes", "decode_step",
            "check_device_status",
            "kernel_launch_count", "LinAttnError",
@@ -29,7 +30,8 @@ EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_abi_version", "la_kernel_launch_count",
             "la_forward_causal_noalloc", "la_forward_host",
             "la_forward_host_workspace_bytes", "la_forward_causal_state",
-            "la_decode_step_ex", "la_forward_variant", "la_decode_step_variant")
+            "la_decode_step_ex", "la_forward_variant", "la_decode_step_variant",
+            "la_forward_gated", "la_decode_step_gated")
 
 FEATURE_MAPS = {"elu1": 0, "identity": 1}
 
@@ -72,6 +74,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     VP = ctypes.POINTER(_Variant)
     lib.la_forward_variant.argtypes = [V, V, V, V, I, I, I, I, I, F, I, VP, V]
     lib.la_decode_step_variant.argtypes = [V, V, V, V, V, V, I, I, I, F, I, VP, V]
+    lib.la_forward_gated.argtypes = [V, V, V, V, V, I, I, I, I, I, VP, V]
+    lib.la_decode_step_gated.argtypes = [V, V, V, V, V, V, V, I, I, I, I, VP, V]
     lib.la_forward_host.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V,
                                     ctypes.c_size_t, V]
     lib.la_forward_host_workspace_bytes.argtypes = [I, I, I, I, I]
@@ -87,6 +91,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     for n in ("la_forward", "la_forward_ex", "la_decode_step", "la_forward_host",
               "la_decode_step_ex", "la_forward_causal_state",
               "la_forward_variant", "la_decode_step_variant",
+              "la_forward_gated", "la_decode_step_gated",
               "la_check_device_status", "la_abi_version"):
         getattr(lib, n).restype = I
     if path is None:
@@ -187,6 +192,60 @@ def forward_variant(q, k, v, causal: bool = True, decay=None, out=None, *,
             ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
             B, H, N, d, int(bool(causal)), _decay_arg(decay, H), _dtype_code(q),
+            _variant(feature_map, normalise), _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out
+
+
+def forward_gated(q, k, v, gates, out=None, *, feature_map: str = "elu1",
+                  normalise: bool = True, stream=None):
+    """Causal recurrence with a data-dependent scalar gate per token and
+    head: gates [B, H, N] float32 on the GPU, values in [0, 1]
+    (S_t = gates_t S_{t-1} + phi(k_t) v_t^T, z likewise)."""
+    torch = _torch()
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, H, N, d = q.shape
+    if tuple(gates.shape) != (B, H, N) or gates.dtype != torch.float32:
+        raise ValueError("gates must be float32 [B, H, N]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda(q, k, v, out, gates)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_forward_gated(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(gates.data_ptr()), B, H, N, d, _dtype_code(q),
+            _variant(feature_map, normalise), _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out
+
+
+def decode_step_gated(S, z, q, k, v, gates, out=None, *, feature_map="elu1",
+                      normalise=True, stream=None):
+    """decode_step with this token's gate per head: gates [B, H] float32 on
+    the GPU (S <- gates S + phi(k) v^T, z likewise)."""
+    torch = _torch()
+    if q.dim() != 3 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, d] shape")
+    B, H, d = q.shape
+    if tuple(S.shape) != (B, H, d, d) or tuple(z.shape) != (B, H, d):
+        raise ValueError("S must be [B, H, d, d] and z [B, H, d]")
+    if tuple(gates.shape) != (B, H) or gates.dtype != torch.float32:
+        raise ValueError("gates must be float32 [B, H]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda(S, z, q, k, v, out, gates)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_decode_step_gated(
+            ctypes.c_void_p(S.data_ptr()), ctypes.c_void_p(z.data_ptr()),
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(gates.data_ptr()), B, H, d, _dtype_code(q),
             _variant(feature_map, normalise), _stream_ptr(stream, q.device))
     _raise_if(st)
     return out

@@ -121,7 +121,7 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
                         int segment_chunks, la_stream_t stream) {
     return la::forward_with_workspace(q, k, v, out, B, H, N, d, causal, decay,
                                       dtype, path, segment_chunks, nullptr, 0,
-                                      nullptr, nullptr, nullptr, stream);
+                                      nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 __attribute__((visibility("default")))
@@ -131,7 +131,7 @@ la_status la_forward_variant(const void *q, const void *k, const void *v,
                              const la_variant *variant, la_stream_t stream) {
     return la::forward_with_workspace(q, k, v, out, B, H, N, d, causal, decay,
                                       dtype, 0, 0, nullptr, 0, nullptr, nullptr,
-                                      variant, stream);
+                                      variant, nullptr, stream);
 }
 
 __attribute__((visibility("default")))
@@ -144,7 +144,7 @@ la_status la_forward_causal_state(const void *q, const void *k, const void *v,
     if ((reinterpret_cast<uintptr_t>(S) & 15u) != 0)
         return fail(LA_ERR_INVALID_ARG, "la_forward_causal_state: S must be 16-byte aligned");
     return la::forward_with_workspace(q, k, v, out, B, H, N, d, 1, decay, dtype,
-                                      0, 0, nullptr, 0, S, z, nullptr, stream);
+                                      0, 0, nullptr, 0, S, z, nullptr, nullptr, stream);
 }
 
 __attribute__((visibility("default")))
@@ -163,7 +163,7 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
                                      la_dtype dtype, int path, int segment_chunks,
                                      void *ws, size_t ws_bytes, float *S_out,
                                      float *z_out, const la_variant *variant,
-                                     la_stream_t stream) {
+                                     const float *gates, la_stream_t stream) {
     if (variant && ((variant->feature_map != LA_PHI_ELU1 &&
                      variant->feature_map != LA_PHI_IDENTITY) ||
                     (variant->normalise != 0 && variant->normalise != 1)))
@@ -195,10 +195,16 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    const bool tc_ok = tc_supported(sh, dtype, causal, q, k, v, out);
+    if (gates && !causal)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_gated: gates are defined for the causal form only");
+    if (gates && decay)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_gated: give gates or a decay, not both");
+    // the data-dependent gates run on the CUDA-core kernels
+    const bool tc_ok = !gates && tc_supported(sh, dtype, causal, q, k, v, out);
     if (path == 2 && !tc_ok)
         return fail(LA_ERR_UNSUPPORTED,
-                    "la_forward_ex: tensor-core path needs bf16, d in {64,128} and 16-byte aligned tensors");
+                    gates ? "la_forward_gated: the tensor-core kernels take no per-token gates"
+                          : "la_forward_ex: tensor-core path needs bf16, d in {64,128} and 16-byte aligned tensors");
     if (tc_ok && path != 1) {
         cudaError_t ce;
         int *status = device_status_word(&ce);
@@ -212,7 +218,7 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
         return LA_OK;
     }
     cudaError_t e = launch_simt_forward(q, k, v, out, sh, causal, dk, dtype,
-                                        S_out, z_out, s);
+                                        S_out, z_out, gates, s);
     if (e != cudaSuccess) return cuda_fail(e, "la_forward (CUDA-core kernel)");
     note_launches(1);
     return LA_OK;
@@ -227,14 +233,12 @@ size_t la::forward_workspace_bytes(int B, int H, int N, int d, int causal,
     return tc_workspace_bytes(sh, causal, decay, 0, sms);
 }
 
-extern "C" {
-
-__attribute__((visibility("default")))
-la_status la_decode_step_variant(float *S, float *z, const void *q,
-                                 const void *k, const void *v, void *out, int B,
-                                 int H, int d, const float *decay,
-                                 la_dtype dtype, const la_variant *variant,
-                                 la_stream_t stream) {
+la_status la::decode_common(float *S, float *z, const void *q, const void *k,
+                           const void *v, void *out, int B, int H, int d,
+                           const float *decay, const float *gates, la_dtype dtype,
+                           const la_variant *variant, la_stream_t stream) {
+    if (gates && decay)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step_gated: give gates or a decay, not both");
     if (variant && ((variant->feature_map != LA_PHI_ELU1 &&
                      variant->feature_map != LA_PHI_IDENTITY) ||
                     (variant->normalise != 0 && variant->normalise != 1)))
@@ -270,10 +274,44 @@ la_status la_decode_step_variant(float *S, float *z, const void *q,
     if (BH > 2147483647LL)
         return fail(LA_ERR_UNSUPPORTED, "la_decode_step: too many heads");
     cudaError_t e = launch_decode_step(S, z, q, k, v, out, BH, d, dk, phi, norm,
-                                       dtype, reinterpret_cast<cudaStream_t>(stream));
+                                       gates, dtype, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
     note_launches(1);
     return LA_OK;
+}
+
+extern "C" {
+
+__attribute__((visibility("default")))
+la_status la_decode_step_variant(float *S, float *z, const void *q,
+                                 const void *k, const void *v, void *out, int B,
+                                 int H, int d, const float *decay,
+                                 la_dtype dtype, const la_variant *variant,
+                                 la_stream_t stream) {
+    return la::decode_common(S, z, q, k, v, out, B, H, d, decay, nullptr, dtype,
+                             variant, stream);
+}
+
+__attribute__((visibility("default")))
+la_status la_decode_step_gated(float *S, float *z, const void *q, const void *k,
+                               const void *v, void *out, const float *gates,
+                               int B, int H, int d, la_dtype dtype,
+                               const la_variant *variant, la_stream_t stream) {
+    if (!gates) return fail(LA_ERR_INVALID_ARG, "la_decode_step_gated: null gates");
+    return la::decode_common(S, z, q, k, v, out, B, H, d, nullptr, gates, dtype,
+                             variant, stream);
+}
+
+__attribute__((visibility("default")))
+la_status la_forward_gated(const void *q, const void *k, const void *v,
+                           void *out, const float *gates, int B, int H, int N,
+                           int d, la_dtype dtype, const la_variant *variant,
+                           la_stream_t stream) {
+    if (!gates && (long long)B * H * N > 0)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_gated: null gates");
+    return la::forward_with_workspace(q, k, v, out, B, H, N, d, 1, nullptr, dtype,
+                                      0, 0, nullptr, 0, nullptr, nullptr, variant,
+                                      gates, stream);
 }
 
 __attribute__((visibility("default")))

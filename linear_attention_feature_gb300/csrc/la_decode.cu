@@ -4,7 +4,8 @@
 // forget-gate passage, 1 without decay).  g = 1 multiplies by one exactly, so
 // the undecayed step is unchanged.  The retention variant ("Story of
 // Attention - Part 5", section 4, recurrent form) uses the identity for phi
-// and no denominator.
+// and no denominator.  A device array of per-head gates (one per call: the
+// data-dependent scalar gate alpha_t of this token) replaces the decay.
 //
 // The step is a pure stream over the fp32 d x d state (read once, written
 // once): 2 * 4 * d^2 bytes per head against ~4 d^2 flops, so it is bound by
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kThreads)
 decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
                   const T *__restrict__ q, const T *__restrict__ k,
                   const T *__restrict__ v, T *__restrict__ out, DecayArgs dk,
-                  int use_phi, int norm) {
+                  int use_phi, int norm, const float *__restrict__ gates) {
     constexpr int NCG = D / 4;                 // column groups (float4 each)
     constexpr int NRG = kThreads / NCG;        // row groups
     constexpr int RPT = D / NRG;               // rows per thread
@@ -89,7 +90,7 @@ decode_vec_kernel(float *__restrict__ S, float *__restrict__ z,
     const int tid = threadIdx.x;
     const int cg = tid % NCG, rg = tid / NCG;
     float4 *__restrict__ Sh = reinterpret_cast<float4 *>(S + (size_t)bh * D * D);
-    const float g = decay_of(dk, (int)bh);
+    const float g = gates ? gates[bh] : decay_of(dk, (int)bh);
     decode_prologue<T>(z + (size_t)bh * D, q + (size_t)bh * D,
                        k + (size_t)bh * D, D, g, use_phi != 0, sk, sq, swarp, &sden);
     const T *vh = v + (size_t)bh * D + 4 * cg;
@@ -144,12 +145,13 @@ __global__ void __launch_bounds__(kThreads)
 decode_generic_kernel(float *__restrict__ S, float *__restrict__ z,
                       const T *__restrict__ q, const T *__restrict__ k,
                       const T *__restrict__ v, T *__restrict__ out, int d,
-                      DecayArgs dk, int use_phi, int norm) {
+                      DecayArgs dk, int use_phi, int norm,
+                      const float *__restrict__ gates) {
     __shared__ float sk[LA_MAX_D], sq[LA_MAX_D];
     __shared__ float swarp[kThreads / 32], sden;
     const long long bh = blockIdx.x;
     float *Sh = S + (size_t)bh * d * d;
-    const float g = decay_of(dk, (int)bh);
+    const float g = gates ? gates[bh] : decay_of(dk, (int)bh);
     decode_prologue<T>(z + (size_t)bh * d, q + (size_t)bh * d,
                        k + (size_t)bh * d, d, g, use_phi != 0, sk, sq, swarp, &sden);
     __syncthreads();
@@ -168,20 +170,21 @@ decode_generic_kernel(float *__restrict__ S, float *__restrict__ z,
 template <typename T>
 cudaError_t launch_t(float *S, float *z, const void *q, const void *k,
                      const void *v, void *out, long long BH, int d,
-                     const DecayArgs &dk, int phi, int norm, cudaStream_t stream) {
+                     const DecayArgs &dk, int phi, int norm, const float *gates,
+                     cudaStream_t stream) {
     const T *qq = static_cast<const T *>(q), *kk = static_cast<const T *>(k),
             *vv = static_cast<const T *>(v);
     T *oo = static_cast<T *>(out);
     const bool aligned = (reinterpret_cast<uintptr_t>(S) & 15u) == 0;
     dim3 grid((unsigned)BH);
     if (aligned && d == 128)
-        decode_vec_kernel<T, 128><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm);
+        decode_vec_kernel<T, 128><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm, gates);
     else if (aligned && d == 64)
-        decode_vec_kernel<T, 64><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm);
+        decode_vec_kernel<T, 64><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm, gates);
     else if (aligned && d == 256)
-        decode_vec_kernel<T, 256><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm);
+        decode_vec_kernel<T, 256><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, dk, phi, norm, gates);
     else
-        decode_generic_kernel<T><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, d, dk, phi, norm);
+        decode_generic_kernel<T><<<grid, kThreads, 0, stream>>>(S, z, qq, kk, vv, oo, d, dk, phi, norm, gates);
     return cudaGetLastError();
 }
 
@@ -190,11 +193,11 @@ cudaError_t launch_t(float *S, float *z, const void *q, const void *k,
 cudaError_t launch_decode_step(float *S, float *z, const void *q,
                                const void *k, const void *v, void *out,
                                long long BH, int d, const DecayArgs &dk,
-                               int phi, int norm, la_dtype dtype,
-                               cudaStream_t stream) {
+                               int phi, int norm, const float *gates,
+                               la_dtype dtype, cudaStream_t stream) {
     if (dtype == LA_F32)
-        return launch_t<float>(S, z, q, k, v, out, BH, d, dk, phi, norm, stream);
-    return launch_t<__nv_bfloat16>(S, z, q, k, v, out, BH, d, dk, phi, norm, stream);
+        return launch_t<float>(S, z, q, k, v, out, BH, d, dk, phi, norm, gates, stream);
+    return launch_t<__nv_bfloat16>(S, z, q, k, v, out, BH, d, dk, phi, norm, gates, stream);
 }
 
 }  // namespace la

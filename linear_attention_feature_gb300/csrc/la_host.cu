@@ -234,7 +234,7 @@ la_status la_forward_host(const void *q, const void *k, const void *v,
             dq + off, dk + off, dv + off, dout + off, g.nb, g.nh, N, d, causal,
             decay ? decay + g.h0 : nullptr, dtype, 0, 0,
             scratch_bytes ? scratch : nullptr, scratch_bytes, nullptr, nullptr,
-            nullptr, stream);
+            nullptr, nullptr, stream);
         if (st != LA_OK) {
             join_copies(en, s);
             return st;

@@ -32,19 +32,22 @@ struct FwdShape {
 
 // ---- CUDA-core (fp32 FMA) forward: any d in 1..LA_MAX_D, fp32 or bf16 ----
 // S_out / z_out (causal only, may be NULL): the final state [BH][d][d] /
-// [BH][d] in fp32.
+// [BH][d] in fp32.  gates (causal only, may be NULL): a device [BH][N]
+// scalar gate per token, used instead of the per-head decay.
 cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
                                 void *out, const FwdShape &sh, int causal,
                                 const DecayArgs &decay, la_dtype dtype,
-                                float *S_out, float *z_out, cudaStream_t stream);
+                                float *S_out, float *z_out, const float *gates,
+                                cudaStream_t stream);
 
 // ---- recurrent decode step ----
-// phi / norm as in FwdShape.
+// phi / norm as in FwdShape; gates (may be NULL): a device [BH] gate per
+// head for this step, used instead of the per-head decay.
 cudaError_t launch_decode_step(float *S, float *z, const void *q,
                                const void *k, const void *v, void *out,
                                long long BH, int d, const DecayArgs &decay,
-                               int phi, int norm, la_dtype dtype,
-                               cudaStream_t stream);
+                               int phi, int norm, const float *gates,
+                               la_dtype dtype, cudaStream_t stream);
 
 // Address of the current device's two status words (kernels set word 0 to a
 // non-zero la_status when a bounded wait gives up, and word 1 to where).
@@ -61,12 +64,22 @@ void set_last_error(const char *msg);
 // kernels (ws = NULL: they allocate it stream-ordered themselves).
 // S_out / z_out (causal only, may be NULL): also write the final state.
 // `variant` NULL: elu(x) + 1 with the normaliser.
+// gates (causal only, may be NULL): a device [B][H][N] scalar gate per
+// token, instead of `decay` (CUDA-core kernels).
 la_status forward_with_workspace(const void *q, const void *k, const void *v,
                                  void *out, int B, int H, int N, int d,
                                  int causal, const float *decay, la_dtype dtype,
                                  int path, int segment_chunks, void *ws,
                                  size_t ws_bytes, float *S_out, float *z_out,
-                                 const la_variant *variant, la_stream_t stream);
+                                 const la_variant *variant, const float *gates,
+                                 la_stream_t stream);
+
+// The decode step behind la_decode_step(_ex/_variant/_gated): decay (host
+// [H]) or gates (device [BH]), not both.
+la_status decode_common(float *S, float *z, const void *q, const void *k,
+                        const void *v, void *out, int B, int H, int d,
+                        const float *decay, const float *gates, la_dtype dtype,
+                        const la_variant *variant, la_stream_t stream);
 
 // Scratch bytes forward_with_workspace needs (automatic path and segment
 // length; 0 where the CUDA-core kernels run, which need none).

@@ -11,6 +11,10 @@
 //   num_i = sum_j A_ij v_j + g^(i+1) phi(q_i)^T S            (S: state before
 //   den_i = sum_j A_ij     + g^(i+1) phi(q_i)^T z             the chunk)
 //   S    <- g^n S + sum_t g^(n-1-t) phi(k_t) v_t^T,  z likewise
+// With a data-dependent gate alpha_t per token (S_t = alpha_t S_{t-1} + ...)
+// every power of g becomes the product of the gates it spans: g^(i-j) ->
+// prod_{t=j+1..i} alpha_t, g^(i+1) -> prod_{t<=i} alpha_t, g^n -> the
+// product over the chunk (a per-chunk table, so a zero gate is exact).
 // The non-causal form first reduces S = phi(K)^T V and z = phi(K)^T 1 over
 // the whole sequence, then reads them with every query.
 #include <cuda_bf16.h>
@@ -43,7 +47,8 @@ __global__ void __launch_bounds__(kThreads)
 simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, T *__restrict__ out, int N,
                     int d, DecayArgs decay, float *__restrict__ S_out,
-                    float *__restrict__ z_out, int use_phi, int norm) {
+                    float *__restrict__ z_out, int use_phi, int norm,
+                    const float *__restrict__ gates) {
     extern __shared__ float smem[];
     const int cb = blockIdx.x;
     const long long bh = blockIdx.y;
@@ -57,6 +62,8 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
     float *A = pv + kT * kCB;         // [kT][kT]
     float *den = A + kT * kT;         // [kT]
     float *gp = den + kT;             // [kT + 1]: g^0 .. g^kT
+    float *gt = gp + kT + 1;          // [kT][kT]: prod_{t=j+1..i} alpha_t (gates)
+    float *gc = gt + kT * kT;         // [kT]: prod_{t<=i} alpha_t (gates)
 
     const int tid = threadIdx.x;
     const size_t base = (size_t)bh * (size_t)N * (size_t)d;
@@ -125,6 +132,27 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
             int t = i / kCB, c = i % kCB;
             pv[i] = c < cw ? ld_in(v + base + (size_t)(t0 + t) * d + c0 + c) : 0.f;
         }
+        if (gates) {
+            // gate products of this chunk: thread j fills column j of the
+            // table in order (gt[i][j] = gt[i-1][j] alpha_i), thread 0 the
+            // prefix products
+            const float *ga = gates + (size_t)bh * N + t0;
+            if (tid < n) {
+                float p = 1.f;
+                gt[tid * kT + tid] = 1.f;
+                for (int i = tid + 1; i < n; ++i) {
+                    p *= ga[i];
+                    gt[i * kT + tid] = p;
+                }
+            }
+            if (tid == kThreads - 1) {
+                float p = 1.f;
+                for (int i = 0; i < n; ++i) {
+                    p *= ga[i];
+                    gc[i] = p;
+                }
+            }
+        }
         __syncthreads();
         // intra-chunk masked, decayed scores
         for (int e = tid; e < kT * kT; e += kThreads) {
@@ -132,7 +160,7 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
             float a = 0.f;
             if (i < n && j <= i) {
                 for (int f = 0; f < d; ++f) a = fmaf(pq[i * d + f], pk[j * d + f], a);
-                a *= gp[i - j];
+                a *= gates ? gt[i * kT + j] : gp[i - j];
             }
             A[e] = a;
         }
@@ -142,7 +170,7 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
             float s = 0.f, r = 0.f;
             for (int j = 0; j <= i; ++j) s += A[i * kT + j];
             for (int a = 0; a < d; ++a) r = fmaf(pq[i * d + a], z[a], r);
-            den[i] = s + gp[i + 1] * r;
+            den[i] = s + (gates ? gc[i] : gp[i + 1]) * r;
         }
         __syncthreads();
         // numerators and outputs
@@ -152,21 +180,25 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
             float s = 0.f, r = 0.f;
             for (int j = 0; j <= i; ++j) s = fmaf(A[i * kT + j], pv[j * kCB + c], s);
             for (int a = 0; a < d; ++a) r = fmaf(pq[i * d + a], S[a * kCB + c], r);
-            const float num = s + gp[i + 1] * r;
+            const float num = s + (gates ? gc[i] : gp[i + 1]) * r;
             st_out(out + base + (size_t)(t0 + i) * d + c0 + c, norm ? num / den[i] : num);
         }
         __syncthreads();
         // state update
+        const float gall = gates ? gc[n - 1] : gp[n];
         for (int e = tid; e < d * kCB; e += kThreads) {
             int a = e / kCB, c = e % kCB;
-            float s = gp[n] * S[e];
-            for (int t = 0; t < n; ++t)
-                s = fmaf(gp[n - 1 - t] * pk[t * d + a], pv[t * kCB + c], s);
+            float s = gall * S[e];
+            for (int t = 0; t < n; ++t) {
+                const float w = gates ? gt[(n - 1) * kT + t] : gp[n - 1 - t];
+                s = fmaf(w * pk[t * d + a], pv[t * kCB + c], s);
+            }
             S[e] = s;
         }
         for (int a = tid; a < d; a += kThreads) {
-            float s = gp[n] * z[a];
-            for (int t = 0; t < n; ++t) s = fmaf(gp[n - 1 - t], pk[t * d + a], s);
+            float s = gall * z[a];
+            for (int t = 0; t < n; ++t)
+                s = fmaf(gates ? gt[(n - 1) * kT + t] : gp[n - 1 - t], pk[t * d + a], s);
             z[a] = s;
         }
         __syncthreads();
@@ -186,10 +218,11 @@ simt_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
 template <typename T, bool kCausal>
 cudaError_t launch_t(const void *q, const void *k, const void *v, void *out,
                      const FwdShape &sh, const DecayArgs &decay, float *S_out,
-                     float *z_out, cudaStream_t stream) {
+                     float *z_out, const float *gates, cudaStream_t stream) {
     const int d = sh.d;
     size_t smem_floats = (size_t)d * kCB + d + 2 * (size_t)kT * d +
-                         (size_t)kT * kCB + kT * kT + kT + (kT + 1);
+                         (size_t)kT * kCB + kT * kT + kT + (kT + 1) +
+                         (size_t)kT * kT + kT;
     size_t smem = smem_floats * sizeof(float);
     auto kern = simt_forward_kernel<T, kCausal>;
     cudaError_t e = cudaFuncSetAttribute(
@@ -199,7 +232,7 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, void *out,
     kern<<<grid, kThreads, smem, stream>>>(
         static_cast<const T *>(q), static_cast<const T *>(k),
         static_cast<const T *>(v), static_cast<T *>(out), sh.N, d, decay, S_out,
-        z_out, sh.phi, sh.norm);
+        z_out, sh.phi, sh.norm, gates);
     return cudaGetLastError();
 }
 
@@ -208,13 +241,14 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, void *out,
 cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
                                 void *out, const FwdShape &sh, int causal,
                                 const DecayArgs &decay, la_dtype dtype,
-                                float *S_out, float *z_out, cudaStream_t stream) {
+                                float *S_out, float *z_out, const float *gates,
+                                cudaStream_t stream) {
     if (dtype == LA_F32)
-        return causal ? launch_t<float, true>(q, k, v, out, sh, decay, S_out, z_out, stream)
-                      : launch_t<float, false>(q, k, v, out, sh, decay, nullptr, nullptr, stream);
+        return causal ? launch_t<float, true>(q, k, v, out, sh, decay, S_out, z_out, gates, stream)
+                      : launch_t<float, false>(q, k, v, out, sh, decay, nullptr, nullptr, nullptr, stream);
     return causal
-               ? launch_t<__nv_bfloat16, true>(q, k, v, out, sh, decay, S_out, z_out, stream)
-               : launch_t<__nv_bfloat16, false>(q, k, v, out, sh, decay, nullptr, nullptr, stream);
+               ? launch_t<__nv_bfloat16, true>(q, k, v, out, sh, decay, S_out, z_out, gates, stream)
+               : launch_t<__nv_bfloat16, false>(q, k, v, out, sh, decay, nullptr, nullptr, nullptr, stream);
 }
 
 }  // namespace la

@@ -231,3 +231,17 @@ def test_variant_null_and_valid_variants_pass_validation(lib):
                                       None) == OK
         assert lib.la_decode_step_variant(P, P, P, P, P, OUT, 0, 2, 64, None, 1, var,
                                           None) == OK
+
+
+def test_gated_entry_points_reject_bad_arguments(lib):
+    G = ctypes.c_void_p(0x500000)
+    f = lib.la_forward_gated
+    assert f(P, P2, P3, OUT, None, 1, 2, 8, 64, 1, None, None) == INVALID
+    assert "null gates" in lib.la_last_error().decode()
+    assert f(P, P2, P3, OUT, G, 1, 2, 8, 300, 1, None, None) == INVALID
+    assert f(P, P2, P3, OUT, G, 1, 2, 8, 64, 1, ctypes.byref(la._Variant(5, 1)), None) == INVALID
+    assert f(P, P2, P3, OUT, G, 0, 2, 8, 64, 1, None, None) == OK  # empty
+    d = lib.la_decode_step_gated
+    assert d(P, P, P, P, P, OUT, None, 1, 2, 64, 1, None, None) == INVALID
+    assert d(P, P, P, P, P, OUT, G, 1, 2, 0, 1, None, None) == INVALID
+    assert d(P, P, P, P, P, OUT, G, 0, 2, 64, 1, None, None) == OK

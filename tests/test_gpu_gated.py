@@ -1,0 +1,81 @@
+"""Data-dependent scalar gate per token and head (la_forward_gated,
+la_decode_step_gated): S_t = alpha_t S_{t-1} + phi(k_t) v_t^T with the
+normaliser gated alike, compared with the double-precision oracle on seeded
+inputs and gates (including exact zeros and ones)."""
+import numpy as np
+import pytest
+
+import oracle
+import linear_attention_feature_gb300 as la
+from linear_attention_feature_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    la.build.build()
+    la.load_library()
+
+
+def make_gates(B, H, N, seed, lo=0.8):
+    g = torch.Generator().manual_seed(seed)
+    a = lo + (1.0 - lo) * torch.rand(B, H, N, generator=g)
+    a[:, :, ::97] = 1.0          # exact ones
+    a[0, 0, min(40, N // 2)] = 0.0  # a reset
+    return a
+
+
+@pytest.mark.parametrize("dtype, d", [("f32", 64), ("bf16", 64), ("bf16", 128), ("f32", 37)])
+@pytest.mark.parametrize("N", [31, 333, 1000])
+def test_gated_forward_matches_oracle(dtype, d, N):
+    q, k, v = wl.make_qkv(2, 2, N, d, dtype, seed=110 + N)
+    a = make_gates(2, 2, N, 111 + N)
+    y = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda())
+    la.check_device_status()
+    ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy(), nthreads=8)
+    tol = wl.TOL["f32"] if dtype == "f32" else wl.TOL["bf16"]
+    assert wl.max_row_rel_err(y.cpu(), ref) <= tol
+
+
+def test_gated_forward_constant_gates_equal_decay():
+    q, k, v = (t.cuda() for t in wl.make_qkv(1, 3, 500, 64, "f32", seed=120))
+    dec = [0.9, 0.5, 1.0]
+    a = torch.tensor(dec).view(1, 3, 1).expand(1, 3, 500).contiguous().cuda()
+    y = la.forward_gated(q, k, v, a)
+    r = la.forward(q, k, v, causal=True, decay=dec)
+    torch.cuda.synchronize()
+    assert wl.max_row_rel_err(y.cpu(), r.cpu()) <= 1e-5
+
+
+def test_gated_retention_variant():
+    q, k, v = wl.make_qkv(1, 2, 400, 64, "f32", seed=121)
+    a = make_gates(1, 2, 400, 122)
+    y = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(),
+                         feature_map="identity", normalise=False)
+    ref = oracle.causal_gated(q, k, v, a.double().numpy(), fmap=oracle.FMAP_IDENTITY,
+                              normalise=False)
+    assert wl.max_row_rel_err(y.cpu(), ref) <= wl.TOL["f32"]
+
+
+@pytest.mark.parametrize("dtype, d", [("bf16", 128), ("f32", 64)])
+def test_gated_decode_continues_the_gated_forward(dtype, d):
+    # decode steps with per-token gates equal the gated forward's last rows
+    B, H, N = 2, 3, 24
+    q, k, v = wl.make_qkv(B, H, N, d, dtype, seed=130 + d)
+    a = make_gates(B, H, N, 131 + d, lo=0.6)
+    S = torch.zeros(B, H, d, d, device="cuda")
+    z = torch.zeros(B, H, d, device="cuda")
+    ys = []
+    for t in range(N):
+        ys.append(la.decode_step_gated(S, z, q[:, :, t].contiguous().cuda(),
+                                       k[:, :, t].contiguous().cuda(),
+                                       v[:, :, t].contiguous().cuda(),
+                                       a[:, :, t].contiguous().cuda()).cpu())
+    la.check_device_status()
+    ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy())
+    tol = wl.TOL["f32"] if dtype == "f32" else wl.TOL["bf16"]
+    assert wl.max_row_rel_err(torch.stack(ys, dim=2), ref) <= tol
