@@ -360,7 +360,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
     Kx, Wx = max(3, args.steps // 2), max(3, args.warmup)
 
     def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2, kernel=None,
-                 state=False, retention=False):
+                 state=False, retention=False, gated=False):
         w = wl.WORKLOADS[wkey]
         try:
             if inputs is None:
@@ -375,6 +375,12 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
                 fn = lambda: la.forward_variant(qq, kk, vv, causal=causal, decay=decay,  # noqa
                                                 out=oo, feature_map="identity",
                                                 normalise=False)
+            if gated:
+                # a data-dependent gate per token, uniform in [0.9, 1)
+                gen = torch.Generator(device="cpu").manual_seed(200 + rank)
+                ga = (0.9 + 0.1 * torch.rand(w.B, w.H, w.N, generator=gen)).to(dev)
+                fn = lambda: la.forward_gated(qq, kk, vv, ga, out=oo)  # noqa
+                extra = 4 * w.B * w.H * w.N  # the gates
             if state:
                 # forward plus the final state (the prefill of a decode)
                 Ss = torch.empty(w.B, w.H, w.d, w.d, device=dev)
@@ -412,6 +418,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
              state=True)
     fwd_path("bf16_decay_b4h8_n16384_d128 retention", wd.name, True,
              decay=list(wd.decay), retention=True)
+    fwd_path(f"{MAIN} gated (CUDA cores)", MAIN, True, inputs=(q, k, v), gated=True)
     try:
         res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,
                                                 args)
