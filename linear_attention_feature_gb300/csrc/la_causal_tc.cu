@@ -72,8 +72,12 @@ constexpr int BAR_T = 1, BAR_E1 = 2, BAR_E2 = 3;
 constexpr uint32_t TM_P = 0, TM_O = 256, TM_OQS = 336, TM_S = 416;
 constexpr uint32_t TM_COLS = 512;
 constexpr int NX = DV + 16;  // extended N of the wide products
-template <bool kDecay>
-struct OBufs { static constexpr int n = kDecay ? 1 : 2; };
+// Kernel mode: 0 no decay, 1 per-head decay g, 2 data-dependent gate per
+// token.  Modes 1 and 2 share the structure of the weighted kernel (a
+// separate inter-chunk accumulator, weighted K rows); they differ only in how
+// the weights are formed (powers of g, or products of gates).
+template <bool kWeighted>
+struct OBufs { static constexpr int n = kWeighted ? 1 : 2; };
 
 struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
@@ -86,7 +90,7 @@ struct Params {
     long long timeout;  // clock cycles per bounded wait
 };
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 struct Layout {
     static constexpr int KB = DK / 64;
     static constexpr int STAGES = DK == 128 ? 2 : 4;
@@ -163,11 +167,11 @@ __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
 
 // ---------------------------------------------------------------- producer
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
                          const Ctx &cx, const CUtensorMap *tq,
                          const CUtensorMap *tk, const CUtensorMap *tv) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
     int j = 0, tl = 0;
     for (;;) {
@@ -208,10 +212,10 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
 // P = phi(Q) phi(K)^T of job `jj` (stage jj % STAGES) into P buffer b of
 // B-chunk number `nbq`, once the chunk is transformed and the buffer's
 // previous P~V has completed.
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ __forceinline__ void issue_p(uint8_t *smem, Small &sm, const Ctx &cx,
                                         uint32_t tmem, int jj, int nbq) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     constexpr uint32_t idP = idesc_bf16(128, 128, 0, 0);
     const int st = jj % L::STAGES, b = nbq & 1;
     wait_bar(&sm.xf[st], (jj / L::STAGES) & 1, cx);
@@ -230,34 +234,34 @@ __device__ __forceinline__ void issue_p(uint8_t *smem, Small &sm, const Ctx &cx,
 // Issues P of B chunk qi+1 now if its feature maps and P buffer are ready;
 // otherwise it is issued (blocking) at the top of the next chunk, so the
 // state-dependent products of chunk qi never wait on the transform.
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ __forceinline__ void try_issue_next_p(uint8_t *smem, Small &sm,
                                                  const Ctx &cx, uint32_t tmem,
                                                  int jj, int nbq, int qi,
                                                  int nB, int &p_next) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     if (p_next != qi + 1 || qi + 1 >= nB) return;
     const int st1 = (jj + 1) % L::STAGES, b1 = (nbq + 1) & 1;
     if (mbar_try_wait(&sm.xf[st1], ((jj + 1) / L::STAGES) & 1) &&
         mbar_try_wait(&sm.pv_done[b1], (((nbq + 1) >> 1) & 1) ^ 1)) {
-        issue_p<DK, kDecay>(smem, sm, cx, tmem, jj + 1, nbq + 1);
+        issue_p<DK, kMode>(smem, sm, cx, tmem, jj + 1, nbq + 1);
         ++p_next;
     }
 }
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                            const Ctx &cx, uint32_t tmem) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     constexpr uint32_t idPV = idesc_bf16(128, NX, 0, 1);  // Pt [V | 1]
     constexpr uint32_t idQS = idesc_bf16(128, NX, 0, 1);  // phi(Q) [S | z]
     constexpr uint32_t idSU = idesc_bf16(128, NX, 1, 1);  // phi(K)^T [V | 1]
     constexpr uint32_t lboA = DK == 128 ? 16384 : 0;      // d=64: rows 64..127 alias
-    constexpr int NOB = OBufs<kDecay>::n;
+    constexpr int NOB = OBufs<kMode != 0>::n;
     // chunk order: P~V first where the look-back and state epilogue are the
     // longer latency (d = 64); phi(Q) [S | z] first where the feature-map
     // ring is (d = 128, two stages) and with decay (one O buffer)
-    constexpr bool kPVFirst = !kDecay && DK == 64;
+    constexpr bool kPVFirst = !kMode && DK == 64;
     const uint32_t sb = smem_u32(smem + L::OFF_SB);
     const uint32_t onesx = smem_u32(smem + L::OFF_ONESX);
     int j = 0, nb = 0, nsb = 0, tl = 0;
@@ -296,7 +300,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             const int st = jj % L::STAGES, b = nbq & 1;
             const bool su = qi + 1 < nB || final_state;
             if (p_next == qi) {
-                issue_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq);
+                issue_p<DK, kMode>(smem, sm, cx, tmem, jj, nbq);
                 ++p_next;
             }
             const uint32_t qb = smem_u32(smem + st * L::STAGE + L::OFF_Q);
@@ -316,7 +320,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                            sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV,
                            ks > 0 ? 1u : 0u);
                 mma_commit(&sm.pv_done[b]);
-                try_issue_next_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
+                try_issue_next_p<DK, kMode>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
                 wait_bar(&sm.sb_ready, nsb & 1, cx);
                 ++nsb;
                 tc_fence_after();
@@ -339,14 +343,14 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 // inter-chunk read (with decay into its own accumulator: it
                 // is scaled per row by g^(i+1) in the output epilogue)
                 for (int ks = 0; ks < DK / 16; ++ks)
-                    mma_ss(tmem + (kDecay ? TM_OQS : tob),
+                    mma_ss(tmem + (kMode ? TM_OQS : tob),
                            sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
                            sdesc_sw128(sb + ks * 2048, L::SBLK, 1024), idQS,
                            ks > 0 ? 1u : 0u);
                 // state update phi(K)^T [V | 1]; with decay Khat^T [V | 1],
                 // Khat_t = g^(n-1-t) phi(k_t), the K rows being rescaled in
                 // place once P(j) has read them
-                if (kDecay) {
+                if (kMode) {
                     wait_bar(&sm.khat_ready, nbq & 1, cx);
                     tc_fence_after();
                 }
@@ -356,14 +360,14 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                                sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idSU, 1u);
                     mma_commit(&sm.s_full);
                 }
-                try_issue_next_p<DK, kDecay>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
+                try_issue_next_p<DK, kMode>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
                 wait_bar(&sm.pt_ready[b], (nbq >> 1) & 1, cx);
                 tc_fence_after();
                 // intra-chunk: P~ [V | 1] (P~ read from TMEM)
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_ts(tmem + tob, tmem + TM_P + 128u * b + ks * 8,
                            sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV,
-                           (kDecay && ks == 0) ? 0u : 1u);
+                           (kMode && ks == 0) ? 0u : 1u);
                 mma_commit(&sm.o_full[ob]);
                 mma_commit(&sm.pv_done[b]);
             }
@@ -446,10 +450,10 @@ __device__ __forceinline__ void scale_row(uint8_t *tile, int row, int part,
     }
 }
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                           const Ctx &cx, const DecayArgs &dk) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     const int et = threadIdx.x - kWarpT * 32;  // 0..255
     const int row = et & 127, part = et >> 7;
     int j = 0, nb = 0, tl = 0;
@@ -466,7 +470,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                 wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
                 uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
                 const int tok = c * C + row;
-                if (kDecay || tok >= p.N) {
+                if (kMode || tok >= p.N) {
                     const float w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
                     transform_row_scaled<DK>(kt, row, part, bf2_splat(w), p.phi);
                 } else {
@@ -488,7 +492,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
-            if (kDecay) {
+            if (kMode) {
                 // Khat_t = g^(n-1-t) phi(k_t) in place, once P(j) (the only
                 // reader of the unweighted rows) has completed; rows past N
                 // are already zero
@@ -507,7 +511,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
 
 // Causal mask and decay on P (fp32, TMEM), rounded to bf16 in place (the A
 // operand of P~V).  One thread per row i (= TMEM lane).
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
                                const DecayArgs &dk, uint32_t tmem) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -521,7 +525,7 @@ __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
-        if (kDecay) {
+        if (kMode) {
             if (et < 32) sm.gtab[et] = gpow(lg, et);
             named_bar_sync(BAR_E1, 128);
         }
@@ -542,7 +546,7 @@ __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
                     tmem_wait_ld();
                     reg_fence(v);
                     if (blk < q) {
-                        if (kDecay) {
+                        if (kMode) {
                             // g^(row - j) = g^(row - 32 blk - 31) g^(31 - e)
                             const float base = gpow(lg, row - 32 * blk - 31);
 #pragma unroll
@@ -562,9 +566,9 @@ __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
                             // the head's table, only where e <= lane
                             float x0 = 0.f, x1 = 0.f;
                             if (e <= lane)
-                                x0 = kDecay ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
+                                x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
                             if (e + 1 <= lane)
-                                x1 = kDecay ? u2f(v[e + 1]) * sm.gtab[lane - e - 1]
+                                x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1]
                                             : u2f(v[e + 1]);
                             pk[e >> 1] = pack_bf16x2(x0, x1);
                         }
@@ -583,33 +587,33 @@ __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
 // bf16 into the stage's (dead) Q slot, TMA store.  With several stages the
 // stage is released when the next store is issued (the store has read it by
 // then), so the store never stalls this warpgroup.
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
                                              const Ctx &cx, uint32_t lb,
                                              int row, int et, float wq,
                                              const Item &it, int c, int j,
                                              int nb, int &pend, bool norm,
                                              const CUtensorMap *to) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     constexpr bool kDefer = !L::OWN_OST && L::STAGES >= 3;
     const int st = j % L::STAGES;
-    const int ob = OBufs<kDecay>::n == 2 ? (nb & 1) : 0;
+    const int ob = OBufs<kMode != 0>::n == 2 ? (nb & 1) : 0;
     const uint32_t tob = TM_O + 80u * ob;
     uint8_t *stage_o = L::OWN_OST ? smem + L::OFF_OST : smem + st * L::STAGE + L::OFF_Q;
     if (L::OWN_OST) {  // the previous chunk's store must have read the buffer
         if (et == 0) tma_store_wait_read<0>();
         named_bar_sync(BAR_E2, 128);
     }
-    wait_bar(&sm.o_full[ob], (OBufs<kDecay>::n == 2 ? (nb >> 1) : nb) & 1, cx);
+    wait_bar(&sm.o_full[ob], (OBufs<kMode != 0>::n == 2 ? (nb >> 1) : nb) & 1, cx);
     tc_fence_after();
     uint32_t dreg = tmem_ld1(lb + tob + DV);
-    uint32_t direg = kDecay ? tmem_ld1(lb + TM_OQS + DV) : 0u;
+    uint32_t direg = kMode ? tmem_ld1(lb + TM_OQS + DV) : 0u;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t o[32];
         tmem_ld32(lb + tob + 32 * h, o);
         float inv;
-        if (kDecay) {
+        if (kMode) {
             uint32_t oi[32];
             tmem_ld32(lb + TM_OQS + 32 * h, oi);
             tmem_wait_ld();
@@ -759,12 +763,12 @@ __device__ __forceinline__ void resolve_lookback(Small &sm, const Params &p,
 
 // Look-back, step 2 (every thread): its 32 columns (half h) of row a of
 // sum_m g^(L m) state(seg-1-m) over the decided predecessors, and z[a].
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
                                              const Item &it, int nlb, int a,
                                              int h, bool zh, float gL,
                                              float (&acc)[32], float &accz) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
 #pragma unroll
     for (int e = 0; e < 32; ++e) acc[e] = 0.f;
     accz = 0.f;
@@ -808,11 +812,11 @@ __device__ __forceinline__ void store_zrow(uint8_t *sb_z, int a, float z) {
     store_zb(sb_z, a, z);
 }
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                              const Ctx &cx, const DecayArgs &dk, uint32_t tmem,
                              const CUtensorMap *to) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     using SM = SMap<DK>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;
@@ -832,7 +836,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         const float gL = gpow(lg, p.seg_chunks * C);
-        const float wq = kDecay ? gpow(lg, row + 1) : 1.f;
+        const float wq = kMode ? gpow(lg, row + 1) : 1.f;
         float *agg = p.agg + (size_t)t * L::STATE;
         float *incl = p.incl + (size_t)t * L::STATE;
         const int n0 = min(C, p.N - it.c0 * C);
@@ -850,7 +854,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
 #pragma unroll 1
                 for (int hh = 0; hh < SM::NH; ++hh) {
                     float acc[32], accz;
-                    lookback_sum<DK, kDecay>(sm, p, it, nlb, a, h0 + hh,
+                    lookback_sum<DK, kMode>(sm, p, it, nlb, a, h0 + hh,
                                              hasz && hh == 0, gL, acc, accz);
                     if (hh == 0) accz_e = accz;
                     float4 *slot = lb_slot<DK>(sb, a, h0, hh);
@@ -943,7 +947,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 const int h = h0 + hh;
                 const bool zh = hasz && hh == 0;
                 float acc[32], accz;
-                lookback_sum<DK, kDecay>(sm, p, it, nlb, a, h, zh, gL, acc, accz);
+                lookback_sum<DK, kMode>(sm, p, it, nlb, a, h, zh, gL, acc, accz);
                 if (it.hasA) {
                     // inclusive prefix = g^L S_start + local state (published
                     // below, once phase B has its start state)
@@ -1008,7 +1012,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[e] = u2f(v[e]);
                     store_sb_half(sb, a, h, x);
-                    if (kDecay) {
+                    if (kMode) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f * x[e]);
                         tmem_st32(lb + TM_S + 32 * h, v);
@@ -1020,15 +1024,15 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                     reg_fence(zr);
                     const float z = u2f(zr);
                     store_zb(sbz, a, z);
-                    if (kDecay) tmem_put_z(lb + TM_S + DV, f * z);
+                    if (kMode) tmem_put_z(lb + TM_S + DV, f * z);
                 }
-                if (kDecay) tmem_wait_st();
+                if (kMode) tmem_wait_st();
                 fence_async_shared();
                 tc_fence_before();
                 named_bar_sync(BAR_E2, 128);
                 if (et == 0) mbar_arrive(&sm.sb_ready);
             }
-            output_chunk<DK, kDecay>(smem, sm, cx, lb, row, et, wq, it, c, j, nb,
+            output_chunk<DK, kMode>(smem, sm, cx, lb, row, et, wq, it, c, j, nb,
                                      pend, p.norm != 0, to);
         }
         if (et == 0 && pend >= 0) {  // the item's last store: release its stage
@@ -1072,14 +1076,14 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
 
 // ---------------------------------------------------------------- kernel
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_kernel(const __grid_constant__ CUtensorMap tq,
               const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv,
               const __grid_constant__ CUtensorMap to, const Params p,
               const DecayArgs dk) {
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1136,15 +1140,15 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) producer<DK, kDecay>(smem, sm, p, cx, &tq, &tk, &tv);
+        if (lane == 0) producer<DK, kMode>(smem, sm, p, cx, &tq, &tk, &tv);
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer<DK, kDecay>(smem, sm, p, cx, tmem);
+        if (lane == 0) mma_issuer<DK, kMode>(smem, sm, p, cx, tmem);
     } else if (warp < kWarpE1) {
-        transform<DK, kDecay>(smem, sm, p, cx, dk);
+        transform<DK, kMode>(smem, sm, p, cx, dk);
     } else if (warp < kWarpE2) {
-        score_epilogue<DK, kDecay>(sm, p, cx, dk, tmem);
+        score_epilogue<DK, kMode>(sm, p, cx, dk, tmem);
     } else {
-        output_state<DK, kDecay>(smem, sm, p, cx, dk, tmem, &to);
+        output_state<DK, kMode>(smem, sm, p, cx, dk, tmem, &to);
     }
 
     tc_fence_before();
@@ -1158,17 +1162,17 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
 // time grows once a wave's phase-A loads of K and V no longer stay in L2
 // until phase B re-reads them, so segments stay short: about three items
 // per SM, 2..8 chunks.
-template <bool kDecay>
+template <bool kWeighted>
 int auto_segment_chunks(long long heads, int nchunks, int sms) {
-    if (!kDecay) return tchost::wave_segment_chunks(heads, nchunks, sms, 3);
+    if (!kWeighted) return tchost::wave_segment_chunks(heads, nchunks, sms, 3);
     const long long units = heads * nchunks;
     const long long want = (units + 3LL * sms - 1) / (3LL * sms);
     return (int)(want < 2 ? 2 : (want > 8 ? 8 : want));
 }
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 constexpr size_t smem_bytes() {
-    return (size_t)Layout<DK, kDecay>::OFF_SMALL + sizeof(Small) + 1024;
+    return (size_t)Layout<DK, kMode>::OFF_SMALL + sizeof(Small) + 1024;
 }
 
 static_assert(smem_bytes<128, true>() <= 232448, "shared memory budget");
@@ -1189,15 +1193,15 @@ struct CausalPlan {
     size_t off_flags, off_agg, off_incl, total;
 };
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms) {
     using namespace causal_tc;
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     CausalPlan pl{};
     pl.nchunks = (sh.N + C - 1) / C;
     pl.nhalf = DK / DV;
     if (seg_chunks <= 0)
-        seg_chunks = auto_segment_chunks<kDecay>(sh.BH() * pl.nhalf, pl.nchunks, sms);
+        seg_chunks = auto_segment_chunks<kMode != 0>(sh.BH() * pl.nhalf, pl.nchunks, sms);
     pl.seg_chunks = seg_chunks;
     pl.nseg = (pl.nchunks + seg_chunks - 1) / seg_chunks;
     pl.items = sh.BH() * pl.nseg * pl.nhalf;
@@ -1210,7 +1214,7 @@ CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms) {
     return pl;
 }
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
                          const FwdShape &sh, const DecayArgs &dk, int seg_chunks,
                          int *status, void *ws_in, size_t ws_bytes, float *S_out,
@@ -1227,7 +1231,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     int sms = 0;
     if ((e = tchost::sm_count(&sms)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: device query"};
-    const CausalPlan pl = plan_causal<DK, kDecay>(sh, seg_chunks, sms);
+    const CausalPlan pl = plan_causal<DK, kMode>(sh, seg_chunks, sms);
     if (pl.items > (1LL << 30))
         return {LA_ERR_UNSUPPORTED, cudaSuccess, "la_forward: too many work items"};
 
@@ -1262,8 +1266,8 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.status = status;
     e = tc_zero_words(ws, pl.off_agg, stream);
     if (e == cudaSuccess) {
-        const size_t smem = smem_bytes<DK, kDecay>();
-        auto kern = causal_kernel<DK, kDecay>;
+        const size_t smem = smem_bytes<DK, kMode>();
+        auto kern = causal_kernel<DK, kMode>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e == cudaSuccess) {
@@ -1349,13 +1353,13 @@ cudaError_t noalloc_scratch(char **out) {
     return cudaSuccess;
 }
 
-template <int DK, bool kDecay>
+template <int DK, int kMode>
 TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
                                  void *out, const FwdShape &sh,
                                  const DecayArgs &dk, int *status,
                                  cudaStream_t stream) {
     using namespace causal_tc;
-    using L = Layout<DK, kDecay>;
+    using L = Layout<DK, kMode>;
     const int BH = (int)sh.BH(), N = sh.N;
     CUtensorMap tq, tk, tv, to;
     cudaError_t e;
@@ -1377,7 +1381,7 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     p.N = N;
     p.nchunks = (N + C - 1) / C;
     p.nhalf = DK / DV;
-    int seg = auto_segment_chunks<kDecay>(BH * p.nhalf, p.nchunks, sms);
+    int seg = auto_segment_chunks<kMode != 0>(BH * p.nhalf, p.nchunks, sms);
     // lengthen segments until the workspace fits the static scratch
     size_t off_agg = 0, off_incl = 0, total = 0;
     long long items = 0;
@@ -1409,8 +1413,8 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     // the counter and flags must start at zero; the states need no clearing
     if ((e = tc_zero_words(scratch, off_agg, stream)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: clearing flags"};
-    const size_t smem = smem_bytes<DK, kDecay>();
-    auto kern = causal_kernel<DK, kDecay>;
+    const size_t smem = smem_bytes<DK, kMode>();
+    auto kern = causal_kernel<DK, kMode>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel attribute"};
