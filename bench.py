@@ -418,7 +418,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
              state=True)
     fwd_path("bf16_decay_b4h8_n16384_d128 retention", wd.name, True,
              decay=list(wd.decay), retention=True)
-    fwd_path(f"{MAIN} gated (CUDA cores)", MAIN, True, inputs=(q, k, v), gated=True)
+    fwd_path(f"{MAIN} gated", MAIN, True, inputs=(q, k, v), gated=True)
     try:
         res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,
                                                 args)

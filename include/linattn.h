@@ -250,8 +250,9 @@ la_status la_decode_step_variant(float *S, float *z, const void *q,
  *            on the device); outside [0, 1] the results are unspecified.
  *   variant  as la_forward_variant (NULL: elu(x) + 1 with the normaliser).
  * Other arguments as la_forward (causal) and la_decode_step.  The forward
- * runs on the fp32 CUDA-core kernels for every dtype and head size; the
- * decode step is the same kernel as la_decode_step.
+ * runs where la_forward would (bf16 with d in {64, 128}: the tcgen05
+ * kernels; otherwise the fp32 CUDA-core kernels); the decode step is the
+ * same kernel as la_decode_step.
  */
 la_status la_forward_gated(const void *q, const void *k, const void *v,
                            void *out, const float *gates, int B, int H, int N,

@@ -199,18 +199,18 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
         return fail(LA_ERR_INVALID_ARG, "la_forward_gated: gates are defined for the causal form only");
     if (gates && decay)
         return fail(LA_ERR_INVALID_ARG, "la_forward_gated: give gates or a decay, not both");
-    // the data-dependent gates run on the CUDA-core kernels
-    const bool tc_ok = !gates && tc_supported(sh, dtype, causal, q, k, v, out);
+    // gates run on the tensor cores as their third mode (no final state)
+    const bool tc_ok = tc_supported(sh, dtype, causal, q, k, v, out) &&
+                       !(gates && S_out);
     if (path == 2 && !tc_ok)
         return fail(LA_ERR_UNSUPPORTED,
-                    gates ? "la_forward_gated: the tensor-core kernels take no per-token gates"
-                          : "la_forward_ex: tensor-core path needs bf16, d in {64,128} and 16-byte aligned tensors");
+                    "la_forward_ex: tensor-core path needs bf16, d in {64,128} and 16-byte aligned tensors");
     if (tc_ok && path != 1) {
         cudaError_t ce;
         int *status = device_status_word(&ce);
         if (!status) return cuda_fail(ce, "la_forward: status word");
         TcResult r = tc_forward(q, k, v, out, sh, causal, dk, segment_chunks,
-                                status, ws, ws_bytes, S_out, z_out, s);
+                                status, ws, ws_bytes, S_out, z_out, gates, s);
         if (r.status != LA_OK) {
             if (r.status == LA_ERR_CUDA) return cuda_fail(r.cuda, r.where);
             return fail(r.status, r.where);

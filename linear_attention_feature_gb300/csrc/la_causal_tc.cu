@@ -85,6 +85,8 @@ struct Params {
     int *flags;         // [items]
     float *S_out, *z_out;  // final state [BH][DK][DK] / [BH][DK], or NULL
     int phi, norm;         // elu(x) + 1 on q, k (else identity); divide by den
+    const float *gates;    // mode 2: alpha [BH][N], a gate per token
+    float *gprod;          // mode 2: [items] each segment's product of gates
     int *ctrl;          // [0] ticket counter, [1] abort flag
     int *status;        // device status word
     long long timeout;  // clock cycles per bounded wait
@@ -93,10 +95,12 @@ struct Params {
 template <int DK, int kMode>
 struct Layout {
     static constexpr int KB = DK / 64;
-    static constexpr int STAGES = DK == 128 ? 2 : 4;
+    static constexpr int STAGES = DK == 128 ? 2 : (kMode == 2 ? 3 : 4);
     static constexpr int TILE = DK * C * 2;   // a Q or K tile (bf16)
     static constexpr int VTILE = C * DV * 2;  // a V (or O) tile half
-    static constexpr int STAGE = 2 * TILE + VTILE;
+    // mode 2: the chunk's gate prefix (GateSlot, 1 KB) after V
+    static constexpr int OFF_GS = 2 * TILE + VTILE;
+    static constexpr int STAGE = 2 * TILE + VTILE + (kMode == 2 ? 1024 : 0);
     static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 2 * TILE;
     // [S | z] in bf16: MN-major B operand [K = a][N = 80]; block 0 = S,
     // block 1 column 0 = z (rest zero)
@@ -110,7 +114,7 @@ struct Layout {
     // output staging: a buffer of its own where shared memory allows (a
     // stage is then free once its last product completes), else the stage's
     // Q slot, dead by the time the chunk's output is ready
-    static constexpr bool OWN_OST = DK == 128;
+    static constexpr bool OWN_OST = DK == 128 && kMode != 2;
     static constexpr int OFF_OST = OFF_ONESX + ONESX;
     static constexpr int OST = OWN_OST ? C * DV * 2 : 0;
     static constexpr int OFF_SMALL = OFF_OST + OST;
@@ -126,6 +130,8 @@ struct Small {
     uint64_t item_full[2], item_empty[2];
     int ring[2];
     int lb_flag[32], lb_n;  // look-back decision of the current item
+    float tg_l[8], eg_l[4];  // mode 2: per-warp gate sums (transform, state roles)
+    int tg_z[8], eg_z[4];
     uint32_t tmem_base;
 };
 
@@ -387,6 +393,116 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
     }
 }
 
+// ---------------------------------------------------------------- gates (mode 2)
+
+// Mode 2, a data-dependent gate alpha_t per token ("Linear Attention", GLA:
+// S_t = G_t (.) S_{t-1} + k_t v_t^T, here with the scalar G_t = alpha_t).
+// For the tokens of one chunk, lg2[t] is the sum of log2(alpha_u) over the
+// nonzero gates u <= t and nz[t] the number of zero gates u <= t (chunk-local
+// inclusive prefixes), so that the product of the gates u = j+1..i is
+// (nz[i] == nz[j]) ? 2^(lg2[i] - lg2[j]) : 0 -- exact where a gate is 0.
+// Tokens past N count as gate 1.  The transform warps write the slot of each
+// stage before its xf arrival; readers wait on that barrier.
+struct GateSlot {
+    float lg2[C];
+    int nz[C];
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// prod_{u=j+1..i} alpha_u within a chunk (j < i; j = -1: from the chunk's
+// first token, i.e. prod_{u<=i}).
+__device__ __forceinline__ float gate_prod(const GateSlot &g, int i, int j) {
+    const float lj = j < 0 ? 0.f : g.lg2[j];
+    const int zj = j < 0 ? 0 : g.nz[j];
+    return g.nz[i] == zj ? fast_exp2(g.lg2[i] - lj) : 0.f;
+}
+
+// log2 and zero count of one gate value
+__device__ __forceinline__ void gate_terms(float a, float &l, int &z) {
+    if (a > 0.f) {
+        l = __log2f(a);
+        z = 0;
+    } else {
+        l = 0.f;
+        z = 1;
+    }
+}
+
+// The chunk's prefixes into `g` (all transform threads call; the first 128,
+// one per token, compute).
+__device__ __forceinline__ void gate_scan(GateSlot &g, Small &sm, const Params &p,
+                                          int bh, int c, int et) {
+    const int lane = et & 31, w = et >> 5;
+    float l = 0.f;
+    int z = 0;
+    if (et < C) {
+        const int tok = c * C + et;
+        gate_terms(tok < p.N ? __ldg(p.gates + (size_t)bh * p.N + tok) : 1.f, l, z);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float lo = __shfl_up_sync(~0u, l, o);
+            const int zo = __shfl_up_sync(~0u, z, o);
+            if (lane >= o) {
+                l += lo;
+                z += zo;
+            }
+        }
+        if (lane == 31) {
+            sm.tg_l[w] = l;
+            sm.tg_z[w] = z;
+        }
+    }
+    named_bar_sync(BAR_T, kTThreads);
+    if (et < C) {
+        for (int w2 = 0; w2 < w; ++w2) {
+            l += sm.tg_l[w2];
+            z += sm.tg_z[w2];
+        }
+        g.lg2[et] = l;
+        g.nz[et] = z;
+    }
+    named_bar_sync(BAR_T, kTThreads);
+}
+
+// Totals over tokens [t0, t1) of head bh: sum of log2 of the nonzero gates
+// and the number of zero gates (`nthr` threads of one role, `tid` 0-based,
+// scratch `sl`/`sz` with one entry per warp, named barrier `bar`).
+__device__ __forceinline__ void gate_totals(float &L2, int &Z, const Params &p,
+                                            int bh, int t0, int t1, int tid,
+                                            int nthr, float *sl, int *sz, int bar) {
+    float l = 0.f;
+    int z = 0;
+    for (int tok = t0 + tid; tok < t1; tok += nthr) {
+        float lt;
+        int zt;
+        gate_terms(__ldg(p.gates + (size_t)bh * p.N + tok), lt, zt);
+        l += lt;
+        z += zt;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        l += __shfl_xor_sync(~0u, l, o);
+        z += __shfl_xor_sync(~0u, z, o);
+    }
+    if ((tid & 31) == 0) {
+        sl[tid >> 5] = l;
+        sz[tid >> 5] = z;
+    }
+    named_bar_sync(bar, nthr);
+    L2 = 0.f;
+    Z = 0;
+    for (int w = 0; w < nthr / 32; ++w) {
+        L2 += sl[w];
+        Z += sz[w];
+    }
+    named_bar_sync(bar, nthr);
+}
+
 // ---------------------------------------------------------------- transform
 
 // phi (bf16 pairs) over this thread's share of one row of a [128][DK]
@@ -464,14 +580,31 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         const float lg = head_log2g(dk, it.bh);
         if (it.hasA) {
             // phase A: Khat_t = g^(L-1-t) phi(k_t), t relative to the segment
+            // end; with gates Khat_t = prod_{u>t in the segment} alpha_u phi(k_t)
             const int seg_end = min(it.c1 * C, p.N);
+            float L2 = 0.f, off2 = 0.f;
+            int Z = 0, offz = 0;
+            if (kMode == 2)
+                gate_totals(L2, Z, p, it.bh, it.c0 * C, seg_end, et, kTThreads,
+                            sm.tg_l, sm.tg_z, BAR_T);
             for (int c = it.c0; c < it.c1; ++c, ++j) {
                 const int st = j % L::STAGES;
                 wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
                 uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
                 const int tok = c * C + row;
                 if (kMode || tok >= p.N) {
-                    const float w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
+                    float w;
+                    if (kMode == 2) {
+                        GateSlot &g = *reinterpret_cast<GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
+                        gate_scan(g, sm, p, it.bh, c, et);
+                        w = tok < p.N && Z == offz + g.nz[row]
+                                ? fast_exp2(L2 - (off2 + g.lg2[row])) : 0.f;
+                        const int nv = min(C, p.N - c * C);
+                        off2 += g.lg2[nv - 1];
+                        offz += g.nz[nv - 1];
+                    } else {
+                        w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
+                    }
                     transform_row_scaled<DK>(kt, row, part, bf2_splat(w), p.phi);
                 } else {
                     transform_row<DK>(kt, row, part, false, p.phi);
@@ -487,17 +620,21 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             uint8_t *qt = smem + st * L::STAGE + L::OFF_Q;
             uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
             const int n = min(C, p.N - c * C);
+            GateSlot &g = *reinterpret_cast<GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
+            if (kMode == 2) gate_scan(g, sm, p, it.bh, c, et);
             transform_row<DK>(qt, row, part, false, p.phi);
             transform_row<DK>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
             if (kMode) {
-                // Khat_t = g^(n-1-t) phi(k_t) in place, once P(j) (the only
-                // reader of the unweighted rows) has completed; rows past N
-                // are already zero
+                // Khat_t = g^(n-1-t) phi(k_t) in place (with gates
+                // prod_{u=t+1..n-1} alpha_u), once P(j) (the only reader of
+                // the unweighted rows) has completed; rows past N are zero
                 wait_bar(&sm.pfull[nb & 1], (nb >> 1) & 1, cx);
-                const float w = row < n ? gpow(lg, n - 1 - row) : 0.f;
+                const float w = row >= n ? 0.f
+                                         : (kMode == 2 ? gate_prod(g, n - 1, row)
+                                                       : gpow(lg, n - 1 - row));
                 scale_row<DK>(kt, row, part, bf2_splat(w));
                 fence_async_shared();
                 named_bar_sync(BAR_T, kTThreads);
@@ -512,28 +649,40 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
 // Causal mask and decay on P (fp32, TMEM), rounded to bf16 in place (the A
 // operand of P~V).  One thread per row i (= TMEM lane).
 template <int DK, int kMode>
-__device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
-                               const DecayArgs &dk, uint32_t tmem) {
+__device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
+                               const Ctx &cx, const DecayArgs &dk, uint32_t tmem) {
+    using L = Layout<DK, kMode>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int et = threadIdx.x - kWarpE1 * 32;
     const uint32_t lb = tmem + ((uint32_t)(q * 32) << 16);
-    int nb = 0, tl = 0;
+    int nb = 0, tl = 0, j = 0;
     for (;;) {
         const int t = pop_item(sm, tl, cx, BAR_E1, 128, et == 0);
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
-        if (kMode) {
+        if (kMode == 1) {
             if (et < 32) sm.gtab[et] = gpow(lg, et);
             named_bar_sync(BAR_E1, 128);
         }
-        for (int c = it.c0; c < it.c1; ++c, ++nb) {
+        if (it.hasA) j += it.c1 - it.c0;  // phase-A jobs
+        for (int c = it.c0; c < it.c1; ++c, ++nb, ++j) {
             const int b = nb & 1;
             const uint32_t tp = lb + TM_P + 128u * b;
             wait_bar(&sm.pfull[b], (nb >> 1) & 1, cx);
             tc_fence_after();
+            const GateSlot &gs = *reinterpret_cast<const GateSlot *>(
+                smem + (j % L::STAGES) * L::STAGE + L::OFF_GS);
+            float gl_i = 0.f;
+            int gz_i = 0;
+            if (kMode == 2) {
+                // the chunk's gate prefix (written before the stage's xf)
+                wait_bar(&sm.xf[j % L::STAGES], (j / L::STAGES) & 1, cx);
+                gl_i = gs.lg2[row];
+                gz_i = gs.nz[row];
+            }
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t pk[16];
@@ -546,7 +695,16 @@ __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
                     tmem_wait_ld();
                     reg_fence(v);
                     if (blk < q) {
-                        if (kMode) {
+                        if (kMode == 2) {
+                            // prod_{u=col+1..row} alpha_u
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const int c0 = 32 * blk + e;
+                                const float w0 = gz_i == gs.nz[c0] ? fast_exp2(gl_i - gs.lg2[c0]) : 0.f;
+                                const float w1 = gz_i == gs.nz[c0 + 1] ? fast_exp2(gl_i - gs.lg2[c0 + 1]) : 0.f;
+                                pk[e >> 1] = pack_bf16x2(u2f(v[e]) * w0, u2f(v[e + 1]) * w1);
+                            }
+                        } else if (kMode) {
                             // g^(row - j) = g^(row - 32 blk - 31) g^(31 - e)
                             const float base = gpow(lg, row - 32 * blk - 31);
 #pragma unroll
@@ -565,11 +723,19 @@ __device__ void score_epilogue(Small &sm, const Params &p, const Ctx &cx,
                             // diagonal block: g^(i - j) = g^(lane - e), from
                             // the head's table, only where e <= lane
                             float x0 = 0.f, x1 = 0.f;
-                            if (e <= lane)
-                                x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
-                            if (e + 1 <= lane)
-                                x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1]
-                                            : u2f(v[e + 1]);
+                            if (kMode == 2) {
+                                const int c0 = 32 * blk + e;
+                                if (e <= lane && gz_i == gs.nz[c0])
+                                    x0 = u2f(v[e]) * fast_exp2(gl_i - gs.lg2[c0]);
+                                if (e + 1 <= lane && gz_i == gs.nz[c0 + 1])
+                                    x1 = u2f(v[e + 1]) * fast_exp2(gl_i - gs.lg2[c0 + 1]);
+                            } else {
+                                if (e <= lane)
+                                    x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
+                                if (e + 1 <= lane)
+                                    x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1]
+                                                : u2f(v[e + 1]);
+                            }
                             pk[e >> 1] = pack_bf16x2(x0, x1);
                         }
                     }
@@ -600,6 +766,12 @@ __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
     const int ob = OBufs<kMode != 0>::n == 2 ? (nb & 1) : 0;
     const uint32_t tob = TM_O + 80u * ob;
     uint8_t *stage_o = L::OWN_OST ? smem + L::OFF_OST : smem + st * L::STAGE + L::OFF_Q;
+    if (kMode == 2) {
+        // this row's read of the chunk's start state: prod_{u<=i} alpha_u
+        wait_bar(&sm.xf[st], (j / L::STAGES) & 1, cx);
+        wq = gate_prod(*reinterpret_cast<const GateSlot *>(
+                           smem + st * L::STAGE + L::OFF_GS), row, -1);
+    }
     if (L::OWN_OST) {  // the previous chunk's store must have read the buffer
         if (et == 0) tma_store_wait_read<0>();
         named_bar_sync(BAR_E2, 128);
@@ -787,7 +959,8 @@ __device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
             acc[4 * e + 3] = fmaf(w, u.w, acc[4 * e + 3]);
         }
         if (zh) accz = fmaf(w, __ldcg(src + DK * DV + a), accz);
-        w *= gL;
+        // the next one back is decayed across this predecessor's segment too
+        w *= kMode == 2 ? __ldcg(p.gprod + pi) : gL;
     }
 }
 
@@ -835,12 +1008,22 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
-        const float gL = gpow(lg, p.seg_chunks * C);
-        const float wq = kMode ? gpow(lg, row + 1) : 1.f;
+        float gL = gpow(lg, p.seg_chunks * C);
+        if (kMode == 2 && it.hasA) {
+            // the segment's product of gates: scales its start state into
+            // its inclusive prefix, and is published for its successors
+            float L2;
+            int Z;
+            gate_totals(L2, Z, p, it.bh, it.c0 * C, min(it.c1 * C, p.N), et, 128,
+                        sm.eg_l, sm.eg_z, BAR_E2);
+            gL = Z == 0 ? exp2f(L2) : 0.f;
+            if (et == 0) p.gprod[t] = gL;  // visible with the item's flags
+        }
+        const float wq = kMode ? gpow(lg, row + 1) : 1.f;  // mode 2: per chunk
         float *agg = p.agg + (size_t)t * L::STATE;
         float *incl = p.incl + (size_t)t * L::STATE;
         const int n0 = min(C, p.N - it.c0 * C);
-        const float f0 = gpow(lg, n0);
+        float f0 = gpow(lg, n0);
         // Look-back, first try: if the predecessors have already published,
         // sum their states now, while phase A runs, into the threads' slots.
         bool early = false;
@@ -868,6 +1051,14 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
             tc_fence_after();
+        }
+        if (kMode == 2) {
+            // the first chunk's product of gates (its transform wrote the
+            // prefix before the stage's xf)
+            wait_bar(&sm.xf[j % L::STAGES], (j / L::STAGES) & 1, cx);
+            f0 = gate_prod(*reinterpret_cast<const GateSlot *>(
+                               smem + (j % L::STAGES) * L::STAGE + L::OFF_GS),
+                           n0 - 1, -1);
         }
         if (early) {
             // inclusive prefix = g^L S_start + local state, and the phase-B
@@ -1000,7 +1191,14 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 ++ns;
                 tc_fence_after();
                 const int n = min(C, p.N - (c + 1) * C);
-                const float f = gpow(lg, n);
+                float f = gpow(lg, n);
+                if (kMode == 2) {
+                    const int j1 = j + 1;
+                    wait_bar(&sm.xf[j1 % L::STAGES], (j1 / L::STAGES) & 1, cx);
+                    f = gate_prod(*reinterpret_cast<const GateSlot *>(
+                                      smem + (j1 % L::STAGES) * L::STAGE + L::OFF_GS),
+                                  n - 1, -1);
+                }
 #pragma unroll
                 for (int hh = 0; hh < SM::NH; ++hh) {
                     const int h = h0 + hh;
@@ -1146,7 +1344,7 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
     } else if (warp < kWarpE1) {
         transform<DK, kMode>(smem, sm, p, cx, dk);
     } else if (warp < kWarpE2) {
-        score_epilogue<DK, kMode>(sm, p, cx, dk, tmem);
+        score_epilogue<DK, kMode>(smem, sm, p, cx, dk, tmem);
     } else {
         output_state<DK, kMode>(smem, sm, p, cx, dk, tmem, &to);
     }
@@ -1179,6 +1377,8 @@ static_assert(smem_bytes<128, true>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<128, false>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<64, true>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<64, false>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<128, 2>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<64, 2>() <= 232448, "shared memory budget");
 
 }  // namespace causal_tc
 
@@ -1190,7 +1390,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct CausalPlan {
     int seg_chunks, nseg, nchunks, nhalf;
     long long items;
-    size_t off_flags, off_agg, off_incl, total;
+    size_t off_flags, off_agg, off_incl, off_gprod, total;
 };
 
 template <int DK, int kMode>
@@ -1210,7 +1410,8 @@ CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms) {
     pl.off_agg = align_up(pl.off_flags + sizeof(int) * (size_t)pl.items, 256);
     const size_t state_bytes = (pl.nseg > 1) ? sizeof(float) * L::STATE * (size_t)pl.items : 0;
     pl.off_incl = align_up(pl.off_agg + state_bytes, 256);
-    pl.total = pl.off_incl + state_bytes;
+    pl.off_gprod = align_up(pl.off_incl + state_bytes, 256);
+    pl.total = pl.off_gprod + (kMode == 2 ? sizeof(float) * (size_t)pl.items : 0);
     return pl;
 }
 
@@ -1218,7 +1419,7 @@ template <int DK, int kMode>
 TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
                          const FwdShape &sh, const DecayArgs &dk, int seg_chunks,
                          int *status, void *ws_in, size_t ws_bytes, float *S_out,
-                         float *z_out, cudaStream_t stream) {
+                         float *z_out, const float *gates, cudaStream_t stream) {
     using namespace causal_tc;
     const int BH = (int)sh.BH(), N = sh.N;
     CUtensorMap tq, tk, tv, to;
@@ -1249,6 +1450,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.z_out = z_out;
     p.phi = sh.phi;
     p.norm = sh.norm;
+    p.gates = gates;
 
     // the caller's workspace when given, else a stream-ordered allocation
     void *ws = ws_in;
@@ -1263,6 +1465,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.flags = reinterpret_cast<int *>(w8 + pl.off_flags);
     p.agg = reinterpret_cast<float *>(w8 + pl.off_agg);
     p.incl = reinterpret_cast<float *>(w8 + pl.off_incl);
+    p.gprod = reinterpret_cast<float *>(w8 + pl.off_gprod);
     p.status = status;
     e = tc_zero_words(ws, pl.off_agg, stream);
     if (e == cudaSuccess) {
@@ -1288,12 +1491,17 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
 TcResult launch_causal_tc(const void *q, const void *k, const void *v,
                           void *out, const FwdShape &sh, const DecayArgs &dk,
                           int seg_chunks, int *status, void *ws, size_t ws_bytes,
-                          float *S_out, float *z_out, cudaStream_t stream) {
+                          float *S_out, float *z_out, const float *gates,
+                          cudaStream_t stream) {
+    if (gates)
+        return sh.d == 128
+                   ? launch_causal_t<128, 2>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, gates, stream)
+                   : launch_causal_t<64, 2>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, gates, stream);
     if (sh.d == 128)
-        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream)
-                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream);
-    return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream)
-                  : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, stream);
+        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream)
+                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream);
+    return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream)
+                  : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream);
 }
 
 size_t causal_tc_workspace_bytes(const FwdShape &sh, bool decay, int seg_chunks, int sms) {

@@ -21,10 +21,11 @@ bool tc_supported(const FwdShape &sh, la_dtype dtype, int causal,
 TcResult tc_forward(const void *q, const void *k, const void *v, void *out,
                     const FwdShape &sh, int causal, const DecayArgs &dk,
                     int segment_chunks, int *status, void *ws, size_t ws_bytes,
-                    float *S_out, float *z_out, cudaStream_t stream) {
+                    float *S_out, float *z_out, const float *gates,
+                    cudaStream_t stream) {
     if (causal)
         return launch_causal_tc(q, k, v, out, sh, dk, segment_chunks, status,
-                                ws, ws_bytes, S_out, z_out, stream);
+                                ws, ws_bytes, S_out, z_out, gates, stream);
     return launch_noncausal_tc(q, k, v, out, sh, segment_chunks, status, ws,
                                ws_bytes, stream);
 }

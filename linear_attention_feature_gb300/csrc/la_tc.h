@@ -24,10 +24,12 @@ bool tc_supported(const FwdShape &sh, la_dtype dtype, int causal,
 // (cudaMallocAsync / cudaFreeAsync on `stream`).
 // S_out / z_out (causal only, may be NULL, S_out 16-byte aligned): also
 // write the final state [BH][d][d] / [BH][d] in fp32.
+// gates (causal only, may be NULL): a device [BH][N] gate per token.
 TcResult tc_forward(const void *q, const void *k, const void *v, void *out,
                     const FwdShape &sh, int causal, const DecayArgs &dk,
                     int segment_chunks, int *status, void *ws, size_t ws_bytes,
-                    float *S_out, float *z_out, cudaStream_t stream);
+                    float *S_out, float *z_out, const float *gates,
+                    cudaStream_t stream);
 
 // Scratch bytes one tensor-core forward needs on a device with `sms` SMs.
 size_t tc_workspace_bytes(const FwdShape &sh, int causal, bool decay,
@@ -52,7 +54,8 @@ size_t noncausal_tc_workspace_bytes(const FwdShape &sh, int seg_chunks, int sms)
 TcResult launch_causal_tc(const void *q, const void *k, const void *v,
                           void *out, const FwdShape &sh, const DecayArgs &dk,
                           int seg_chunks, int *status, void *ws, size_t ws_bytes,
-                          float *S_out, float *z_out, cudaStream_t stream);
+                          float *S_out, float *z_out, const float *gates,
+                          cudaStream_t stream);
 size_t causal_tc_workspace_bytes(const FwdShape &sh, bool decay, int seg_chunks, int sms);
 
 }  // namespace la

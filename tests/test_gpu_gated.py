@@ -79,3 +79,42 @@ def test_gated_decode_continues_the_gated_forward(dtype, d):
     ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy())
     tol = wl.TOL["f32"] if dtype == "f32" else wl.TOL["bf16"]
     assert wl.max_row_rel_err(torch.stack(ys, dim=2), ref) <= tol
+
+
+def test_gated_bf16_runs_on_the_tensor_cores():
+    q, k, v = (t.cuda() for t in wl.make_qkv(1, 2, 256, 64, "bf16", seed=140))
+    a = make_gates(1, 2, 256, 141).cuda()
+    n0 = la.kernel_launch_count()
+    la.forward_gated(q, k, v, a)
+    la.check_device_status()
+    assert la.kernel_launch_count() == n0 + 2  # workspace clear + tcgen05 kernel
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_gated_tensor_cores_across_segments(d):
+    # 12 heads x 40 chunks: several segments per head, so each segment's
+    # gate product travels through the look-back; zero gates sit inside
+    # middle segments and on a chunk boundary
+    B, H, N = 2, 6, 5000
+    q, k, v = wl.make_qkv(B, H, N, d, "bf16", seed=150 + d)
+    a = make_gates(B, H, N, 151 + d, lo=0.97)
+    a[1, 2, 2500] = 0.0
+    a[0, 5, 1280] = 0.0
+    y = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda())
+    la.check_device_status()
+    heads = [(0, 0), (0, 5), (1, 2), (1, 5)]
+    for b, h in heads:
+        ref = oracle.causal_gated(q[b, h][None].float(), k[b, h][None].float(),
+                                  v[b, h][None].float(), a[b, h][None].double().numpy())[0]
+        assert wl.max_row_rel_err(y[b, h].cpu(), ref) <= wl.TOL["bf16"], (b, h)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_gated_constant_gates_equal_decay_on_tensor_cores(d):
+    q, k, v = (t.cuda() for t in wl.make_qkv(1, 4, 2000, d, "bf16", seed=160 + d))
+    dec = [0.9, 0.5, 0.99, 1.0]
+    a = torch.tensor(dec).view(1, 4, 1).expand(1, 4, 2000).contiguous().cuda()
+    y = la.forward_gated(q, k, v, a)
+    r = la.forward(q, k, v, causal=True, decay=dec)
+    torch.cuda.synchronize()
+    assert wl.max_row_rel_err(y.cpu(), r.cpu()) <= wl.TOL["bf16"]
