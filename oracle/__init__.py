@@ -66,11 +66,12 @@ def _load():
     lib.ora_causal.argtypes = [P, P, P, P, L, L, L, P, I, I, I]
     lib.ora_causal_state.argtypes = [P, P, P, P, L, L, L, P, I]
     lib.ora_causal_gated.argtypes = [P, P, P, P, P, L, L, L, I, I, I]
+    lib.ora_delta_step.argtypes = [P, P, P, P, P, P, P, L, L]
     lib.ora_decode_step.argtypes = [P, P, P, P, P, P, L, L, P, I]
     lib.ora_quadratic.argtypes = [P, P, P, P, L, L, L, P, I, I, P]
     lib.ora_chunked.argtypes = [P, P, P, P, L, L, L, P, L, L]
     for name in ("ora_noncausal_state", "ora_state_read", "ora_noncausal",
-                 "ora_causal_state", "ora_causal_gated",
+                 "ora_causal_state", "ora_causal_gated", "ora_delta_step",
                  "ora_recurrent_step", "ora_causal", "ora_decode_step",
                  "ora_quadratic", "ora_chunked"):
         getattr(lib, name).restype = I
@@ -191,6 +192,27 @@ def causal_gated(q, k, v, alpha, *, fmap=FMAP_ELU1, normalise=True, nthreads=1):
     _check(_load().ora_causal_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(out),
                                     BH, N, d, fmap, int(normalise), int(nthreads)),
            "causal_gated")
+    return out
+
+
+def delta_step(S, q, k, v, beta, alpha=None):
+    """Delta-rule step on float64 state S [..., d, d] (S[a][c], a key feature,
+    c value column; updated in place): S <- alpha S + beta k (v - alpha S^T k)^T
+    in this layout; returns o = S^T q [..., d].  beta, alpha: one per head."""
+    if S.dtype != np.float64 or not S.flags.c_contiguous:
+        raise TypeError("S must be a C-contiguous float64 array (in place)")
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    d = q.shape[-1]
+    BH = q.size // d
+    b = np.ascontiguousarray(np.asarray(beta, dtype=np.float64).reshape(-1))
+    a = None if alpha is None else np.ascontiguousarray(
+        np.asarray(alpha, dtype=np.float64).reshape(-1))
+    if b.size != BH or (a is not None and a.size != BH):
+        raise ValueError("beta and alpha need one entry per head")
+    out = np.empty_like(q)
+    _check(_load().ora_delta_step(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(b),
+                                  _ptr(a) if a is not None else None, _ptr(out),
+                                  BH, d), "delta_step")
     return out
 
 

@@ -319,6 +319,43 @@ int ora_decode_step(double *S, double *z, const double *q, const double *k,
     return c.err;
 }
 
+/* Delta-rule decode step ("Story of Attention - Part 5", section 7, Gated
+ * DeltaNet / Delta Attention): one step of online gradient descent on
+ * 1/2 ||S_{t-1} k_t - v_t||^2, with the optional scalar forget gate alpha_t:
+ *   S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T,
+ *   o_t = S_t q_t
+ * (alpha = 1 without the gate; no feature map and no normaliser).  In the
+ * page's orientation S k is the value stored for key k; here S [BH][d][d] is
+ * stored transposed, S[a][c] with a the key feature and c the value column,
+ * so (S k)[c] = sum_a S[a][c] k[a].  beta [BH], alpha [BH] or NULL. */
+int ora_delta_step(double *S, const double *q, const double *k,
+                   const double *v, const double *beta, const double *alpha,
+                   double *out, long BH, long d) {
+    if (!S || !q || !k || !v || !beta || !out || BH < 0 || d <= 0) return -1;
+    double *pred = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!pred) return -2;
+    for (long h = 0; h < BH; ++h) {
+        double *Sh = S + h * d * d;
+        const double *qh = q + h * d, *kh = k + h * d, *vh = v + h * d;
+        const double a = alpha ? alpha[h] : 1.0, b = beta[h];
+        for (long c = 0; c < d; ++c) {
+            double s = 0.0;
+            for (long r = 0; r < d; ++r) s += Sh[r * d + c] * kh[r];
+            pred[c] = s;  /* S_{t-1} k_t */
+        }
+        for (long r = 0; r < d; ++r)
+            for (long c = 0; c < d; ++c)
+                Sh[r * d + c] = a * Sh[r * d + c] + b * kh[r] * (vh[c] - a * pred[c]);
+        for (long c = 0; c < d; ++c) {
+            double s = 0.0;
+            for (long r = 0; r < d; ++r) s += Sh[r * d + c] * qh[r];
+            out[h * d + c] = s;
+        }
+    }
+    free(pred);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Masked parallel (quadratic) form -- the other bracketing of the same
  * product ("Linear Attention: Removing the Softmax Buys Associativity",

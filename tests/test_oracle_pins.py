@@ -175,6 +175,64 @@ def test_decode_steps_equal_causal(decay):
 
 
 # --------------------------------------------------------------------------
+# delta rule (DeltaNet / Gated DeltaNet decode step)
+
+
+def test_delta_rule_worked_example_printed(golden):
+    g = golden("deltanet_worked_example.json")
+    # the library's layout is the page's S transposed
+    S = np.ascontiguousarray(arr(g["S_prev"]).T)
+    k, v = arr(g["k"]), arr(g["v"])
+    assert np.array_equal(S.T @ k, arr(g["prediction"]))
+    out = oracle.delta_step(S, k, k, v, [g["beta"]])
+    np.testing.assert_array_equal(S, arr(g["S_next"]).T)
+    # querying with the same key returns exactly v_t (the printed S_t k_t)
+    np.testing.assert_array_equal(out, arr(g["S_next_k"]))
+
+
+def test_delta_rule_properties():
+    rng = np.random.default_rng(60)
+    d = 6
+    S0 = rng.standard_normal((d, d))
+    k = rng.standard_normal(d)
+    k /= np.linalg.norm(k)
+    v, q = rng.standard_normal(d), rng.standard_normal(d)
+    # beta = 1 with a unit key stores v exactly: S^T k = v afterwards
+    S = S0.copy()
+    oracle.delta_step(S, q, k, v, [1.0])
+    np.testing.assert_allclose(S.T @ k, v, rtol=1e-12, atol=1e-12)
+    # directions orthogonal to k are untouched (without a gate)
+    x = rng.standard_normal(d)
+    x -= (x @ k) * k
+    np.testing.assert_allclose(S.T @ x, S0.T @ x, rtol=1e-12, atol=1e-12)
+    # beta = 0 leaves the state alone; the output reads it
+    S = S0.copy()
+    o = oracle.delta_step(S, q, k, v, [0.0])
+    np.testing.assert_array_equal(S, S0)
+    np.testing.assert_allclose(o, S0.T @ q, rtol=1e-13)
+    # alpha = 0 forgets everything: S = beta k v^T
+    S = S0.copy()
+    oracle.delta_step(S, q, k, v, [0.5], alpha=[0.0])
+    np.testing.assert_allclose(S, 0.5 * np.outer(k, v), rtol=1e-14, atol=1e-14)
+
+
+def test_gated_delta_rule_closed_form():
+    # S_t = alpha S + beta (v - alpha S k) k^T in the page's orientation,
+    # written with numpy on the transposed state
+    rng = np.random.default_rng(61)
+    d = 5
+    S0 = rng.standard_normal((d, d))
+    k, v, q = (rng.standard_normal(d) for _ in range(3))
+    a, b = 0.8, 0.3
+    P = S0.T                      # page's orientation
+    P1 = a * P + b * np.outer(v - a * P @ k, k)
+    S = S0.copy()
+    o = oracle.delta_step(S, q, k, v, [b], alpha=[a])
+    np.testing.assert_allclose(S, P1.T, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(o, P1 @ q, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
 # data-dependent scalar gate per token (GLA-style; Gated DeltaNet's alpha_t)
 
 
