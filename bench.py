@@ -441,7 +441,56 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
             decay=list(wl.decay_schedule(wdec.H)))
     except Exception as e:
         res["decode_b256h32_d128 decay"] = {"error": f"{type(e).__name__}: {e}"}
+    try:
+        res["decode_b256h32_d128 gated delta rule"] = run_delta_decode(
+            la, wl, dev, peaks, world, rank, args)
+    except Exception as e:
+        res["decode_b256h32_d128 gated delta rule"] = {"error": f"{type(e).__name__}: {e}"}
     return res
+
+
+def run_delta_decode(la, wl, dev, peaks, world, rank, args):
+    """The decode workload with the Gated DeltaNet step: beta = 0.5, alpha_h
+    = 1 - 2^(-5-h) per head, unit-norm keys; 1024 untimed prefill steps,
+    then the timed steps as one graph."""
+    import torch
+    w = wl.WORKLOADS["decode_b256h32_d128"]
+    B, H, d = w.B, w.H, w.d
+    P, T = w.extra["prefill"], w.extra["steps"]
+    if args.decode_steps:
+        T = args.decode_steps
+    q, k, v = wl.make_decode_tokens(B, H, d, P + T, "bf16", seed=300 + rank,
+                                    device=dev)
+    k = (k.float() / k.float().norm(dim=-1, keepdim=True)).to(k.dtype)
+    S = torch.zeros(B, H, d, d, device=dev)
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    beta = torch.full((B, H), 0.5, device=dev)
+    alpha = torch.tensor(wl.decay_schedule(H), dtype=torch.float32,
+                         device=dev).expand(B, H).contiguous()
+    step = lambda t: la.decode_step_delta(S, q[t], k[t], v[t], beta, alpha, out=o)  # noqa
+    for t in range(P):
+        step(t)
+    replay, _ = capture(lambda: [step(t) for t in range(P, P + T)])
+    S.zero_()
+    for t in range(P):
+        step(t)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    la.check_device_status()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world)
+    ms = ms_total / T
+    byts = B * H * (2 * d * d * 4 + 4 * d * 2 + 8)  # S read and written, q k v o, beta alpha
+    return {"tokens_per_s": round(B * T * world / (ms_total * 1e-3), 1),
+            "ms_per_step": round(ms, 5), "steps": T, "prefill": P,
+            "roofline": roofline_hbm(byts, ms, peaks["hbm_gbs"])}
 
 
 def decode_bytes(BH, d, elem):

@@ -263,6 +263,30 @@ la_status la_decode_step_gated(float *S, float *z, const void *q, const void *k,
                                int B, int H, int d, la_dtype dtype,
                                const la_variant *variant, la_stream_t stream);
 
+/*
+ * la_decode_step_delta -- one delta-rule decode step per head ("Story of
+ * Attention - Part 5", section 7, Gated DeltaNet / Delta Attention: one step
+ * of online gradient descent on 1/2 ||S_{t-1} k_t - v_t||^2, with the scalar
+ * forget gate alpha_t):
+ *   S_t = alpha S_{t-1} + beta (v_t - alpha S_{t-1} k_t) k_t^T,  o_t = S_t q_t
+ * in the page's orientation, where S k is the value stored for key k.  No
+ * feature map and no normaliser (the page's form; a model normalises k).
+ *   S        [B][H][d][d] fp32 device, read and written in place, stored as
+ *            in la_decode_step: S[a][c] with a the key feature and c the
+ *            value column (the transpose of the page's S).
+ *   q, k, v  [B][H][d] device, dtype `dtype`, read only.
+ *   out      [B][H][d] device, dtype `dtype`, written.
+ *   beta     DEVICE fp32 [B][H]: this step's update strength per head.
+ *   alpha    DEVICE fp32 [B][H]: this step's forget gate per head, or NULL
+ *            for alpha = 1 (plain DeltaNet).  beta and alpha are not checked
+ *            (the page's ranges are beta in [0, 1], alpha in (0, 1)).
+ *   B, H >= 0 (B*H == 0 is a no-op), d in 1..LA_MAX_D.
+ */
+la_status la_decode_step_delta(float *S, const void *q, const void *k,
+                               const void *v, void *out, const float *beta,
+                               const float *alpha, int B, int H, int d,
+                               la_dtype dtype, la_stream_t stream);
+
 /* Size of the fixed device scratch used by la_forward_causal_noalloc. */
 #define LA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

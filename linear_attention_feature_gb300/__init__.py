@@ -15,6 +15,7 @@ import os
 from . import build as _build
 
 __all__ = ["forward", "forward_variant", "forward_gated", "decode_step_gated",
+           "decode_step_delta",
            "forward_causal_state", "forward_host",
            "host_workspace_bytes", "decode_step",
            "check_device_status",
@@ -31,7 +32,7 @@ EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_forward_causal_noalloc", "la_forward_host",
             "la_forward_host_workspace_bytes", "la_forward_causal_state",
             "la_decode_step_ex", "la_forward_variant", "la_decode_step_variant",
-            "la_forward_gated", "la_decode_step_gated")
+            "la_forward_gated", "la_decode_step_gated", "la_decode_step_delta")
 
 FEATURE_MAPS = {"elu1": 0, "identity": 1}
 
@@ -76,6 +77,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.la_decode_step_variant.argtypes = [V, V, V, V, V, V, I, I, I, F, I, VP, V]
     lib.la_forward_gated.argtypes = [V, V, V, V, V, I, I, I, I, I, VP, V]
     lib.la_decode_step_gated.argtypes = [V, V, V, V, V, V, V, I, I, I, I, VP, V]
+    lib.la_decode_step_delta.argtypes = [V, V, V, V, V, V, V, I, I, I, I, V]
     lib.la_forward_host.argtypes = [V, V, V, V, I, I, I, I, I, F, I, V,
                                     ctypes.c_size_t, V]
     lib.la_forward_host_workspace_bytes.argtypes = [I, I, I, I, I]
@@ -91,7 +93,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     for n in ("la_forward", "la_forward_ex", "la_decode_step", "la_forward_host",
               "la_decode_step_ex", "la_forward_causal_state",
               "la_forward_variant", "la_decode_step_variant",
-              "la_forward_gated", "la_decode_step_gated",
+              "la_forward_gated", "la_decode_step_gated", "la_decode_step_delta",
               "la_check_device_status", "la_abi_version"):
         getattr(lib, n).restype = I
     if path is None:
@@ -247,6 +249,34 @@ def decode_step_gated(S, z, q, k, v, gates, out=None, *, feature_map="elu1",
             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
             ctypes.c_void_p(gates.data_ptr()), B, H, d, _dtype_code(q),
             _variant(feature_map, normalise), _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out
+
+
+def decode_step_delta(S, q, k, v, beta, alpha=None, out=None, *, stream=None):
+    """One delta-rule step per head (Gated DeltaNet with `alpha`): S [B, H,
+    d, d] fp32 (S[a][c], a key feature) updated in place; beta, alpha
+    [B, H] fp32 on the GPU; returns o = S_t^T q [B, H, d]."""
+    torch = _torch()
+    if q.dim() != 3 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, d] shape")
+    B, H, d = q.shape
+    if tuple(S.shape) != (B, H, d, d) or S.dtype != torch.float32:
+        raise ValueError("S must be float32 [B, H, d, d]")
+    for name, t in (("beta", beta), ("alpha", alpha)):
+        if t is not None and (tuple(t.shape) != (B, H) or t.dtype != torch.float32):
+            raise ValueError(f"{name} must be float32 [B, H]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda(S, q, k, v, out, beta, *([alpha] if alpha is not None else []))
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_decode_step_delta(
+            ctypes.c_void_p(S.data_ptr()), ctypes.c_void_p(q.data_ptr()),
+            ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+            ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(beta.data_ptr()),
+            ctypes.c_void_p(alpha.data_ptr() if alpha is not None else None),
+            B, H, d, _dtype_code(q), _stream_ptr(stream, q.device))
     _raise_if(st)
     return out
 

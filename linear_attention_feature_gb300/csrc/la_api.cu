@@ -315,6 +315,30 @@ la_status la_forward_gated(const void *q, const void *k, const void *v,
 }
 
 __attribute__((visibility("default")))
+la_status la_decode_step_delta(float *S, const void *q, const void *k,
+                               const void *v, void *out, const float *beta,
+                               const float *alpha, int B, int H, int d,
+                               la_dtype dtype, la_stream_t stream) {
+    if (!S || !q || !k || !v || !out || !beta)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step_delta: null pointer");
+    if (B < 0 || H < 0)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step_delta: negative B or H");
+    if (d < 1 || d > LA_MAX_D)
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step_delta: d must be in 1..256");
+    if (!valid_dtype(dtype))
+        return fail(LA_ERR_INVALID_ARG, "la_decode_step_delta: unknown dtype");
+    const long long BH = (long long)B * H;
+    if (BH == 0) return LA_OK;
+    if (BH > 2147483647LL)
+        return fail(LA_ERR_UNSUPPORTED, "la_decode_step_delta: too many heads");
+    cudaError_t e = launch_delta_step(S, q, k, v, out, beta, alpha, BH, d, dtype,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "la_decode_step_delta");
+    note_launches(1);
+    return LA_OK;
+}
+
+__attribute__((visibility("default")))
 la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k,
                             const void *v, void *out, int B, int H, int d,
                             const float *decay, la_dtype dtype,

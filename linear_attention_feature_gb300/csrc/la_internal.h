@@ -40,6 +40,13 @@ cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
                                 float *S_out, float *z_out, const float *gates,
                                 cudaStream_t stream);
 
+// ---- delta-rule decode step (S only; beta, alpha device [BH], alpha may
+// be NULL) ----
+cudaError_t launch_delta_step(float *S, const void *q, const void *k,
+                              const void *v, void *out, const float *beta,
+                              const float *alpha, long long BH, int d,
+                              la_dtype dtype, cudaStream_t stream);
+
 // ---- recurrent decode step ----
 // phi / norm as in FwdShape; gates (may be NULL): a device [BH] gate per
 // head for this step, used instead of the per-head decay.

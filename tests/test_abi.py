@@ -245,3 +245,15 @@ def test_gated_entry_points_reject_bad_arguments(lib):
     assert d(P, P, P, P, P, OUT, None, 1, 2, 64, 1, None, None) == INVALID
     assert d(P, P, P, P, P, OUT, G, 1, 2, 0, 1, None, None) == INVALID
     assert d(P, P, P, P, P, OUT, G, 0, 2, 64, 1, None, None) == OK
+
+
+def test_decode_step_delta_rejects_bad_arguments(lib):
+    f = lib.la_decode_step_delta
+    BETA = ctypes.c_void_p(0x600000)
+    assert f(P, P, P, P, OUT, None, None, 1, 2, 64, 1, None) == INVALID
+    assert "null" in lib.la_last_error().decode()
+    assert f(None, P, P, P, OUT, BETA, None, 1, 2, 64, 1, None) == INVALID
+    assert f(P, P, P, P, OUT, BETA, None, -1, 2, 64, 1, None) == INVALID
+    assert f(P, P, P, P, OUT, BETA, None, 1, 2, 300, 1, None) == INVALID
+    assert f(P, P, P, P, OUT, BETA, None, 1, 2, 64, 4, None) == INVALID
+    assert f(P, P, P, P, OUT, BETA, None, 0, 2, 64, 1, None) == OK
