@@ -129,7 +129,7 @@ la_status la_forward_ex(const void *q, const void *k, const void *v,
  *   q, k, v   [B][H][N][d] host, dtype `dtype`, read only.  Page-locked
  *             memory (cudaHostAlloc, cudaHostRegister, torch pin_memory)
  *             gives asynchronous full-speed copies; pageable memory works,
- *             but the driver stages its copies and the call then blocks.
+ *             but the CUDA driver stages its copies and the call then blocks.
  *   out       [B][H][N][d] host, written; may not alias q, k or v.
  *   B, H, N, d, causal, decay, dtype   as la_forward (decay is a host
  *             array of H floats, read during the call).

@@ -73,7 +73,7 @@ def test_host_fp32_small_single_group_ragged():
 
 def test_host_pageable_buffers():
     q, k, v = wl.make_qkv(2, 4, 1024, 64, "bf16", seed=35)
-    out = torch.empty_like(q)  # pageable: the driver stages the copies
+    out = torch.empty_like(q)  # pageable: the CUDA driver stages the copies
     la.forward_host(q.contiguous(), k.contiguous(), v.contiguous(), causal=True, out=out)
     torch.cuda.current_stream().synchronize()
     ref = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True).cpu()
