@@ -622,13 +622,28 @@ def run_reference(args):
 
 
 def run_kernel_case(B, H, N, d, form):
-    """Four calls of one forward on seeded inputs (no timing, no output)."""
+    """Four calls of one forward (or, for FORM decode / delta, four decode
+    steps on a [B, H, d, d] state; N is ignored) on seeded inputs (no timing,
+    no output)."""
     import torch
     import linear_attention_feature_gb300 as la
     from linear_attention_feature_gb300 import workloads as wl
     B, H, N, d = int(B), int(H), int(N), int(d)
     la.build.build()
     la.load_library()
+    if form in ("decode", "delta"):
+        q, k, v = wl.make_decode_tokens(B, H, d, 4, "bf16", seed=0, device="cuda")
+        S = torch.zeros(B, H, d, d, device="cuda")
+        z = torch.zeros(B, H, d, device="cuda")
+        beta = torch.full((B, H), 0.5, device="cuda")
+        for t in range(4):
+            if form == "decode":
+                la.decode_step(S, z, q[t], k[t], v[t])
+            else:
+                la.decode_step_delta(S, q[t], k[t], v[t], beta)
+        torch.cuda.synchronize()
+        la.check_device_status()
+        return
     q, k, v = wl.make_qkv(B, H, N, d, "bf16", seed=0, device="cuda")
     out = torch.empty_like(q)
     decay = list(wl.decay_schedule(H)) if form == "decay" else None
@@ -654,7 +669,8 @@ def main():
     ap.add_argument("--kernel-case", nargs=5,
                     metavar=("B", "H", "N", "D", "FORM"),
                     help="run one forward (FORM: causal, noncausal or decay) "
-                         "four times and exit; a driver for ncu captures")
+                         "or decode step (FORM: decode or delta) four times "
+                         "and exit; a driver for ncu captures")
     args = ap.parse_args()
     if args.kernel_case:
         run_kernel_case(*args.kernel_case)
