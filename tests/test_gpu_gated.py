@@ -118,3 +118,30 @@ def test_gated_constant_gates_equal_decay_on_tensor_cores(d):
     r = la.forward(q, k, v, causal=True, decay=dec)
     torch.cuda.synchronize()
     assert wl.max_row_rel_err(y.cpu(), r.cpu()) <= wl.TOL["bf16"]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_gated_retention_on_tensor_cores(d):
+    q, k, v = wl.make_qkv(1, 3, 1500, d, "bf16", seed=190 + d)
+    a = make_gates(1, 3, 1500, 191 + d, lo=0.9)
+    y = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(),
+                         feature_map="identity", normalise=False)
+    la.check_device_status()
+    ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy(),
+                              fmap=oracle.FMAP_IDENTITY, normalise=False, nthreads=3)
+    assert wl.max_row_rel_err(y.cpu(), ref) <= wl.TOL["bf16"]
+
+
+def test_gated_long_head_many_segments():
+    # one head of 2^16 tokens: dozens of segments whose gate products chain
+    # through the look-back; gates close to 1 keep old state alive, with a
+    # reset in the middle
+    N, d = 1 << 16, 64
+    q, k, v = wl.make_qkv(1, 1, N, d, "bf16", seed=200)
+    a = make_gates(1, 1, N, 201, lo=0.999)
+    a[0, 0, N // 2 + 77] = 0.0
+    y = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda())
+    la.check_device_status()
+    ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy())
+    idx = np.r_[0:128, N // 2:N // 2 + 256, N - 256:N]
+    assert wl.max_row_rel_err(y[0, 0].cpu()[idx], ref[0, 0][idx]) <= wl.TOL["bf16"]
