@@ -98,9 +98,12 @@ struct Layout {
     static constexpr int STAGES = DK == 128 ? 2 : (kMode == 2 ? 3 : 4);
     static constexpr int TILE = DK * C * 2;   // a Q or K tile (bf16)
     static constexpr int VTILE = C * DV * 2;  // a V (or O) tile half
-    // mode 2: the chunk's gate prefix (GateSlot, 1 KB) after V
+    // mode 2: the chunk's gate prefix and column factors (GateSlot, 1.5 KB,
+    // padded to keep every stage 1024-byte aligned) after V
+    static constexpr int GS = kMode == 2 ? 2048 : 0;
     static constexpr int OFF_GS = 2 * TILE + VTILE;
-    static constexpr int STAGE = 2 * TILE + VTILE + (kMode == 2 ? 1024 : 0);
+    static constexpr int STAGE = 2 * TILE + VTILE + GS;
+    static_assert(STAGE % 1024 == 0, "SW128 tiles need 1024-byte aligned stages");
     static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = 2 * TILE;
     // [S | z] in bf16: MN-major B operand [K = a][N = 80]; block 0 = S,
     // block 1 column 0 = z (rest zero)
@@ -401,12 +404,18 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
 // nonzero gates u <= t and nz[t] the number of zero gates u <= t (chunk-local
 // inclusive prefixes), so that the product of the gates u = j+1..i is
 // (nz[i] == nz[j]) ? 2^(lg2[i] - lg2[j]) : 0 -- exact where a gate is 0.
-// Tokens past N count as gate 1.  The transform warps write the slot of each
+// Tokens past N count as gate 1.  colf[j] is the product of the gates
+// u = j+1 .. e(j), e(j) the last token of j's 32-token block, so that where
+// j's block lies wholly before row i's block the product u = j+1..i factors
+// into a per-row term (u = e(j)+1..i) times colf[j]; both factors lie in
+// [0, 1] and neither overflows.  The transform warps write the slot of each
 // stage before its xf arrival; readers wait on that barrier.
 struct GateSlot {
     float lg2[C];
     int nz[C];
+    float colf[C];
 };
+static_assert(sizeof(GateSlot) <= 2048, "GateSlot outgrows its stage slot");
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -433,16 +442,21 @@ __device__ __forceinline__ void gate_terms(float a, float &l, int &z) {
     }
 }
 
-// The chunk's prefixes into `g` (all transform threads call; the first 128,
-// one per token, compute).
-__device__ __forceinline__ void gate_scan(GateSlot &g, Small &sm, const Params &p,
-                                          int bh, int c, int et) {
+// Gate of token et of chunk c (1 past N); transform threads et >= C get 1.
+__device__ __forceinline__ float gate_load(const Params &p, int bh, int c, int et) {
+    const int tok = c * C + et;
+    return et < C && tok < p.N ? __ldg(p.gates + (size_t)bh * p.N + tok) : 1.f;
+}
+
+// The chunk's prefixes and column factors into `g` from the gates `a` the
+// calling threads loaded (all transform threads call; the first 128, one
+// per token, compute).
+__device__ __forceinline__ void gate_scan(GateSlot &g, Small &sm, float a, int et) {
     const int lane = et & 31, w = et >> 5;
     float l = 0.f;
     int z = 0;
     if (et < C) {
-        const int tok = c * C + et;
-        gate_terms(tok < p.N ? __ldg(p.gates + (size_t)bh * p.N + tok) : 1.f, l, z);
+        gate_terms(a, l, z);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float lo = __shfl_up_sync(~0u, l, o);
@@ -467,6 +481,10 @@ __device__ __forceinline__ void gate_scan(GateSlot &g, Small &sm, const Params &
         g.nz[et] = z;
     }
     named_bar_sync(BAR_T, kTThreads);
+    if (et < C) {
+        const int e = et | 31;
+        g.colf[et] = g.nz[e] == z ? fast_exp2(g.lg2[e] - l) : 0.f;
+    }
 }
 
 // Totals over tokens [t0, t1) of head bh: sum of log2 of the nonzero gates
@@ -477,12 +495,24 @@ __device__ __forceinline__ void gate_totals(float &L2, int &Z, const Params &p,
                                             int nthr, float *sl, int *sz, int bar) {
     float l = 0.f;
     int z = 0;
-    for (int tok = t0 + tid; tok < t1; tok += nthr) {
-        float lt;
-        int zt;
-        gate_terms(__ldg(p.gates + (size_t)bh * p.N + tok), lt, zt);
-        l += lt;
-        z += zt;
+    const float *ga = p.gates + (size_t)bh * p.N;
+    // eight loads in flight per thread before any is used
+    constexpr int kBatch = 8;
+    for (int t = t0 + tid; t < t1; t += kBatch * nthr) {
+        float a[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int tok = t + u * nthr;
+            a[u] = tok < t1 ? __ldg(ga + tok) : 1.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            float lt;
+            int zt;
+            gate_terms(a[u], lt, zt);
+            l += lt;
+            z += zt;
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -578,17 +608,23 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
+        float gnext = 1.f;  // mode 2: gates of the next chunk this role transforms
         if (it.hasA) {
             // phase A: Khat_t = g^(L-1-t) phi(k_t), t relative to the segment
             // end; with gates Khat_t = prod_{u>t in the segment} alpha_u phi(k_t)
             const int seg_end = min(it.c1 * C, p.N);
             float L2 = 0.f, off2 = 0.f;
             int Z = 0, offz = 0;
-            if (kMode == 2)
+            if (kMode == 2) {
+                gnext = gate_load(p, it.bh, it.c0, et);
                 gate_totals(L2, Z, p, it.bh, it.c0 * C, seg_end, et, kTThreads,
                             sm.tg_l, sm.tg_z, BAR_T);
+            }
             for (int c = it.c0; c < it.c1; ++c, ++j) {
                 const int st = j % L::STAGES;
+                // the next chunk's gates (phase B restarts at c0)
+                const float gcur = gnext;
+                if (kMode == 2) gnext = gate_load(p, it.bh, c + 1 < it.c1 ? c + 1 : it.c0, et);
                 wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
                 uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
                 const int tok = c * C + row;
@@ -596,7 +632,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                     float w;
                     if (kMode == 2) {
                         GateSlot &g = *reinterpret_cast<GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
-                        gate_scan(g, sm, p, it.bh, c, et);
+                        gate_scan(g, sm, gcur, et);
                         w = tok < p.N && Z == offz + g.nz[row]
                                 ? fast_exp2(L2 - (off2 + g.lg2[row])) : 0.f;
                         const int nv = min(C, p.N - c * C);
@@ -614,14 +650,17 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                 if (et == 0) mbar_arrive(&sm.xf[st]);
             }
         }
+        if (kMode == 2 && !it.hasA) gnext = gate_load(p, it.bh, it.c0, et);
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % L::STAGES;
+            const float gcur = gnext;
+            if (kMode == 2 && c + 1 < it.c1) gnext = gate_load(p, it.bh, c + 1, et);
             wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
             uint8_t *qt = smem + st * L::STAGE + L::OFF_Q;
             uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
             const int n = min(C, p.N - c * C);
             GateSlot &g = *reinterpret_cast<GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
-            if (kMode == 2) gate_scan(g, sm, p, it.bh, c, et);
+            if (kMode == 2) gate_scan(g, sm, gcur, et);
             transform_row<DK>(qt, row, part, false, p.phi);
             transform_row<DK>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
             fence_async_shared();
@@ -696,14 +735,15 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
                     reg_fence(v);
                     if (blk < q) {
                         if (kMode == 2) {
-                            // prod_{u=col+1..row} alpha_u
+                            // prod_{u=col+1..row} alpha_u = (prod over
+                            // u = e+1..row) colf[col], e the block's last token
+                            const int e = 32 * blk + 31;
+                            const float base = gz_i == gs.nz[e] ? fast_exp2(gl_i - gs.lg2[e]) : 0.f;
 #pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int c0 = 32 * blk + e;
-                                const float w0 = gz_i == gs.nz[c0] ? fast_exp2(gl_i - gs.lg2[c0]) : 0.f;
-                                const float w1 = gz_i == gs.nz[c0 + 1] ? fast_exp2(gl_i - gs.lg2[c0 + 1]) : 0.f;
-                                pk[e >> 1] = pack_bf16x2(u2f(v[e]) * w0, u2f(v[e + 1]) * w1);
-                            }
+                            for (int e2 = 0; e2 < 32; e2 += 2)
+                                pk[e2 >> 1] = pack_bf16x2(
+                                    u2f(v[e2]) * (base * gs.colf[32 * blk + e2]),
+                                    u2f(v[e2 + 1]) * (base * gs.colf[32 * blk + e2 + 1]));
                         } else if (kMode) {
                             // g^(row - j) = g^(row - 32 blk - 31) g^(31 - e)
                             const float base = gpow(lg, row - 32 * blk - 31);
