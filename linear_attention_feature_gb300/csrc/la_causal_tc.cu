@@ -408,13 +408,19 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
 // u = j+1 .. e(j), e(j) the last token of j's 32-token block, so that where
 // j's block lies wholly before row i's block the product u = j+1..i factors
 // into a per-row term (u = e(j)+1..i) times colf[j]; both factors lie in
-// [0, 1] and neither overflows.  The transform warps write the slot of each
-// stage before its xf arrival; readers wait on that barrier.
+// [0, 1] and neither overflows.  colg[j] = 2^(lg2[s] - lg2[j]), s the token
+// before j's block, serves the diagonal block (row and column in one block)
+// where that block has no zero gate and a log2 span within kGateSpan: the
+// product is then 2^(lg2[i] - lg2[s]) colg[j], both factors normal floats.
+// The transform warps write the slot of each stage before its xf arrival;
+// readers wait on that barrier.
 struct GateSlot {
     float lg2[C];
     int nz[C];
     float colf[C];
+    float colg[C];
 };
+constexpr float kGateSpan = 100.f;
 static_assert(sizeof(GateSlot) <= 2048, "GateSlot outgrows its stage slot");
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -482,8 +488,10 @@ __device__ __forceinline__ void gate_scan(GateSlot &g, Small &sm, float a, int e
     }
     named_bar_sync(BAR_T, kTThreads);
     if (et < C) {
-        const int e = et | 31;
+        const int e = et | 31, s = (et & ~31) - 1;
         g.colf[et] = g.nz[e] == z ? fast_exp2(g.lg2[e] - l) : 0.f;
+        // >= 1; clamped, as blocks past the span never read it
+        g.colg[et] = fast_exp2(fminf((s < 0 ? 0.f : g.lg2[s]) - l, kGateSpan + 1.f));
     }
 }
 
@@ -757,25 +765,47 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
                             for (int e = 0; e < 32; e += 2)
                                 pk[e >> 1] = pack_bf16x2(u2f(v[e]), u2f(v[e + 1]));
                         }
+                    } else if (kMode == 2) {
+                        // diagonal block: prod_{u=col+1..row} alpha_u, only
+                        // where col <= row.  s is the token before the block.
+                        const int s = 32 * blk - 1, eb = 32 * blk + 31;
+                        const float ls = s < 0 ? 0.f : gs.lg2[s];
+                        const int zs = s < 0 ? 0 : gs.nz[s];
+                        if (gs.nz[eb] == zs && ls - gs.lg2[eb] <= kGateSpan) {
+                            // no zero gate, span in range (warp-uniform)
+                            const float rf = fast_exp2(gl_i - ls);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const float x0 = e <= lane
+                                    ? u2f(v[e]) * (rf * gs.colg[32 * blk + e]) : 0.f;
+                                const float x1 = e + 1 <= lane
+                                    ? u2f(v[e + 1]) * (rf * gs.colg[32 * blk + e + 1]) : 0.f;
+                                pk[e >> 1] = pack_bf16x2(x0, x1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const int c0 = 32 * blk + e;
+                                const float a0 = fast_exp2(fminf(gl_i - gs.lg2[c0], 0.f));
+                                const float a1 = fast_exp2(fminf(gl_i - gs.lg2[c0 + 1], 0.f));
+                                const float x0 = e <= lane && gz_i == gs.nz[c0]
+                                    ? u2f(v[e]) * a0 : 0.f;
+                                const float x1 = e + 1 <= lane && gz_i == gs.nz[c0 + 1]
+                                    ? u2f(v[e + 1]) * a1 : 0.f;
+                                pk[e >> 1] = pack_bf16x2(x0, x1);
+                            }
+                        }
                     } else {
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
                             // diagonal block: g^(i - j) = g^(lane - e), from
                             // the head's table, only where e <= lane
                             float x0 = 0.f, x1 = 0.f;
-                            if (kMode == 2) {
-                                const int c0 = 32 * blk + e;
-                                if (e <= lane && gz_i == gs.nz[c0])
-                                    x0 = u2f(v[e]) * fast_exp2(gl_i - gs.lg2[c0]);
-                                if (e + 1 <= lane && gz_i == gs.nz[c0 + 1])
-                                    x1 = u2f(v[e + 1]) * fast_exp2(gl_i - gs.lg2[c0 + 1]);
-                            } else {
-                                if (e <= lane)
-                                    x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
-                                if (e + 1 <= lane)
-                                    x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1]
-                                                : u2f(v[e + 1]);
-                            }
+                            if (e <= lane)
+                                x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
+                            if (e + 1 <= lane)
+                                x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1]
+                                            : u2f(v[e + 1]);
                             pk[e >> 1] = pack_bf16x2(x0, x1);
                         }
                     }

@@ -145,3 +145,21 @@ def test_gated_long_head_many_segments():
     ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy())
     idx = np.r_[0:128, N // 2:N // 2 + 256, N - 256:N]
     assert wl.max_row_rel_err(y[0, 0].cpu()[idx], ref[0, 0][idx]) <= wl.TOL["bf16"]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_gated_tiny_gates_exceed_the_factored_range(d):
+    # heads 0, 2: gates 2^-U(0, 8), whose 32-token spans of log2 overshoot
+    # what a product of two normal floats covers, so the diagonal score
+    # blocks form each weight directly; heads 1, 3: gates in [0.95, 1), the
+    # factored form; a zero gate in one block of head 1
+    N = 1000
+    q, k, v = wl.make_qkv(1, 4, N, d, "bf16", seed=210 + d)
+    g = torch.Generator().manual_seed(211 + d)
+    a = 0.95 + 0.05 * torch.rand(1, 4, N, generator=g)
+    a[:, 0::2] = torch.exp2(-8.0 * torch.rand(1, 2, N, generator=g))
+    a[0, 1, 300] = 0.0
+    y = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda())
+    la.check_device_status()
+    ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy(), nthreads=4)
+    assert wl.max_row_rel_err(y.cpu(), ref) <= wl.TOL["bf16"]
