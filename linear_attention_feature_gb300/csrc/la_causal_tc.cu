@@ -66,18 +66,15 @@ constexpr int kWarpT = 2, kNumT = 8, kWarpE1 = 10, kWarpE2 = 14;
 constexpr int kThreads = (kWarpE2 + 4) * 32;  // 576
 constexpr int kTThreads = kNumT * 32;
 constexpr int BAR_T = 1, BAR_E1 = 2, BAR_E2 = 3;
-// TMEM columns: P in two buffers (2 x 128); O | den (80) in two buffers
-// without decay, or O | den and the inter-chunk O | den (80 each) with
-// decay; S | z (80).  496 of 512 columns either way.
-constexpr uint32_t TM_P = 0, TM_O = 256, TM_OQS = 336, TM_S = 416;
+// TMEM columns: P in two buffers (2 x 128); O | den (80) in two buffers;
+// S | z (80).  496 of 512 columns.
+constexpr uint32_t TM_P = 0, TM_O = 256, TM_S = 416;
 constexpr uint32_t TM_COLS = 512;
 constexpr int NX = DV + 16;  // extended N of the wide products
 // Kernel mode: 0 no decay, 1 per-head decay g, 2 data-dependent gate per
-// token.  Modes 1 and 2 share the structure of the weighted kernel (a
-// separate inter-chunk accumulator, weighted K rows); they differ only in how
-// the weights are formed (powers of g, or products of gates).
-template <bool kWeighted>
-struct OBufs { static constexpr int n = kWeighted ? 1 : 2; };
+// token.  Modes 1 and 2 share the structure of the weighted kernel (Q and K
+// rows weighted in place once P has read them); they differ only in how the
+// weights are formed (powers of g, or products of gates).
 
 struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
@@ -129,7 +126,11 @@ struct Small {
     uint64_t full[4], empty[4], xf[4];
     uint64_t pfull[2], pt_ready[2], pv_done[2], o_full[2], o_empty[2];
     uint64_t s_full, sb_ready;
-    uint64_t khat_ready;  // with decay: the stage's K rows carry their weights
+    // with weights: chunk nb's Q and K rows carry their weights (two, by the
+    // parity of nb: the transform may complete chunk nb + 1 before the MMA
+    // issuer has observed chunk nb, never nb + 2, since P(nb + 2) is only
+    // issued after that observation)
+    uint64_t khat_ready[2];
     uint64_t item_full[2], item_empty[2];
     int ring[2];
     int lb_flag[32], lb_n;  // look-back decision of the current item
@@ -266,11 +267,10 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
     constexpr uint32_t idQS = idesc_bf16(128, NX, 0, 1);  // phi(Q) [S | z]
     constexpr uint32_t idSU = idesc_bf16(128, NX, 1, 1);  // phi(K)^T [V | 1]
     constexpr uint32_t lboA = DK == 128 ? 16384 : 0;      // d=64: rows 64..127 alias
-    constexpr int NOB = OBufs<kMode != 0>::n;
     // chunk order: P~V first where the look-back and state epilogue are the
     // longer latency (d = 64); phi(Q) [S | z] first where the feature-map
-    // ring is (d = 128, two stages) and with decay (one O buffer)
-    constexpr bool kPVFirst = !kMode && DK == 64;
+    // ring is (d = 128, two stages)
+    constexpr bool kPVFirst = DK == 64;
     const uint32_t sb = smem_u32(smem + L::OFF_SB);
     const uint32_t onesx = smem_u32(smem + L::OFF_ONESX);
     int j = 0, nb = 0, nsb = 0, tl = 0;
@@ -315,9 +315,9 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             const uint32_t qb = smem_u32(smem + st * L::STAGE + L::OFF_Q);
             const uint32_t kb = smem_u32(smem + st * L::STAGE + L::OFF_K);
             const uint32_t vb = smem_u32(smem + st * L::STAGE + L::OFF_V);
-            const int ob = NOB == 2 ? (nbq & 1) : 0;
+            const int ob = nbq & 1;
             const uint32_t tob = TM_O + 80u * ob;
-            wait_bar(&sm.o_empty[ob], ((NOB == 2 ? (nbq >> 1) : nbq) & 1) ^ 1, cx);
+            wait_bar(&sm.o_empty[ob], ((nbq >> 1) & 1) ^ 1, cx);
             if (kPVFirst) {
                 // The state-independent half first: P~V(j) and P(j+1) fill
                 // the tensor pipe while the state epilogue (or, for the
@@ -332,6 +332,8 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 try_issue_next_p<DK, kMode>(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
                 wait_bar(&sm.sb_ready, nsb & 1, cx);
                 ++nsb;
+                // with weights: Qhat, Khat in place (after P(j) read them)
+                if (kMode) wait_bar(&sm.khat_ready[nbq & 1], (nbq >> 1) & 1, cx);
                 tc_fence_after();
                 for (int ks = 0; ks < DK / 16; ++ks)
                     mma_ss(tmem + tob, sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
@@ -348,21 +350,17 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 // state update run while the score epilogue works on P(j).
                 wait_bar(&sm.sb_ready, nsb & 1, cx);
                 ++nsb;
+                // with weights: Qhat_i = g^(i+1) phi(q_i) and Khat_t =
+                // g^(n-1-t) phi(k_t) (or the products of gates) in place,
+                // once P(j) has read the unweighted rows
+                if (kMode) wait_bar(&sm.khat_ready[nbq & 1], (nbq >> 1) & 1, cx);
                 tc_fence_after();
-                // inter-chunk read (with decay into its own accumulator: it
-                // is scaled per row by g^(i+1) in the output epilogue)
+                // inter-chunk read phi(Q) [S | z] (Qhat with weights)
                 for (int ks = 0; ks < DK / 16; ++ks)
-                    mma_ss(tmem + (kMode ? TM_OQS : tob),
-                           sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
+                    mma_ss(tmem + tob, sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
                            sdesc_sw128(sb + ks * 2048, L::SBLK, 1024), idQS,
                            ks > 0 ? 1u : 0u);
-                // state update phi(K)^T [V | 1]; with decay Khat^T [V | 1],
-                // Khat_t = g^(n-1-t) phi(k_t), the K rows being rescaled in
-                // place once P(j) has read them
-                if (kMode) {
-                    wait_bar(&sm.khat_ready, nbq & 1, cx);
-                    tc_fence_after();
-                }
+                // state update phi(K)^T [V | 1] (Khat with weights)
                 if (su) {
                     for (int ks = 0; ks < C / 16; ++ks)
                         mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
@@ -375,8 +373,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 // intra-chunk: P~ [V | 1] (P~ read from TMEM)
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_ts(tmem + tob, tmem + TM_P + 128u * b + ks * 8,
-                           sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV,
-                           (kMode && ks == 0) ? 0u : 1u);
+                           sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idPV, 1u);
                 mma_commit(&sm.o_full[ob]);
                 mma_commit(&sm.pv_done[b]);
             }
@@ -604,6 +601,30 @@ __device__ __forceinline__ void scale_row(uint8_t *tile, int row, int part,
     }
 }
 
+// In place in stage `st`, once P of that chunk (`nb`, the only reader of the
+// unweighted rows) has completed: Khat_t = g^(n-1-t) phi(k_t), the weight of
+// token t in the state after the chunk (rows past N are zero), and
+// Qhat_i = g^(i+1) phi(q_i), the weight of the chunk's start state in row i;
+// with gates prod_{u=t+1..n-1} alpha_u and prod_{u<=i} alpha_u.  The
+// inter-chunk read Qhat [S | z] then accumulates onto P~ [V | 1] directly.
+// All transform threads call.
+template <int DK, int kMode>
+__device__ __forceinline__ void weight_qk(uint8_t *smem, Small &sm, const Ctx &cx,
+                                          float lg, int st, int n, int nb,
+                                          int row, int part, int et) {
+    using L = Layout<DK, kMode>;
+    wait_bar(&sm.pfull[nb & 1], (nb >> 1) & 1, cx);
+    const GateSlot &g = *reinterpret_cast<const GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
+    const float wk = row >= n ? 0.f
+                              : (kMode == 2 ? gate_prod(g, n - 1, row) : gpow(lg, n - 1 - row));
+    const float wq = kMode == 2 ? gate_prod(g, row, -1) : gpow(lg, row + 1);
+    scale_row<DK>(smem + st * L::STAGE + L::OFF_K, row, part, bf2_splat(wk));
+    scale_row<DK>(smem + st * L::STAGE + L::OFF_Q, row, part, bf2_splat(wq));
+    fence_async_shared();
+    named_bar_sync(BAR_T, kTThreads);
+    if (et == 0) mbar_arrive(&sm.khat_ready[nb & 1]);
+}
+
 template <int DK, int kMode>
 __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                           const Ctx &cx, const DecayArgs &dk) {
@@ -659,6 +680,13 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             }
         }
         if (kMode == 2 && !it.hasA) gnext = gate_load(p, it.bh, it.c0, et);
+        // With weights, chunk c's Q and K rows are weighted in place once
+        // P(c) has read them.  With three or more stages that step runs
+        // after the feature map of chunk c + 1, so the feature map overlaps
+        // P(c); with two, chunk c + 1's stage is chunk c - 1's, whose
+        // release would then sit on the path, so it runs at once.
+        constexpr bool kPipe = L::STAGES >= 3;
+        int pst = -1, pn = 0, pnb = 0;
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % L::STAGES;
             const float gcur = gnext;
@@ -674,20 +702,15 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
-            if (kMode) {
-                // Khat_t = g^(n-1-t) phi(k_t) in place (with gates
-                // prod_{u=t+1..n-1} alpha_u), once P(j) (the only reader of
-                // the unweighted rows) has completed; rows past N are zero
-                wait_bar(&sm.pfull[nb & 1], (nb >> 1) & 1, cx);
-                const float w = row >= n ? 0.f
-                                         : (kMode == 2 ? gate_prod(g, n - 1, row)
-                                                       : gpow(lg, n - 1 - row));
-                scale_row<DK>(kt, row, part, bf2_splat(w));
-                fence_async_shared();
-                named_bar_sync(BAR_T, kTThreads);
-                if (et == 0) mbar_arrive(&sm.khat_ready);
+            if (kMode && !kPipe) weight_qk<DK, kMode>(smem, sm, cx, lg, st, n, nb, row, part, et);
+            if (kMode && kPipe) {
+                if (pst >= 0) weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et);
+                pst = st;
+                pn = n;
+                pnb = nb;
             }
         }
+        if (kMode && pst >= 0) weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et);
     }
 }
 
@@ -819,60 +842,38 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
     }
 }
 
-// One chunk's output: (O + g^(i+1) O_inter) / (den + g^(i+1) den_inter),
-// bf16 into the stage's (dead) Q slot, TMA store.  With several stages the
+// One chunk's output: O / den (O alone without the normaliser), bf16 into
+// the stage's (dead) Q slot, TMA store.  With several stages the
 // stage is released when the next store is issued (the store has read it by
 // then), so the store never stalls this warpgroup.
 template <int DK, int kMode>
 __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
                                              const Ctx &cx, uint32_t lb,
-                                             int row, int et, float wq,
+                                             int row, int et,
                                              const Item &it, int c, int j,
                                              int nb, int &pend, bool norm,
                                              const CUtensorMap *to) {
     using L = Layout<DK, kMode>;
     constexpr bool kDefer = !L::OWN_OST && L::STAGES >= 3;
     const int st = j % L::STAGES;
-    const int ob = OBufs<kMode != 0>::n == 2 ? (nb & 1) : 0;
+    const int ob = nb & 1;
     const uint32_t tob = TM_O + 80u * ob;
     uint8_t *stage_o = L::OWN_OST ? smem + L::OFF_OST : smem + st * L::STAGE + L::OFF_Q;
-    if (kMode == 2) {
-        // this row's read of the chunk's start state: prod_{u<=i} alpha_u
-        wait_bar(&sm.xf[st], (j / L::STAGES) & 1, cx);
-        wq = gate_prod(*reinterpret_cast<const GateSlot *>(
-                           smem + st * L::STAGE + L::OFF_GS), row, -1);
-    }
     if (L::OWN_OST) {  // the previous chunk's store must have read the buffer
         if (et == 0) tma_store_wait_read<0>();
         named_bar_sync(BAR_E2, 128);
     }
-    wait_bar(&sm.o_full[ob], (OBufs<kMode != 0>::n == 2 ? (nb >> 1) : nb) & 1, cx);
+    wait_bar(&sm.o_full[ob], (nb >> 1) & 1, cx);
     tc_fence_after();
     uint32_t dreg = tmem_ld1(lb + tob + DV);
-    uint32_t direg = kMode ? tmem_ld1(lb + TM_OQS + DV) : 0u;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t o[32];
         tmem_ld32(lb + tob + 32 * h, o);
-        float inv;
-        if (kMode) {
-            uint32_t oi[32];
-            tmem_ld32(lb + TM_OQS + 32 * h, oi);
-            tmem_wait_ld();
-            reg_fence(o);
-            reg_fence(oi);
-            reg_fence(dreg);
-            reg_fence(direg);
-            inv = norm ? 1.f / fmaf(wq, u2f(direg), u2f(dreg)) : 1.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                o[e] = __float_as_uint(fmaf(wq, u2f(oi[e]), u2f(o[e])));
-        } else {
-            tmem_wait_ld();
-            reg_fence(o);
-            reg_fence(dreg);
-            inv = norm ? 1.f / u2f(dreg) : 1.f;
-        }
+        tmem_wait_ld();
+        reg_fence(o);
+        reg_fence(dreg);
+        const float inv = norm ? 1.f / u2f(dreg) : 1.f;
         if (h == 1) {
             tc_fence_before();
             mbar_arrive(&sm.o_empty[ob]);  // 128 arrivals: O has been read
@@ -1089,7 +1090,6 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             gL = Z == 0 ? exp2f(L2) : 0.f;
             if (et == 0) p.gprod[t] = gL;  // visible with the item's flags
         }
-        const float wq = kMode ? gpow(lg, row + 1) : 1.f;  // mode 2: per chunk
         float *agg = p.agg + (size_t)t * L::STATE;
         float *incl = p.incl + (size_t)t * L::STATE;
         const int n0 = min(C, p.N - it.c0 * C);
@@ -1300,7 +1300,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 named_bar_sync(BAR_E2, 128);
                 if (et == 0) mbar_arrive(&sm.sb_ready);
             }
-            output_chunk<DK, kMode>(smem, sm, cx, lb, row, et, wq, it, c, j, nb,
+            output_chunk<DK, kMode>(smem, sm, cx, lb, row, et, it, c, j, nb,
                                      pend, p.norm != 0, to);
         }
         if (et == 0 && pend >= 0) {  // the item's last store: release its stage
@@ -1374,7 +1374,8 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
         }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.sb_ready, 1);
-        mbar_init(&sm.khat_ready, 1);
+        mbar_init(&sm.khat_ready[0], 1);
+        mbar_init(&sm.khat_ready[1], 1);
         for (int r = 0; r < 2; ++r) {
             mbar_init(&sm.item_full[r], 1);
             mbar_init(&sm.item_empty[r], 4);
