@@ -202,14 +202,17 @@ def timed_steps(fn, K, W, world, flush=None):
 # one ncu capture of a kernel, keyed by kernel and workload, valid only while
 # the kernel's sources hash to the recorded digest (else reported as null).
 KNOWN_TRAFFIC = {
-    # ncu --set full --clock-control none -k regex:<kernel> -s 3 -c 1
-    #     python bench.py --kernel-case B H N D causal|noncausal
-    # (dram__bytes_read.sum + dram__bytes_write.sum of the captured launch;
-    # "sources": kernel_sources_digest(kernel) at capture time)
-    ("causal_kernel<64,false>", "bf16_b4h16_n4096_d64"):
-        {"sources": "033844ebb3e80cff", "bytes": 100818432 + 5384960},
-    ("causal_kernel<128,false>", "bf16_b2h16_n32768_d128"):
-        {"sources": "033844ebb3e80cff", "bytes": 1302684672 + 234194688},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+    #     -k regex:<kernel> -s 3 -c 1 python bench.py --kernel-case B H N D FORM
+    # (FORM causal, decay or noncausal; dram__bytes_read.sum +
+    # dram__bytes_write.sum of the captured launch; "sources":
+    # kernel_sources_digest(kernel) at capture time)
+    ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
+        {"sources": "78d9d80b358cae4a", "bytes": 100798720 + 4932096},
+    ("causal_kernel<128,0>", "bf16_b2h16_n32768_d128"):
+        {"sources": "78d9d80b358cae4a", "bytes": 1312434688 + 234056448},
+    ("causal_kernel<128,1>", "bf16_decay_b4h8_n16384_d128"):
+        {"sources": "78d9d80b358cae4a", "bytes": 409565184 + 131761152},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
         {"sources": "8023d72c789a91db", "bytes": 100728320 + 2898688},
 }
@@ -310,7 +313,7 @@ def run_ours(args):
     byts = forward_bytes(w.B, w.H, w.N, w.d, 2)
     C = 128
     roof = roofline_hbm(byts, ms, peaks["hbm_gbs"],
-                        known_traffic("causal_kernel<64,false>", w))
+                        known_traffic("causal_kernel<64,0>", w))
     tens = tensor_fraction(chunk_flops(w.B, w.H, w.N, w.d, C), ms,
                            peaks["bf16_tflops"])
 
@@ -421,10 +424,10 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
     fwd_path(f"{MAIN} noncausal", MAIN, False, inputs=(q, k, v),
              kernel="noncausal_kernel<64>")
     fwd_path("bf16_b2h16_n32768_d128 causal", "bf16_b2h16_n32768_d128", True,
-             kernel="causal_kernel<128,false>")
+             kernel="causal_kernel<128,0>")
     wd = wl.WORKLOADS["bf16_decay_b4h8_n16384_d128"]
     fwd_path("bf16_decay_b4h8_n16384_d128 causal", wd.name, True,
-             decay=list(wd.decay))
+             decay=list(wd.decay), kernel="causal_kernel<128,1>")
     fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
     fwd_path(f"{MAIN} causal with final state", MAIN, True, inputs=(q, k, v),
              state=True)
