@@ -541,12 +541,32 @@ def run_decode(la, wl, dev, peaks, world, rank, args, decay=None):
     la.check_device_status()
     ms_total = max_over_ranks(e0.elapsed_time(e1), world)
     ms = ms_total / T
+    # the same T steps launched one by one from Python (no graph), from the
+    # same prefilled state: the graph hides the host's per-launch gaps
+    S.zero_()
+    z.zero_()
+    for t in range(P):
+        la.decode_step(S, z, q[t], k[t], v[t], out=o, decay=decay)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for t in range(P, P + T):
+        la.decode_step(S, z, q[t], k[t], v[t], out=o, decay=decay)
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    la.check_device_status()
+    ms_eager = max_over_ranks(e0.elapsed_time(e1), world)
     return {"tokens_per_s": round(B * T * world / (ms_total * 1e-3), 1),
             "ms_per_step": round(ms, 5), "steps": T, "prefill": P,
             "state_bytes": S.numel() * 4,
             "l2": "state (512 MiB) larger than L2; steps back to back",
             "roofline": roofline_hbm(decode_bytes(B * H, d, 2), ms,
-                                     peaks["hbm_gbs"])}
+                                     peaks["hbm_gbs"]),
+            "eager": {"tokens_per_s": round(B * T * world / (ms_eager * 1e-3), 1),
+                      "ms_per_step": round(ms_eager / T, 5),
+                      "launch": "one call per step, no CUDA graph"}}
 
 
 # ------------------------------------------------------------------ oracle
