@@ -598,11 +598,24 @@ def cpu_baseline(w, q, k, v, seconds):
         if dt >= seconds:
             break
     frac = heads / BH
+    # the same oracle on one core: one head, one thread, for about 2 s
+    reps1 = 0
+    t1 = time.perf_counter()
+    while True:
+        oracle.causal(qf[:1], kf[:1], vf[:1], nthreads=1)
+        reps1 += 1
+        dt1 = time.perf_counter() - t1
+        if dt1 >= min(2.0, seconds / 5):
+            break
     return {"value": round(reps * frac * w.B * w.N / dt, 1), "unit": "tokens/s",
             "cores": min(cores, heads), "kind": "oracle",
             "sample": f"causal form, {heads} of {BH} heads of {MAIN} "
                       f"(N={w.N}, d={w.d}), fp64, {reps} passes in {dt:.1f} s; "
-                      f"tokens/s scaled by the head fraction"}
+                      f"tokens/s scaled by the head fraction",
+            "single_core": {"value": round(reps1 * w.B * w.N / BH / dt1, 1),
+                            "unit": "tokens/s",
+                            "sample": f"1 head, 1 thread, {reps1} passes in "
+                                      f"{dt1:.1f} s; scaled by the head fraction"}}
 
 
 def run_reference(args):
