@@ -3,11 +3,12 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = one causal la_forward over one batch of the main workload
-(bf16 q, k, v [B=4, H=16, N=4096, d=64], N(0,1)/sqrt(d), seed = rank).  The
-other paths of the hot path (non-causal form on the same batch, long-context
-causal, causal with per-head decay, fp32 causal, recurrent decode) are timed
-in the same run and reported under "paths".  Rank 0 prints one JSON line.
+One step = one causal la_forward over one batch of the long-context workload
+(bf16 q, k, v [B=2, H=16, N=32768, d=128], N(0,1)/sqrt(d), seed = rank), the
+largest single-GPU forward configuration.  The other paths of the hot path
+(causal and non-causal forms at B=4, H=16, N=4096, d=64; causal with per-head
+decay; fp32 causal; recurrent decode) are timed in the same run and reported
+under "paths".  Rank 0 prints one JSON line.
 
 Timing: each step is captured once in a CUDA graph (so that host-side
 launch work does not sit between the events); W untimed warm-up replays, then
@@ -18,8 +19,15 @@ second.  `e2e` repeats the main step through the C ABI with pinned host
 buffers, the host->device copies of q, k, v and the device->host copy of the
 output inside the timed region.
 
---impl reference times the CPU oracle (the slow double-precision reference
-that the parity tests use) on a bounded sample of the same workload.
+The CPU-baseline leg times the CPU oracle (the slow double-precision
+reference that the parity tests use) on a bounded sample of the main
+workload, and compares the oracle with the output of every timed leg (every
+head of the forward legs; a stated sample of heads, every step replayed, for
+the decode legs): each leg's `max_rel_err` is the largest per-row
+||y - r||_inf / ||r||_inf.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload.
 """
 from __future__ import annotations
 
@@ -39,7 +47,8 @@ if ROOT not in sys.path:
 
 METRIC = ("causal linear-attn tokens/s and % tensor roofline; "
           "decode step % HBM peak")
-MAIN = "bf16_b4h16_n4096_d64"
+MAIN = "bf16_b2h16_n32768_d128"
+MID = "bf16_b4h16_n4096_d64"
 FLUSH_BYTES = 256 << 20
 
 
@@ -272,6 +281,14 @@ def chunk_flops(B, H, N, d, C):
 # ------------------------------------------------------------------ our arm
 
 
+MAIN_KERNEL = "causal_kernel<128,0>"
+MID_KERNEL = "causal_kernel<64,0>"
+
+
+def host_copy(*ts):
+    return tuple(t.detach().cpu() for t in ts)
+
+
 def run_ours(args):
     import torch
     import linear_attention_feature_gb300 as la
@@ -297,8 +314,11 @@ def run_ours(args):
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
     sampler = ClockSampler(gpu_index).start()
+    # host copies of each leg's inputs and output, compared with the oracle
+    # by the CPU-baseline leg (rank 0, one GPU)
+    keep = {} if (rank == 0 and world == 1 and not args.no_cpu) else None
 
-    # ---------------- main: causal forward on the main workload
+    # ---------------- main: causal forward on the long-context workload
     w = wl.WORKLOADS[MAIN]
     q, k, v = (t.to(dev) for t in wl.make_workload_qkv(w, seed=rank))
     out = torch.empty_like(q)
@@ -312,10 +332,12 @@ def run_ours(args):
     value = tokens_step * world / (ms * 1e-3)
     byts = forward_bytes(w.B, w.H, w.N, w.d, 2)
     C = 128
-    roof = roofline_hbm(byts, ms, peaks["hbm_gbs"],
-                        known_traffic("causal_kernel<64,0>", w))
+    roof = roofline_hbm(byts, ms, peaks["hbm_gbs"], known_traffic(MAIN_KERNEL, w))
     tens = tensor_fraction(chunk_flops(w.B, w.H, w.N, w.d, C), ms,
                            peaks["bf16_tflops"])
+    if keep is not None:
+        keep["main"] = {"form": "causal", "qkv": host_copy(q, k, v),
+                        "y": out.cpu()}
 
     # ---------------- e2e through the C ABI with host buffers
     # (la_forward_host: page-locked host q, k, v in, host out back; the
@@ -337,14 +359,18 @@ def run_ours(args):
 
     paths = {}
     if not args.main_only:
-        paths = run_other_paths(args, la, wl, dev, flush, peaks, world, rank,
-                                q, k, v, out)
+        paths = run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep)
     clocks = sampler.stop()
 
-    # ---------------- CPU baseline (oracle) on rank 0
+    # ---------------- CPU baseline (oracle) on rank 0: timing and parity
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(w, q, k, v, args.cpu_seconds)
+    errs = {}
+    if keep is not None:
+        cpu = cpu_baseline(w, keep, args.cpu_seconds)
+        errs = cpu.get("max_rel_err", {})
+        for name, r in paths.items():
+            if name in errs:
+                r["max_rel_err"] = errs[name]
 
     if rank == 0:
         line = {
@@ -359,6 +385,7 @@ def run_ours(args):
                        "inputs": "N(0,1)/sqrt(d), bf16, seed=rank",
                        "l2": "flushed between timed steps (256 MiB write)"},
             "roofline": roof, "tensor": tens, "chunk": C,
+            "max_rel_err": errs.get("main"), "tolerance": wl.TOL["bf16"],
             "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks, "cpu_baseline": cpu, "paths": paths,
             "peaks": peaks,
@@ -369,10 +396,17 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
+def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
     import torch
     res = {}
     Kx, Wx = max(3, args.steps // 2), max(3, args.warmup)
+    mid = {}
+
+    def mid_inputs():
+        if not mid:
+            w = wl.WORKLOADS[MID]
+            mid["qkv"] = tuple(t.to(dev) for t in wl.make_workload_qkv(w, seed=rank))
+        return mid["qkv"]
 
     def fwd_path(name, wkey, causal, decay=None, inputs=None, elem=2, kernel=None,
                  state=False, retention=False, gated=False):
@@ -385,17 +419,21 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
             oo = torch.empty_like(qq)
             fn = lambda: la.forward(qq, kk, vv, causal=causal, decay=decay, out=oo)  # noqa
             extra = 0
+            form = "causal" if causal else "noncausal"
+            ga = Ss = zs = None
             if retention:
                 # identity feature map, no normaliser (retention)
                 fn = lambda: la.forward_variant(qq, kk, vv, causal=causal, decay=decay,  # noqa
                                                 out=oo, feature_map="identity",
                                                 normalise=False)
+                form = "retention"
             if gated:
                 # a data-dependent gate per token, uniform in [0.9, 1)
                 gen = torch.Generator(device="cpu").manual_seed(200 + rank)
                 ga = (0.9 + 0.1 * torch.rand(w.B, w.H, w.N, generator=gen)).to(dev)
                 fn = lambda: la.forward_gated(qq, kk, vv, ga, out=oo)  # noqa
                 extra = 4 * w.B * w.H * w.N  # the gates
+                form = "gated"
             if state:
                 # forward plus the final state (the prefill of a decode)
                 Ss = torch.empty(w.B, w.H, w.d, w.d, device=dev)
@@ -403,6 +441,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
                 fn = lambda: la.forward_causal_state(qq, kk, vv, decay=decay, out=oo,  # noqa
                                                      S=Ss, z=zs)
                 extra = 4 * w.B * w.H * (w.d * w.d + w.d)
+                form = "state"
             replay, _ = capture(fn)
             steps = timed_steps(replay, Kx, Wx, world, flush)
             la.check_device_status()
@@ -418,25 +457,32 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
                                               ms, peaks["bf16_tflops"])
                 r["chunk"] = C
             res[name] = r
+            if keep is not None:
+                keep[name] = {"form": form, "qkv": host_copy(qq, kk, vv),
+                              "y": oo.cpu(), "decay": decay,
+                              "gates": None if ga is None else ga.cpu(),
+                              "S": None if Ss is None else Ss.cpu(),
+                              "z": None if zs is None else zs.cpu()}
         except Exception as e:  # keep the main line; report the failure
             res[name] = {"error": f"{type(e).__name__}: {e}"}
 
-    fwd_path(f"{MAIN} noncausal", MAIN, False, inputs=(q, k, v),
+    fwd_path(f"{MID} causal", MID, True, inputs=mid_inputs(), kernel=MID_KERNEL)
+    fwd_path(f"{MID} noncausal", MID, False, inputs=mid_inputs(),
              kernel="noncausal_kernel<64>")
-    fwd_path("bf16_b2h16_n32768_d128 causal", "bf16_b2h16_n32768_d128", True,
-             kernel="causal_kernel<128,0>")
     wd = wl.WORKLOADS["bf16_decay_b4h8_n16384_d128"]
     fwd_path("bf16_decay_b4h8_n16384_d128 causal", wd.name, True,
              decay=list(wd.decay), kernel="causal_kernel<128,1>")
     fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
-    fwd_path(f"{MAIN} causal with final state", MAIN, True, inputs=(q, k, v),
+    fwd_path(f"{MID} causal with final state", MID, True, inputs=mid_inputs(),
              state=True)
     fwd_path("bf16_decay_b4h8_n16384_d128 retention", wd.name, True,
              decay=list(wd.decay), retention=True)
-    fwd_path(f"{MAIN} gated", MAIN, True, inputs=(q, k, v), gated=True)
+    fwd_path(f"{MID} gated", MID, True, inputs=mid_inputs(), gated=True)
+    mid.clear()
     try:
         res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,
-                                                args)
+                                                args, keep=keep,
+                                                name="decode_b256h32_d128")
     except Exception as e:
         res["decode_b256h32_d128"] = {"error": f"{type(e).__name__}: {e}"}
     try:
@@ -444,18 +490,43 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, q, k, v, out):
         wdec = wl.WORKLOADS["decode_b256h32_d128"]
         res["decode_b256h32_d128 decay"] = run_decode(
             la, wl, dev, peaks, world, rank, args,
-            decay=list(wl.decay_schedule(wdec.H)))
+            decay=list(wl.decay_schedule(wdec.H)), keep=keep,
+            name="decode_b256h32_d128 decay")
     except Exception as e:
         res["decode_b256h32_d128 decay"] = {"error": f"{type(e).__name__}: {e}"}
     try:
         res["decode_b256h32_d128 gated delta rule"] = run_delta_decode(
-            la, wl, dev, peaks, world, rank, args)
+            la, wl, dev, peaks, world, rank, args, keep=keep,
+            name="decode_b256h32_d128 gated delta rule")
     except Exception as e:
         res["decode_b256h32_d128 gated delta rule"] = {"error": f"{type(e).__name__}: {e}"}
     return res
 
 
-def run_delta_decode(la, wl, dev, peaks, world, rank, args):
+def decode_sample(B, H):
+    """Heads (b, b mod H) for every sequence b: every batch entry and every
+    head index appear; the decode legs' parity sample."""
+    return [(b, b % H) for b in range(B)]
+
+
+def keep_decode(keep, name, form, q, k, v, o, S, z=None, decay=None, beta=None,
+                alpha=None):
+    """Host copies of the sampled heads' tokens (all steps), their last output
+    and their final state, for the CPU-baseline leg's replay."""
+    B, H = q.shape[1], q.shape[2]
+    bs = [b for b, _ in decode_sample(B, H)]
+    hs = [h for _, h in decode_sample(B, H)]
+    sel = lambda t: t[:, bs, hs].cpu()  # noqa: E731  [T, heads, d]
+    keep[name] = {"form": form, "q": sel(q), "k": sel(k), "v": sel(v),
+                  "y": o[bs, hs].cpu(), "S": S[bs, hs].cpu(),
+                  "z": None if z is None else z[bs, hs].cpu(),
+                  "decay": None if decay is None else [decay[h] for h in hs],
+                  "beta": None if beta is None else beta[bs, hs].cpu(),
+                  "alpha": None if alpha is None else alpha[bs, hs].cpu(),
+                  "heads": f"{len(bs)} of {B * H} heads, (b, b mod {H}) for every b"}
+
+
+def run_delta_decode(la, wl, dev, peaks, world, rank, args, keep=None, name=None):
     """The decode workload with the Gated DeltaNet step: beta = 0.5, alpha_h
     = 1 - 2^(-5-h) per head, unit-norm keys; 1024 untimed prefill steps,
     then the timed steps as one graph."""
@@ -493,6 +564,9 @@ def run_delta_decode(la, wl, dev, peaks, world, rank, args):
     la.check_device_status()
     ms_total = max_over_ranks(e0.elapsed_time(e1), world)
     ms = ms_total / T
+    if keep is not None:
+        keep_decode(keep, name, "delta", q[:P + T], k[:P + T], v[:P + T], o, S,
+                    beta=beta, alpha=alpha)
     byts = B * H * (2 * d * d * 4 + 4 * d * 2 + 8)  # S read and written, q k v o, beta alpha
     return {"tokens_per_s": round(B * T * world / (ms_total * 1e-3), 1),
             "ms_per_step": round(ms, 5), "steps": T, "prefill": P,
@@ -505,7 +579,8 @@ def decode_bytes(BH, d, elem):
     return BH * (2 * (d * d + d) * 4 + 4 * d * elem)
 
 
-def run_decode(la, wl, dev, peaks, world, rank, args, decay=None):
+def run_decode(la, wl, dev, peaks, world, rank, args, decay=None, keep=None,
+               name=None):
     import torch
     w = wl.WORKLOADS["decode_b256h32_d128"]
     B, H, d = w.B, w.H, w.d
@@ -558,6 +633,9 @@ def run_decode(la, wl, dev, peaks, world, rank, args, decay=None):
     barrier(world)
     la.check_device_status()
     ms_eager = max_over_ranks(e0.elapsed_time(e1), world)
+    if keep is not None:
+        keep_decode(keep, name, "decode", q[:P + T], k[:P + T], v[:P + T], o, S,
+                    z=z, decay=decay)
     return {"tokens_per_s": round(B * T * world / (ms_total * 1e-3), 1),
             "ms_per_step": round(ms, 5), "steps": T, "prefill": P,
             "state_bytes": S.numel() * 4,
@@ -572,12 +650,76 @@ def run_decode(la, wl, dev, peaks, world, rank, args, decay=None):
 # ------------------------------------------------------------------ oracle
 
 
-def cpu_baseline(w, q, k, v, seconds):
+def _max_err_by_heads(wl, y, ref_fn, q, k, v, cores, extra=None):
+    """Max row-relative error of y [..., N, d] against ref_fn on groups of
+    `cores` flattened heads (bounded host memory)."""
+    N, d = q.shape[-2], q.shape[-1]
+    flat = [t.reshape(-1, N, d) for t in (y, q, k, v)]
+    ex = None if extra is None else extra.reshape(flat[1].shape[0], -1)
+    worst = 0.0
+    for h0 in range(0, flat[1].shape[0], cores):
+        sl = slice(h0, h0 + cores)
+        ref = ref_fn(flat[1][sl], flat[2][sl], flat[3][sl],
+                     None if ex is None else ex[sl], h0)
+        worst = max(worst, wl.max_row_rel_err(flat[0][sl], ref))
+    return worst
+
+
+def leg_error(oracle, wl, leg, cores):
+    """Max row-relative error of one kept leg against the oracle."""
+    import numpy as np
+    form = leg["form"]
+    if form in ("decode", "delta"):
+        qs, ks, vs = leg["q"], leg["k"], leg["v"]
+        nh, d = qs.shape[1], qs.shape[2]
+        So = np.zeros((nh, d, d))
+        zo = np.zeros((nh, d))
+        for t in range(qs.shape[0]):
+            if form == "decode":
+                r = oracle.decode_step(So, zo, qs[t], ks[t], vs[t], leg["decay"],
+                                       nthreads=cores)
+            else:
+                r = oracle.delta_step(So, qs[t], ks[t], vs[t], leg["beta"].numpy(),
+                                      leg["alpha"].numpy())
+        err = wl.max_row_rel_err(leg["y"], r)
+        s_err = float(np.abs(leg["S"].double().numpy() - So).max() / np.abs(So).max())
+        return err, {"state_rel_err": s_err, "sample": leg["heads"]}
+    q, k, v = leg["qkv"]
+    H = q.shape[1]
+    BH = q.shape[0] * H
+    g = None
+    if leg.get("decay") is not None:
+        g = np.array([leg["decay"][i % H] for i in range(BH)])
+
+    def ref(qs, ks, vs, ex, h0):
+        gs = None if g is None else g[h0:h0 + qs.shape[0]]
+        if form == "noncausal":
+            return oracle.noncausal(qs, ks, vs, nthreads=cores)
+        if form == "retention":
+            return oracle.causal(qs, ks, vs, gs, fmap=oracle.FMAP_IDENTITY,
+                                 normalise=False, nthreads=cores)
+        if form == "gated":
+            return oracle.causal_gated(qs, ks, vs, ex, nthreads=cores)
+        return oracle.causal(qs, ks, vs, gs, nthreads=cores)
+
+    err = _max_err_by_heads(wl, leg["y"], ref, q, k, v, cores,
+                            extra=leg.get("gates"))
+    info = {}
+    if form == "state":
+        So, zo = oracle.causal_state(k, v, None if g is None else g)
+        info["state_rel_err"] = float(
+            np.abs(leg["S"].double().numpy() - So).max() / np.abs(So).max())
+    return err, info
+
+
+def cpu_baseline(w, keep, seconds):
     """Time the oracle (as it stands) on a bounded sample of the main
-    workload: whole heads of the causal form, on all host cores."""
+    workload: whole heads of the causal form, on all host cores.  Then
+    compare the oracle with every kept leg's output (`max_rel_err`)."""
     import oracle
+    from linear_attention_feature_gb300 import workloads as wl
     cores = os.cpu_count() or 1
-    qs, ks, vs = (t.cpu() for t in (q, k, v))
+    qs, ks, vs = keep["main"]["qkv"]
     BH = w.B * w.H
     # calibrate on one head, then take as many heads as fit the budget
     t0 = time.perf_counter()
@@ -607,6 +749,18 @@ def cpu_baseline(w, q, k, v, seconds):
         dt1 = time.perf_counter() - t1
         if dt1 >= min(2.0, seconds / 5):
             break
+    # parity of every timed leg against the oracle
+    errs, info = {}, {}
+    t2 = time.perf_counter()
+    for name, leg in keep.items():
+        try:
+            e, extra = leg_error(oracle, wl, leg, cores)
+            errs[name] = round(e, 6)
+            if extra:
+                info[name] = extra
+        except Exception as ex:  # report, do not lose the line
+            info[name] = {"error": f"{type(ex).__name__}: {ex}"}
+    dt2 = time.perf_counter() - t2
     return {"value": round(reps * frac * w.B * w.N / dt, 1), "unit": "tokens/s",
             "cores": min(cores, heads), "kind": "oracle",
             "sample": f"causal form, {heads} of {BH} heads of {MAIN} "
@@ -615,7 +769,12 @@ def cpu_baseline(w, q, k, v, seconds):
             "single_core": {"value": round(reps1 * w.B * w.N / BH / dt1, 1),
                             "unit": "tokens/s",
                             "sample": f"1 head, 1 thread, {reps1} passes in "
-                                      f"{dt1:.1f} s; scaled by the head fraction"}}
+                                      f"{dt1:.1f} s; scaled by the head fraction"},
+            "max_rel_err": errs, "parity_detail": info,
+            "parity_seconds": round(dt2, 1),
+            "parity": "oracle vs each timed leg's output: every head of the "
+                      "forward legs; decode legs: the sampled heads replayed "
+                      "over every step, last output and final state"}
 
 
 def run_reference(args):

@@ -305,8 +305,9 @@ la_status la_decode_step_delta(float *S, const void *q, const void *k,
  * but its workspace lives in a static device array of
  * LA_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads the library's
  * causal kernels keeps until the process exits.  The call makes no
- * cudaMalloc/cudaFree or other allocating call; it clears the part of the
- * scratch that must start at zero with cudaMemsetAsync on `stream`.
+ * cudaMalloc/cudaFree or other allocating call.  It enqueues two kernels on
+ * `stream`: a small zeroing kernel that clears the part of the scratch that
+ * must start at zero (ticket counter and segment flags), then the forward.
  *   - Sequence segments are lengthened until the workspace fits the
  *     scratch; if it cannot fit even with one segment per head the call
  *     returns LA_ERR_UNSUPPORTED ("needs more workspace than ...") and

@@ -71,3 +71,42 @@ def test_peaks_come_from_the_measured_file_or_the_stated_fallback():
     assert p["hbm_gbs"] > 1000 and p["bf16_tflops"] > 100
     if p["source"] == "fallback":
         assert (p["hbm_gbs"], p["bf16_tflops"]) == (6800.0, 1900.0)
+
+
+def test_bench_parity_reads_every_head_of_a_forward_leg():
+    # the CPU-baseline leg's comparison: an exact output scores ~0, and a
+    # planted error in the LAST head (the oracle side is exact) is found
+    torch = pytest.importorskip("torch")
+    import oracle
+    from linear_attention_feature_gb300 import workloads as wl
+    q, k, v = wl.make_qkv(2, 3, 40, 8, "f32", 1.0, seed=1)
+    y = torch.from_numpy(oracle.causal(q, k, v)).float()
+    leg = {"form": "causal", "qkv": (q, k, v), "y": y.clone(), "decay": None}
+    e, _ = bench.leg_error(oracle, wl, leg, 2)
+    assert e < 1e-6
+    y2 = y.clone()
+    y2[1, 2, 17, 3] += 1.0
+    leg["y"] = y2
+    e2, _ = bench.leg_error(oracle, wl, leg, 2)
+    assert e2 > 0.1
+
+
+def test_bench_parity_replays_decode_legs():
+    torch = pytest.importorskip("torch")
+    import numpy as np
+    import oracle
+    from linear_attention_feature_gb300 import workloads as wl
+    T, nh, d = 5, 3, 8
+    q, k, v = wl.make_decode_tokens(1, nh, d, T, "f32", 1.0, seed=2)
+    q, k, v = q[:, 0], k[:, 0], v[:, 0]      # [T, heads, d]
+    S, z = np.zeros((nh, d, d)), np.zeros((nh, d))
+    for t in range(T):
+        y = oracle.decode_step(S, z, q[t], k[t], v[t])
+    leg = {"form": "decode", "q": q, "k": k, "v": v,
+           "y": torch.from_numpy(y).float(), "S": torch.from_numpy(S).float(),
+           "z": torch.from_numpy(z).float(), "decay": None, "heads": "all"}
+    e, info = bench.leg_error(oracle, wl, leg, 2)
+    assert e < 1e-6 and info["state_rel_err"] < 1e-6
+    leg["S"] = leg["S"] * 1.01
+    _, info = bench.leg_error(oracle, wl, leg, 2)
+    assert info["state_rel_err"] > 5e-3

@@ -59,6 +59,23 @@ def test_noalloc_matches_la_forward_two_calls_in_a_row(lib, d, decay):
         assert wl.max_row_rel_err(out.cpu(), ref.cpu()) <= TOL
 
 
+@pytest.mark.parametrize("d, decay", [(64, None), (128, [0.96875, 0.75, 1.0])])
+def test_noalloc_matches_the_oracle(lib, d, decay):
+    # parity of the allocation-free call on its own, independent of
+    # la_forward: the double-precision oracle, every head, twice in a row
+    import oracle
+    B, H, N = 1, 3, 900
+    q, k, v = wl.make_qkv(B, H, N, d, "bf16", seed=13)
+    ref = oracle.causal(q, k, v, decay, nthreads=8)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    for _ in range(2):
+        out = torch.empty_like(qd)
+        assert noalloc(lib, qd, kd, vd, out, decay) == 0, \
+            lib.la_last_error().decode()
+        la.check_device_status()
+        assert wl.max_row_rel_err(out.cpu(), ref) <= TOL
+
+
 def test_noalloc_long_sequence_fits_by_longer_segments(lib):
     # 64 heads of d=128 over 16 chunks: the default segmentation would need
     # more than the static scratch, so segments are lengthened to fit.
