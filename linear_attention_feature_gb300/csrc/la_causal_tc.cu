@@ -540,67 +540,6 @@ __device__ __forceinline__ void gate_totals(float &L2, int &Z, const Params &p,
 
 // ---------------------------------------------------------------- transform
 
-// phi (bf16 pairs) over this thread's share of one row of a [128][DK]
-// swizzled tile, in place (identity when `phi` is false); rows with `zero`
-// set become 0.
-template <int DK>
-__device__ __forceinline__ void transform_row(uint8_t *tile, int row, int part,
-                                              bool zero, bool phi) {
-    constexpr int NCH = DK / 16;  // 16-byte chunks per thread (half a row)
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-        const int cc = part * NCH + i;
-        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
-        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
-        uint4 y = x;
-        if (phi) {
-            y.x = phi2(x.x);
-            y.y = phi2(x.y);
-            y.z = phi2(x.z);
-            y.w = phi2(x.w);
-        }
-        if (zero) y = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(tile + off) = y;
-    }
-}
-
-// Khat = w phi(K) in place (phase A weights relative to the segment end);
-// w K with the identity feature map.
-template <int DK>
-__device__ __forceinline__ void transform_row_scaled(uint8_t *tile, int row,
-                                                     int part, uint32_t w2,
-                                                     bool phi) {
-    constexpr int NCH = DK / 16;
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-        const int cc = part * NCH + i;
-        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
-        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
-        uint4 y;
-        y.x = bf2_mul(phi ? phi2(x.x) : x.x, w2);
-        y.y = bf2_mul(phi ? phi2(x.y) : x.y, w2);
-        y.z = bf2_mul(phi ? phi2(x.z) : x.z, w2);
-        y.w = bf2_mul(phi ? phi2(x.w) : x.w, w2);
-        *reinterpret_cast<uint4 *>(tile + off) = y;
-    }
-}
-
-// Row `row` of a [128][DK] swizzled bf16 tile times w (this thread's half).
-template <int DK>
-__device__ __forceinline__ void scale_row(uint8_t *tile, int row, int part,
-                                          uint32_t w2) {
-    constexpr int NCH = DK / 16;
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-        const int cc = part * NCH + i;
-        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
-        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
-        *reinterpret_cast<uint4 *>(tile + off) =
-            make_uint4(bf2_mul(x.x, w2), bf2_mul(x.y, w2), bf2_mul(x.z, w2),
-                       bf2_mul(x.w, w2));
-    }
-}
-
 // In place in stage `st`, once P of that chunk (`nb`, the only reader of the
 // unweighted rows) has completed: Khat_t = g^(n-1-t) phi(k_t), the weight of
 // token t in the state after the chunk (rows past N are zero), and
@@ -1444,8 +1383,6 @@ constexpr size_t smem_bytes() {
     return (size_t)Layout<DK, kMode>::OFF_SMALL + sizeof(Small) + 1024;
 }
 
-static_assert(smem_bytes<128, true>() <= 232448, "shared memory budget");
-static_assert(smem_bytes<128, false>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<64, true>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<64, false>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<128, 2>() <= 232448, "shared memory budget");
@@ -1568,17 +1505,17 @@ TcResult launch_causal_tc(const void *q, const void *k, const void *v,
         return sh.d == 128
                    ? launch_causal_t<128, 2>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, gates, stream)
                    : launch_causal_t<64, 2>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, gates, stream);
+    // d = 128 without gates: one CTA per (head, segment) over all 128 value
+    // columns (la_causal_wide.cu)
     if (sh.d == 128)
-        return dk.has ? launch_causal_t<128, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream)
-                      : launch_causal_t<128, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream);
+        return launch_causal_wide(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes,
+                                  S_out, z_out, stream);
     return dk.has ? launch_causal_t<64, true>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream)
                   : launch_causal_t<64, false>(q, k, v, out, sh, dk, seg_chunks, status, ws, ws_bytes, S_out, z_out, nullptr, stream);
 }
 
 size_t causal_tc_workspace_bytes(const FwdShape &sh, bool decay, int seg_chunks, int sms) {
-    if (sh.d == 128)
-        return decay ? plan_causal<128, true>(sh, seg_chunks, sms).total
-                     : plan_causal<128, false>(sh, seg_chunks, sms).total;
+    if (sh.d == 128) return causal_wide_workspace_bytes(sh, seg_chunks, sms);
     return decay ? plan_causal<64, true>(sh, seg_chunks, sms).total
                  : plan_causal<64, false>(sh, seg_chunks, sms).total;
 }
@@ -1765,10 +1702,14 @@ la_status la_forward_causal_noalloc(const void *q, const void *k,
     }
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     TcResult r;
-    if (d == 128)
-        r = dk.has ? launch_causal_noalloc_t<128, true>(q, k, v, out, sh, dk, status, s)
-                   : launch_causal_noalloc_t<128, false>(q, k, v, out, sh, dk, status, s);
-    else
+    if (d == 128) {
+        char *scratch = nullptr;
+        const cudaError_t e = noalloc_scratch(&scratch);
+        r = e != cudaSuccess
+                ? TcResult{LA_ERR_CUDA, e, "la_forward_causal_noalloc: scratch address"}
+                : launch_causal_wide_fixed(q, k, v, out, sh, dk, status, scratch,
+                                           (size_t)LA_NOALLOC_SCRATCH_BYTES, s);
+    } else
         r = dk.has ? launch_causal_noalloc_t<64, true>(q, k, v, out, sh, dk, status, s)
                    : launch_causal_noalloc_t<64, false>(q, k, v, out, sh, dk, status, s);
     if (r.status != LA_OK) {

@@ -58,4 +58,21 @@ TcResult launch_causal_tc(const void *q, const void *k, const void *v,
                           cudaStream_t stream);
 size_t causal_tc_workspace_bytes(const FwdShape &sh, bool decay, int seg_chunks, int sms);
 
+// d = 128 causal kernel, one CTA per (head, segment) over all value columns
+// (la_causal_wide.cu); no gates.  launch_causal_wide takes a caller's
+// workspace or allocates it stream-ordered; launch_causal_wide_fixed runs in
+// a fixed device scratch of `cap` bytes (lengthening segments to fit) and
+// allocates nothing.
+TcResult launch_causal_wide(const void *q, const void *k, const void *v, void *out,
+                            const FwdShape &sh, const DecayArgs &dk, int seg_chunks,
+                            int *status, void *ws, size_t ws_bytes, float *S_out,
+                            float *z_out, cudaStream_t stream);
+TcResult launch_causal_wide_fixed(const void *q, const void *k, const void *v,
+                                  void *out, const FwdShape &sh, const DecayArgs &dk,
+                                  int *status, char *scratch, size_t cap,
+                                  cudaStream_t stream);
+size_t causal_wide_workspace_bytes(const FwdShape &sh, int seg_chunks, int sms);
+// Automatic segment length (chunks) of the d = 128 kernel.
+int wide_segment_chunks(long long heads, int nchunks, int sms);
+
 }  // namespace la

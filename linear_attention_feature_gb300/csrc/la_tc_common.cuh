@@ -102,5 +102,68 @@ __device__ __forceinline__ uint32_t kmajor_off(int ks, uint32_t atom_bytes) {
     return (uint32_t)(ks >> 2) * atom_bytes + (uint32_t)(ks & 3) * 32u;
 }
 
+// ---------------------------------------------------------------- row transforms
+
+// phi (bf16 pairs) over this thread's share of one row of a [128][DK]
+// swizzled tile, in place (identity when `phi` is false); rows with `zero`
+// set become 0.
+template <int DK>
+__device__ __forceinline__ void transform_row(uint8_t *tile, int row, int part,
+                                              bool zero, bool phi) {
+    constexpr int NCH = DK / 16;  // 16-byte chunks per thread (half a row)
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int cc = part * NCH + i;
+        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
+        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
+        uint4 y = x;
+        if (phi) {
+            y.x = phi2(x.x);
+            y.y = phi2(x.y);
+            y.z = phi2(x.z);
+            y.w = phi2(x.w);
+        }
+        if (zero) y = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(tile + off) = y;
+    }
+}
+
+// Khat = w phi(K) in place (phase A weights relative to the segment end);
+// w K with the identity feature map.
+template <int DK>
+__device__ __forceinline__ void transform_row_scaled(uint8_t *tile, int row,
+                                                     int part, uint32_t w2,
+                                                     bool phi) {
+    constexpr int NCH = DK / 16;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int cc = part * NCH + i;
+        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
+        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
+        uint4 y;
+        y.x = bf2_mul(phi ? phi2(x.x) : x.x, w2);
+        y.y = bf2_mul(phi ? phi2(x.y) : x.y, w2);
+        y.z = bf2_mul(phi ? phi2(x.z) : x.z, w2);
+        y.w = bf2_mul(phi ? phi2(x.w) : x.w, w2);
+        *reinterpret_cast<uint4 *>(tile + off) = y;
+    }
+}
+
+// Row `row` of a [128][DK] swizzled bf16 tile times w (this thread's half).
+template <int DK>
+__device__ __forceinline__ void scale_row(uint8_t *tile, int row, int part,
+                                          uint32_t w2) {
+    constexpr int NCH = DK / 16;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int cc = part * NCH + i;
+        const uint32_t off = (cc >> 3) * 16384 + sw128_offset(row, (cc & 7) * 8);
+        const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
+        *reinterpret_cast<uint4 *>(tile + off) =
+            make_uint4(bf2_mul(x.x, w2), bf2_mul(x.y, w2), bf2_mul(x.z, w2),
+                       bf2_mul(x.w, w2));
+    }
+}
+
 }  // namespace tcc
 }  // namespace la

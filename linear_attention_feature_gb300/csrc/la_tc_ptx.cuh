@@ -97,6 +97,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap,
         : "memory");
 }
 
+// L2 prefetch of the tile a 3-D tiled load with the same coordinates would
+// read (no shared-memory destination, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1,
+                                                int c2, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, "
+        "%2, %3}], %4;" ::"l"(tmap),
+        "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
 // 3-D tiled store shared -> global (bulk group).
 __device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src,
                                              int c0, int c1, int c2) {
@@ -147,6 +158,27 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;"
                  : "=l"(p));
     return p;
+}
+
+// ------------------------------------------------------------------ 256-bit global access
+
+// 32 bytes from global memory through L2 (not L1); `p` 32-byte aligned.
+__device__ __forceinline__ void ld_cg_v8(const float *p, float (&r)[8]) {
+    asm volatile(
+        "ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]),
+          "=f"(r[5]), "=f"(r[6]), "=f"(r[7])
+        : "l"(p)
+        : "memory");
+}
+
+// 32 bytes to global memory; `p` 32-byte aligned.
+__device__ __forceinline__ void st_v8(void *p, const uint32_t (&r)[8]) {
+    asm volatile(
+        "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+        "r"(r[6]), "r"(r[7])
+        : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
