@@ -168,7 +168,7 @@ __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
                                         int bar_id, int nthreads, bool leader) {
     const int r = tl & 1;
     wait_bar(&sm.item_full[r], (tl >> 1) & 1, cx);
-    const int t = (*cx.abort) ? -1 : ((volatile int *)sm.ring)[r];
+    const int t = ((volatile int *)sm.ring)[r];  // -1 once a wait gave up
     if (bar_id) named_bar_sync(bar_id, nthreads);
     if (leader) mbar_arrive(&sm.item_empty[r]);
     ++tl;

@@ -71,7 +71,7 @@ constexpr int OFF_SB = STAGES * STAGE;
 constexpr int SB = 2 * BLK;
 constexpr int OFF_SMALL = OFF_SB + SB;
 constexpr int STATE = D * D + D;  // a published state: S rows (a-major), then z
-constexpr int kPrefetch = 2;      // L2 prefetch distance in jobs
+constexpr int kPrefetch = 3;      // L2 prefetch distance in jobs
 // TMEM columns: P in two buffers, O, S
 constexpr uint32_t TM_P = 0, TM_O = 256, TM_S = 384, TM_COLS = 512;
 
@@ -93,7 +93,11 @@ struct Small {
     float z[D];         // running z (state warps)
     float zpark[D];     // z of the predecessor's prefix, fetched early
     float gtab[32];     // g^0 .. g^31 of the current head (score warps)
-    uint64_t full[STAGES], empty[STAGES], xf[STAGES];
+    // per stage: Q and K (full_qk / empty_qk) and V (full_v / empty_v) are
+    // loaded and released separately (Q and K die at Qhat S, V at Pt V)
+    uint64_t full_qk[STAGES], empty_qk[STAGES], full_v[STAGES], empty_v[STAGES];
+    uint64_t xf[STAGES];
+    uint64_t ost_free[2];  // the output epilogue's staging in P buffer b is read
     uint64_t pfull[2], pt_ready[2], pv_done[2];
     uint64_t o_full, o_empty, s_full, sb_ready, lb_done;
     uint64_t khat_ready[2], dint_full[2], dint_empty[2];
@@ -128,7 +132,7 @@ __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
                                         int bar_id, int nthreads, bool leader) {
     const int r = tl & 1;
     wait_bar(&sm.item_full[r], (tl >> 1) & 1, cx);
-    const int t = (*cx.abort) ? -1 : ((volatile int *)sm.ring)[r];
+    const int t = ((volatile int *)sm.ring)[r];  // -1 once a wait gave up
     if (bar_id) named_bar_sync(bar_id, nthreads);
     if (leader) mbar_arrive(&sm.item_empty[r]);
     ++tl;
@@ -137,13 +141,6 @@ __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
-
-// Lane 0's view of an mbarrier phase, shared by the warp (warp-uniform).
-__device__ __forceinline__ bool warp_ready(uint64_t *bar, uint32_t parity) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_try_wait(bar, parity) ? 1 : 0;
-    return __shfl_sync(~0u, ok, 0) != 0;
-}
 
 // A wait that ignores the abort flag (bounded by the same deadline): used
 // at exit, so that no TMA load or MMA is still in flight when the CTA's
@@ -163,7 +160,7 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
                          const CUtensorMap *tv) {
     const uint64_t keep = policy_evict_last(), stream = policy_evict_first(),
                    normal = policy_evict_normal();
-    int j = 0, tl = 0;
+    int j = 0, jqk = 0, tl = 0;
     for (;;) {
         int t = atomicAdd(p.ctrl, 1);
         if (t >= p.items || *cx.abort) t = -1;
@@ -191,25 +188,31 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
             const int pass = y < nA ? 0 : 1;
             const int c = it.c0 + (pass == 0 ? y : y - nA);
             const int st = j % STAGES;
-            if (!wait_bar(&sm.empty[st], ((j / STAGES) & 1) ^ 1, cx)) break;
+            const uint32_t par = ((j / STAGES) & 1) ^ 1;
             uint8_t *base = smem + st * STAGE;
-            mbar_arrive_expect_tx(&sm.full[st], pass == 0 ? 2 * TILE : 3 * TILE);
-            const uint64_t pol = pass == 0 ? keep : stream;
+            if (!wait_bar(&sm.empty_qk[st], par, cx)) break;
+            mbar_arrive_expect_tx(&sm.full_qk[st], pass == 0 ? TILE : 2 * TILE);
             for (int kb = 0; kb < 2; ++kb) {
                 if (pass == 1)
-                    tma_load_3d(base + OFF_Q + kb * BLK, tq, &sm.full[st], 64 * kb,
+                    tma_load_3d(base + OFF_Q + kb * BLK, tq, &sm.full_qk[st], 64 * kb,
                                 c * C, it.bh, stream);
-                tma_load_3d(base + OFF_K + kb * BLK, tk, &sm.full[st], 64 * kb, c * C,
-                            it.bh, pol);
-                tma_load_3d(base + OFF_V + kb * BLK, tv, &sm.full[st], 64 * kb, c * C,
-                            it.bh, pol);
+                tma_load_3d(base + OFF_K + kb * BLK, tk, &sm.full_qk[st], 64 * kb, c * C,
+                            it.bh, pass == 0 ? keep : stream);
             }
+            ++jqk;
+            if (!wait_bar(&sm.empty_v[st], par, cx)) break;
+            mbar_arrive_expect_tx(&sm.full_v[st], TILE);
+            for (int kb = 0; kb < 2; ++kb)
+                tma_load_3d(base + OFF_V + kb * BLK, tv, &sm.full_v[st], 64 * kb, c * C,
+                            it.bh, pass == 0 ? keep : stream);
             ++j;
         }
     }
-    // the last load of each stage has landed before the CTA may exit
+    // the last loads of each stage have landed before the CTA may exit
+    for (int x = jqk - STAGES; x < jqk; ++x)
+        if (x >= 0) drain_wait(&sm.full_qk[x % STAGES], (x / STAGES) & 1, cx);
     for (int x = j - STAGES; x < j; ++x)
-        if (x >= 0) drain_wait(&sm.full[x % STAGES], (x / STAGES) & 1, cx);
+        if (x >= 0) drain_wait(&sm.full_v[x % STAGES], (x / STAGES) & 1, cx);
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -222,6 +225,7 @@ __device__ __forceinline__ void issue_p(uint8_t *smem, Small &sm, const Ctx &cx,
     const int st = jj % STAGES, b = nbq & 1;
     wait_bar(&sm.xf[st], (jj / STAGES) & 1, cx);
     wait_bar(&sm.pv_done[b], ((nbq >> 1) & 1) ^ 1, cx);
+    wait_bar(&sm.ost_free[b], ((nbq >> 1) & 1) ^ 1, cx);
     tc_fence_after();
     const uint32_t qb = smem_u32(smem + st * STAGE + OFF_Q);
     const uint32_t kb = smem_u32(smem + st * STAGE + OFF_K);
@@ -242,7 +246,8 @@ __device__ __forceinline__ void try_issue_next_p(uint8_t *smem, Small &sm,
     if (p_next != qi + 1 || qi + 1 >= nB) return;
     const int st1 = (jj + 1) % STAGES, b1 = (nbq + 1) & 1;
     if (mbar_try_wait(&sm.xf[st1], ((jj + 1) / STAGES) & 1) &&
-        mbar_try_wait(&sm.pv_done[b1], (((nbq + 1) >> 1) & 1) ^ 1)) {
+        mbar_try_wait(&sm.pv_done[b1], (((nbq + 1) >> 1) & 1) ^ 1) &&
+        mbar_try_wait(&sm.ost_free[b1], (((nbq + 1) >> 1) & 1) ^ 1)) {
         issue_p(smem, sm, cx, tmem, jj + 1, nbq + 1);
         ++p_next;
     }
@@ -268,6 +273,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             for (int c = it.c0; c < it.c1; ++c, ++j) {
                 const int st = j % STAGES;
                 wait_bar(&sm.xf[st], (j / STAGES) & 1, cx);
+                wait_bar(&sm.full_v[st], (j / STAGES) & 1, cx);
                 tc_fence_after();
                 const uint32_t kb = smem_u32(smem + st * STAGE + OFF_K);
                 const uint32_t vb = smem_u32(smem + st * STAGE + OFF_V);
@@ -277,7 +283,8 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                            sdesc_sw128(vb + ks * 2048, BLK, 1024), idSU,
                            (c > it.c0 || ks > 0) ? 1u : 0u);
                 if (c == it.c1 - 1) mma_commit(&sm.s_full);
-                mma_commit(&sm.empty[st]);
+                mma_commit(&sm.empty_qk[st]);
+                mma_commit(&sm.empty_v[st]);
             }
         }
         // phase B.  The state after the item's last chunk is only needed as
@@ -301,6 +308,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             wait_bar(&sm.sb_ready, nsb & 1, cx);
             ++nsb;
             if (kMode) wait_bar(&sm.khat_ready[nbq & 1], (nbq >> 1) & 1, cx);
+            wait_bar(&sm.full_v[st], (jj / STAGES) & 1, cx);
             tc_fence_after();
             if (su) {
 #pragma unroll
@@ -317,9 +325,13 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_ss(tmem + TM_O, sdesc_sw128(qb + kmajor_off(ks, BLK), 16, 1024),
                        sdesc_sw128(sb + ks * 2048, BLK, 1024), idQS, ks > 0 ? 1u : 0u);
-            // the state warps may now read S and rewrite its bf16 copy
+            // the state warps may now read S and rewrite its bf16 copy; the
+            // stage's Q and K are no longer read by the tensor cores
             mma_commit(&sm.s_full);
-            try_issue_next_p(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
+            mma_commit(&sm.empty_qk[st]);
+            // P of the next chunk ahead of Pt V only if Pt is not ready yet
+            if (!mbar_try_wait(&sm.pt_ready[b], (nbq >> 1) & 1))
+                try_issue_next_p(smem, sm, cx, tmem, jj, nbq, qi, nB, p_next);
             wait_bar(&sm.pt_ready[b], (nbq >> 1) & 1, cx);
             tc_fence_after();
 #pragma unroll
@@ -328,7 +340,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                        sdesc_sw128(vb + ks * 2048, BLK, 1024), idPV, 1u);
             mma_commit(&sm.o_full);
             mma_commit(&sm.pv_done[b]);
-            mma_commit(&sm.empty[st]);
+            mma_commit(&sm.empty_v[st]);
         }
         if (final_state) {
             // S's columns are reused by the next item: wait until the state
@@ -362,7 +374,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             const int seg_end = min(it.c1 * C, p.N);
             for (int c = it.c0; c < it.c1; ++c, ++j) {
                 const int st = j % STAGES;
-                wait_bar(&sm.full[st], (j / STAGES) & 1, cx);
+                wait_bar(&sm.full_qk[st], (j / STAGES) & 1, cx);
                 uint8_t *kt = smem + st * STAGE + OFF_K;
                 const int tok = c * C + row;
                 if (kMode || tok >= p.N) {
@@ -378,7 +390,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         }
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % STAGES;
-            wait_bar(&sm.full[st], (j / STAGES) & 1, cx);
+            wait_bar(&sm.full_qk[st], (j / STAGES) & 1, cx);
             uint8_t *qt = smem + st * STAGE + OFF_Q;
             uint8_t *kt = smem + st * STAGE + OFF_K;
             const int n = min(C, p.N - c * C);
@@ -471,8 +483,11 @@ __device__ __forceinline__ float score_chunk(Small &sm, const Ctx &cx, uint32_t 
     return den;
 }
 
-// One chunk's output: O / den (O alone without the normaliser) in bf16,
-// stored from registers to global memory (a thread writes its row).
+// One chunk's output: O / den (O alone without the normaliser) in bf16.  O
+// is converted into the chunk's P buffer (its Pt is dead once Pt V has
+// completed), which frees O for the next chunk's Qhat S at once; the row is
+// then read back and stored to global memory (a thread writes its row).
+// P of the chunk after next waits for this buffer (ost_free).
 __device__ __forceinline__ void output_chunk(Small &sm, const Params &p,
                                              const Ctx &cx, uint32_t lb, int row,
                                              int bh, int c, int nbo, float den_intra,
@@ -485,34 +500,45 @@ __device__ __forceinline__ void output_chunk(Small &sm, const Params &p,
         inv = 1.f / (den_intra + sm.dint[nbo & 1][row]);
         mbar_arrive(&sm.dint_empty[nbo & 1]);  // 128 arrivals
     }
-    const int tok = c * C + row;
-    __nv_bfloat16 *dst = p.out + ((size_t)bh * p.N + tok) * D;
+    const uint32_t tp = lb + TM_P + 128u * (nbo & 1);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         uint32_t o[32];
         tmem_ld32(lb + TM_O + 32 * g, o);
         tmem_wait_ld();
         reg_fence(o);
-        if (g == 3) {
-            tc_fence_before();
-            mbar_arrive(&sm.o_empty);  // 128 arrivals: O has been read
-        }
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
             w[e] = pack_bf16x2(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
+        tmem_st16(tp + 16 * g, w);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&sm.o_empty);  // 128 arrivals: O has been read
+    const int tok = c * C + row;
+    __nv_bfloat16 *dst = p.out + ((size_t)bh * p.N + tok) * D;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
+        tmem_ld32(tp + 32 * h, w);
+        tmem_wait_ld();
+        reg_fence(w);
         if (tok < p.N) {
             if (p.out_v8) {
-                st_v8(dst + 32 * g, *reinterpret_cast<const uint32_t(*)[8]>(w));
-                st_v8(dst + 32 * g + 16, *reinterpret_cast<const uint32_t(*)[8]>(w + 8));
-            } else {
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * g);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
+                    st_v8(dst + 64 * h + 16 * u, *reinterpret_cast<const uint32_t(*)[8]>(w + 8 * u));
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + 64 * h);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
                     d4[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
             }
         }
     }
+    tc_fence_before();
+    mbar_arrive(&sm.ost_free[nbo & 1]);  // 128 arrivals
 }
 
 template <int kMode>
@@ -558,22 +584,16 @@ __device__ void score_output(Small &sm, const Params &p, const Ctx &cx,
         tc_fence_before();
         named_bar_sync(BAR_E1, 128);
         if (et == 0) mbar_arrive(&sm.lb_done);
-        // phase B: the scores of chunk c, then the output of chunk c - 1
-        // (or that output first when its O is complete and P(c) is not)
+        // phase B: the output of chunk c - 1 (its O completes before P of
+        // chunk c, issued after it), then the scores of chunk c
         int pend = -1, pend_c = 0;
         float pend_den = 0.f;
         for (int c = it.c0; c < it.c1; ++c, ++nb) {
-            if (pend >= 0 && !warp_ready(&sm.pfull[nb & 1], (nb >> 1) & 1) &&
-                warp_ready(&sm.o_full, pend & 1)) {
-                output_chunk(sm, p, cx, lb, row, it.bh, pend_c, pend, pend_den, norm);
-                pend = -1;
-            }
-            const float den = score_chunk<kMode>(sm, cx, lb, q, lane, lg, nb, norm);
             if (pend >= 0)
                 output_chunk(sm, p, cx, lb, row, it.bh, pend_c, pend, pend_den, norm);
+            pend_den = score_chunk<kMode>(sm, cx, lb, q, lane, lg, nb, norm);
             pend = nb;
             pend_c = c;
-            pend_den = den;
         }
         if (pend >= 0) output_chunk(sm, p, cx, lb, row, it.bh, pend_c, pend, pend_den, norm);
     }
@@ -674,7 +694,7 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
                 colsum(smem + st * STAGE + OFF_K, pr, hf, s0, s1);
                 zA += hf ? s1 : s0;
                 named_bar_sync(BAR_E2, 128);
-                if (et == 0) mbar_arrive(&sm.empty[st]);
+                if (et == 0) mbar_arrive(&sm.empty_qk[st]);
             }
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
@@ -769,13 +789,13 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
                 named_bar_sync(BAR_E2, 128);  // z read, den terms written
                 if (et == 0) {
                     if (norm) mbar_arrive(&sm.dint_full[nb & 1]);
-                    mbar_arrive(&sm.empty[st]);
+                    mbar_arrive(&sm.empty_qk[st]);
                 }
                 sm.z[fz] = fmaf(kMode ? gpow(lg, n) : 1.f, sm.z[fz], hf ? s1 : s0);
                 named_bar_sync(BAR_E2, 128);
             } else {
                 named_bar_sync(BAR_E2, 128);
-                if (et == 0) mbar_arrive(&sm.empty[st]);
+                if (et == 0) mbar_arrive(&sm.empty_qk[st]);
             }
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
@@ -851,8 +871,10 @@ causal_wide_kernel(const __grid_constant__ CUtensorMap tq,
     const Ctx cx{reinterpret_cast<volatile int *>(p.ctrl + 1), p.status, p.timeout};
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 2);  // MMA commit + state warps
+            mbar_init(&sm.full_qk[s], 1);
+            mbar_init(&sm.full_v[s], 1);
+            mbar_init(&sm.empty_qk[s], 2);  // MMA commit + state warps
+            mbar_init(&sm.empty_v[s], 1);
             mbar_init(&sm.xf[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -862,6 +884,7 @@ causal_wide_kernel(const __grid_constant__ CUtensorMap tq,
             mbar_init(&sm.khat_ready[b], 1);
             mbar_init(&sm.dint_full[b], 1);
             mbar_init(&sm.dint_empty[b], 128);
+            mbar_init(&sm.ost_free[b], 128);
             mbar_init(&sm.item_full[b], 1);
             mbar_init(&sm.item_empty[b], 4);
         }

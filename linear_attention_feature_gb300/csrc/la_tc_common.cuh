@@ -28,17 +28,22 @@ __device__ __forceinline__ void raise_timeout(const Ctx &cx, uint32_t where) {
     *cx.abort = 1;
 }
 
-// Bounded mbarrier wait; passes through (returns false) once aborted.
+// Bounded mbarrier wait; passes through (returns false) once aborted.  The
+// abort flag lives in global memory, so it is read only every 64 polls: a
+// read on every wait would add an L2 round trip to each hand-off between
+// the warp roles.  The deadline starts at the first of those checks.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
                                          const Ctx &cx) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*cx.abort) return false;
-    const long long dl = clock64() + cx.timeout;
+    long long dl = 0;
     for (int n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 63) == 0) {
             if (*cx.abort) return false;
-            if (clock64() > dl) {
+            const long long now = clock64();
+            if (dl == 0) {
+                dl = now + cx.timeout;
+            } else if (now > dl) {
                 raise_timeout(cx, smem_u32(bar));
                 return false;
             }
