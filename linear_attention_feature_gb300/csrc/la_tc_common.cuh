@@ -29,15 +29,20 @@ __device__ __forceinline__ void raise_timeout(const Ctx &cx, uint32_t where) {
 }
 
 // Bounded mbarrier wait; passes through (returns false) once aborted.  The
-// abort flag lives in global memory, so it is read only every 64 polls: a
-// read on every wait would add an L2 round trip to each hand-off between
-// the warp roles.  The deadline starts at the first of those checks.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
-                                         const Ctx &cx) {
-    if (mbar_try_wait(bar, parity)) return true;
+// single-thread roles (TMA producer, MMA issuer) poll with test_wait, which
+// never suspends, so that they react at once; warps of the multi-warp roles
+// suspend between polls for at most `kSuspendNs`, so that waiting warps do
+// not take issue slots from the working ones.  The abort flag lives in
+// global memory, so it is read only every 64 polls; the deadline starts at
+// the first of those checks.
+constexpr uint32_t kSuspendNs = 64;
+
+__device__ __forceinline__ bool wait_bar_poll(uint64_t *bar, uint32_t parity,
+                                              const Ctx &cx, bool spin) {
     long long dl = 0;
     for (int n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait_ns(bar, parity, kSuspendNs))
+            return true;
         if ((n & 63) == 0) {
             if (*cx.abort) return false;
             const long long now = clock64();
@@ -49,6 +54,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
             }
         }
     }
+}
+
+// For warps of the multi-warp roles.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity,
+                                         const Ctx &cx) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return wait_bar_poll(bar, parity, cx, false);
+}
+
+// For the single-thread roles.
+__device__ __forceinline__ bool wait_bar_spin(uint64_t *bar, uint32_t parity,
+                                              const Ctx &cx) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return wait_bar_poll(bar, parity, cx, true);
 }
 
 // Reads a published-state flag (acquire, device scope).
