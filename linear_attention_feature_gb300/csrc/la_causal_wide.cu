@@ -29,13 +29,13 @@
 // CTAs (one per SM) take (head, segment) items from a ticket counter in
 // segment-major order.  A segment with successors first reduces its own
 // K and V to its local state (phase A: Khat^T [V | 1] with weights relative
-// to the segment end); its start state is the inclusive prefix that its
-// predecessor published, and it publishes its own inclusive prefix
-//   incl(s) = g^L incl(s-1) + local(s)
-// before running its chunks (phase B).  Every start state is formed by this
-// one fixed chain, so results do not depend on timing: repeated calls are
-// bit-identical.  The score warps, idle in phase A, fetch the predecessor's
-// prefix while phase A runs when it is already published.
+// to the segment end) and publishes it at once; its start state is the
+// decayed sum of all its predecessors' local states,
+//   start(s) = sum_{m = 1..s} g^(L (m - 1)) local(s - m),
+// added in this fixed order, so results do not depend on timing (repeated
+// calls are bit-identical) and no segment waits on another's look-back.
+// The score warps, idle in phase A, form the sum while phase A runs when the
+// predecessors have already published.
 //
 // Warp roles (576 threads): warp 0 TMA producer (with L2 prefetch ahead),
 // warp 1 MMA issuer and TMEM owner, warps 2-9 feature map (phi(K) in place,
@@ -95,7 +95,7 @@ __host__ __device__ constexpr int v_lbo(int st) { return st ? LBO_V1 : LBO_V0; }
 
 struct Params {
     int BH, N, nchunks, seg_chunks, nseg, items;
-    float *incl;            // [items][STATE] inclusive prefixes
+    float *agg;             // [items][STATE] each segment's local state
     int *flags;             // [items]
     float *S_out, *z_out;   // final state [BH][D][D] / [BH][D], or NULL
     int phi, norm;          // elu(x) + 1 on q, k (else identity); divide by den
@@ -117,7 +117,7 @@ struct Small {
     uint64_t item_full[2], item_empty[2];
     uint64_t fin;
     int ring[2];
-    int lb_early;  // the predecessor's prefix is parked in TMEM O
+    int lb_early;  // the start state is parked in TMEM O (S, and z in column D)
     uint32_t tmem_base;
 };
 
@@ -158,6 +158,61 @@ __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctx &cx) {
     const long long dl = clock64() + cx.timeout;
     while (!mbar_try_wait(bar, parity) && clock64() <= dl) {
+    }
+}
+
+// ---------------------------------------------------------------- look-back
+
+// True once segments 0 .. seg-1 of head bh have all published their local
+// states (one warp; 32 flags per look).  Without `wait` it looks once.
+__device__ __forceinline__ bool preds_published(const Params &p, const Ctx &cx, int bh,
+                                                int seg, int lane, bool wait) {
+    long long dl = 0;
+    for (int base = 0; base < seg; base += 32) {
+        const int s = base + lane;
+        const int *fp = p.flags + item_index(bh, s < seg ? s : 0, p);
+        for (;;) {
+            const int f = s < seg ? load_flag(fp) : FLAG_AGG;
+            if (__all_sync(~0u, f >= FLAG_AGG)) break;
+            if (!wait) return false;
+            if (__any_sync(~0u, *cx.abort != 0)) return false;
+            const long long now = __shfl_sync(~0u, clock64(), 0);
+            if (dl == 0) {
+                dl = now + cx.timeout;
+            } else if (now > dl) {
+                if (lane == 0)
+                    raise_timeout(cx, 0x80000u | ((uint32_t)(reinterpret_cast<uintptr_t>(fp) >> 2) & 0x7FFFFu));
+                return false;
+            }
+            __nanosleep(64);
+        }
+    }
+    return true;
+}
+
+// Row r of the start state, columns [32 g, 32 g + 32) (g < 4) or z[r] in
+// acc[0] (g = 4): sum_{m = 1..seg} gL^(m - 1) local(seg - m), in this order.
+__device__ __forceinline__ void start_sum(const Params &p, int bh, int seg, int r, int g,
+                                          float gL, float (&acc)[32]) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+    float w = 1.f;
+    for (int m = 1; m <= seg; ++m) {
+        const float *src = p.agg + (size_t)item_index(bh, seg - m, p) * STATE;
+        if (g < 4) {
+            const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float4 x = __ldcg(s4 + (8 * g + u) * 128 + r);
+                acc[4 * u] = fmaf(w, x.x, acc[4 * u]);
+                acc[4 * u + 1] = fmaf(w, x.y, acc[4 * u + 1]);
+                acc[4 * u + 2] = fmaf(w, x.z, acc[4 * u + 2]);
+                acc[4 * u + 3] = fmaf(w, x.w, acc[4 * u + 3]);
+            }
+        } else {
+            acc[0] = fmaf(w, __ldcg(src + D * D + r), acc[0]);
+        }
+        w *= gL;
     }
 }
 
@@ -569,35 +624,34 @@ __device__ void score_output(uint8_t *smem, Small &sm, const Params &p, const Ct
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         if (kMode && et < 32) sm.gtab[et] = gpow(lg, et);
-        // The predecessor's inclusive prefix, if it is already published,
-        // fetched now (phase A runs meanwhile) into TMEM O (row `row` of S,
-        // and z in column D); the state warps take it from there.
-        if (et == 0)
-            sm.lb_early = (it.hasA && it.seg > 0 &&
-                           load_flag(p.flags + item_index(it.bh, it.seg - 1, p)) >= FLAG_INCL)
-                              ? 1 : 0;
+        // The start state, if every predecessor has already published its
+        // local state, summed now (phase A runs meanwhile) into TMEM O (row
+        // `row` of S, and z in column D); the state warps take it from there.
+        if (et < 32) {
+            const bool e = it.hasA && it.seg > 0 &&
+                           preds_published(p, cx, it.bh, it.seg, lane, false);
+            if (lane == 0) sm.lb_early = e ? 1 : 0;
+        }
         named_bar_sync(BAR_E1, 128);
         if (sm.lb_early) {
-            const float *src = p.incl + (size_t)item_index(it.bh, it.seg - 1, p) * STATE;
-            const float4 *s4 = reinterpret_cast<const float4 *>(src);
+            const float gL = gpow(lg, p.seg_chunks * C);
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-                uint32_t w[32];
+            for (int g = 0; g < 5; ++g) {
+                float acc[32];
+                start_sum(p, it.bh, it.seg, row, g, gL, acc);
+                if (g < 4) {
+                    uint32_t w[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float4 x = __ldcg(s4 + (8 * g + u) * 128 + row);
-                    w[4 * u] = __float_as_uint(x.x);
-                    w[4 * u + 1] = __float_as_uint(x.y);
-                    w[4 * u + 2] = __float_as_uint(x.z);
-                    w[4 * u + 3] = __float_as_uint(x.w);
+                    for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(acc[e]);
+                    tmem_st32(lb + TM_O + 32 * g, w);
+                } else {
+                    uint32_t zw[16];
+                    zw[0] = __float_as_uint(acc[0]);
+#pragma unroll
+                    for (int e = 1; e < 16; ++e) zw[e] = 0u;
+                    tmem_st16(lb + TM_O + D, zw);
                 }
-                tmem_st32(lb + TM_O + 32 * g, w);
             }
-            uint32_t zw[16];
-            zw[0] = __float_as_uint(__ldcg(src + D * D + row));
-#pragma unroll
-            for (int e = 1; e < 16; ++e) zw[e] = 0u;
-            tmem_st16(lb + TM_O + D, zw);
             tmem_wait_st();
         }
         tc_fence_before();
@@ -664,26 +718,41 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
         const float gL = gpow(lg, p.seg_chunks * C);
         const float f0 = gpow(lg, min(C, p.N - it.c0 * C));
         if (it.hasA) {
-            wait_bar(&sm.s_full, ns & 1, cx);  // phase A's local state
+            // publish the segment's local state (phase A) at once
+            wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
             tc_fence_after();
+            float4 *d4 = reinterpret_cast<float4 *>(p.agg + (size_t)t * STATE);
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                uint32_t v[32];
+                tmem_ld32(lb + TM_S + 32 * g, v);
+                tmem_wait_ld();
+                reg_fence(v);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    d4[(8 * g + u) * 128 + a] = make_float4(u2f(v[4 * u]), u2f(v[4 * u + 1]),
+                                                            u2f(v[4 * u + 2]), u2f(v[4 * u + 3]));
+            }
+            uint32_t zl = tmem_ld1(lb + TM_S + D);
+            tmem_wait_ld();
+            reg_fence(zl);
+            p.agg[(size_t)t * STATE + D * D + a] = u2f(zl);
+            __threadfence();
+            named_bar_sync(BAR_E2, 128);
+            if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
         }
-        // The start state is the predecessor's inclusive prefix: parked by
-        // the score warps, or read here once published.
+        // The start state: summed by the score warps during phase A (parked
+        // in TMEM O), or here once every predecessor has published.
         wait_bar(&sm.lb_done, nl & 1, cx);
         ++nl;
         tc_fence_after();
         const bool pred = it.seg > 0;
         const bool early = sm.lb_early != 0;
-        const float *src =
-            pred ? p.incl + (size_t)item_index(it.bh, it.seg - 1, p) * STATE : nullptr;
         if (pred && !early) {
-            if (warp == kWarpE2 && lane == 0)
-                poll_flag_at_least(p.flags + item_index(it.bh, it.seg - 1, p), FLAG_INCL,
-                                   FLAG_INCL, cx);
+            if (warp == kWarpE2) preds_published(p, cx, it.bh, it.seg, lane, true);
             named_bar_sync(BAR_E2, 128);
         }
-        float *dst = it.hasA ? p.incl + (size_t)t * STATE : nullptr;
 #pragma unroll 1
         for (int g = 0; g < 5; ++g) {
             // g = 4: the z column
@@ -691,59 +760,27 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
             if (!pred) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) pv[e] = 0.f;
-            } else if (g == 4) {
-                float zp;
-                if (early) {
+            } else if (early) {
+                if (g < 4) {
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_O + 32 * g, v);
+                    tmem_wait_ld();
+                    reg_fence(v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pv[e] = u2f(v[e]);
+                } else {
                     uint32_t zr = tmem_ld1(lb + TM_O + D);
                     tmem_wait_ld();
                     reg_fence(zr);
-                    zp = u2f(zr);
-                } else {
-                    zp = __ldcg(src + D * D + a);
+                    pv[0] = u2f(zr);
                 }
-                pv[0] = zp;
-            } else if (early) {
-                uint32_t v[32];
-                tmem_ld32(lb + TM_O + 32 * g, v);
-                tmem_wait_ld();
-                reg_fence(v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) pv[e] = u2f(v[e]);
             } else {
-                const float4 *s4 = reinterpret_cast<const float4 *>(src);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float4 x = __ldcg(s4 + (8 * g + u) * 128 + a);
-                    pv[4 * u] = x.x;
-                    pv[4 * u + 1] = x.y;
-                    pv[4 * u + 2] = x.z;
-                    pv[4 * u + 3] = x.w;
-                }
+                start_sum(p, it.bh, it.seg, a, g, gL, pv);
             }
             if (g == 4) {
-                if (it.hasA) {
-                    uint32_t zl = tmem_ld1(lb + TM_S + D);
-                    tmem_wait_ld();
-                    reg_fence(zl);
-                    dst[D * D + a] = fmaf(gL, pv[0], u2f(zl));
-                }
                 store_zb(sb, a, pv[0]);
                 tmem_put_z(lb + TM_S + D, f0 * pv[0]);
                 continue;
-            }
-            if (it.hasA) {
-                // incl(s) = g^L incl(s-1) + local(s)
-                uint32_t v[32];
-                tmem_ld32(lb + TM_S + 32 * g, v);
-                tmem_wait_ld();
-                reg_fence(v);
-                float4 *d4 = reinterpret_cast<float4 *>(dst);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    d4[(8 * g + u) * 128 + a] = make_float4(fmaf(gL, pv[4 * u], u2f(v[4 * u])),
-                                        fmaf(gL, pv[4 * u + 1], u2f(v[4 * u + 1])),
-                                        fmaf(gL, pv[4 * u + 2], u2f(v[4 * u + 2])),
-                                        fmaf(gL, pv[4 * u + 3], u2f(v[4 * u + 3])));
             }
             store_sb32(sb, a, g, pv);
             // phase-B start: TMEM S = g^n0 S_start
@@ -753,14 +790,10 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
             tmem_st32(lb + TM_S + 32 * g, w);
         }
         tmem_wait_st();
-        if (it.hasA) __threadfence();
         fence_async_shared();
         tc_fence_before();
         named_bar_sync(BAR_E2, 128);
-        if (et == 0) {
-            if (it.hasA) publish_flag(p.flags + t, FLAG_INCL);
-            mbar_arrive(&sm.sb_ready);
-        }
+        if (et == 0) mbar_arrive(&sm.sb_ready);
         // phase B: per chunk, once its Khat^T [V | 1] and Qhat [S | z] have
         // completed, the bf16 [S | z] of the next chunk and with decay the
         // rescale g^n of the accumulator
@@ -930,7 +963,7 @@ inline size_t align_up_w(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct WidePlan {
     int seg_chunks, nseg, nchunks;
     long long items;
-    size_t off_flags, off_incl, total;
+    size_t off_flags, off_agg, total;
 };
 
 WidePlan plan_wide(const FwdShape &sh, int seg_chunks, int sms) {
@@ -943,8 +976,8 @@ WidePlan plan_wide(const FwdShape &sh, int seg_chunks, int sms) {
     pl.nseg = (pl.nchunks + seg_chunks - 1) / seg_chunks;
     pl.items = sh.BH() * pl.nseg;
     pl.off_flags = 256;
-    pl.off_incl = align_up_w(pl.off_flags + sizeof(int) * (size_t)pl.items, 256);
-    pl.total = pl.off_incl +
+    pl.off_agg = align_up_w(pl.off_flags + sizeof(int) * (size_t)pl.items, 256);
+    pl.total = pl.off_agg +
                (pl.nseg > 1 ? sizeof(float) * (size_t)STATE * (size_t)pl.items : 0);
     return pl;
 }
@@ -976,11 +1009,11 @@ TcResult launch_wide_with(const void *q, const void *k, const void *v, void *out
     p.norm = sh.norm;
     p.ctrl = reinterpret_cast<int *>(ws);
     p.flags = reinterpret_cast<int *>(ws + pl.off_flags);
-    p.incl = reinterpret_cast<float *>(ws + pl.off_incl);
+    p.agg = reinterpret_cast<float *>(ws + pl.off_agg);
     p.status = status;
     // the ticket counter, abort flag and segment flags start at zero; the
     // published states need no clearing
-    if ((e = tc_zero_words(ws, pl.off_incl, stream)) != cudaSuccess)
+    if ((e = tc_zero_words(ws, pl.off_agg, stream)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: workspace clear"};
     auto kern = dk.has ? causal_wide_kernel<1> : causal_wide_kernel<0>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -997,11 +1030,12 @@ TcResult launch_wide_with(const void *q, const void *k, const void *v, void *out
 }  // namespace
 
 // Segment length for the d = 128 kernel: as many segments per head as let
-// all items run in one wave (one item per SM), at most 16 (each segment adds
-// a link to the chain of inclusive prefixes).  Measured on the long-context
-// and decay workloads, one wave of long segments beats several waves of
-// short ones, whose per-item costs (look-back, publication, pipeline fill
-// and drain) outweigh the L2 hits of phase B's re-read of K and V.
+// all items run in one wave (one item per SM), at most 16 (a segment's
+// look-back reads every predecessor's local state).  Measured on the
+// long-context and decay workloads, one wave of long segments beats several
+// waves of short ones, whose per-item costs (look-back, publication,
+// pipeline fill and drain) outweigh the L2 hits of phase B's re-read of K
+// and V.
 int wide_segment_chunks(long long heads, int nchunks, int sms) {
     constexpr long long kMaxSegments = 16;
     if (sms < 1) sms = 1;
