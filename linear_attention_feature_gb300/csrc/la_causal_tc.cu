@@ -23,17 +23,21 @@
 // map is evaluated on packed bf16 pairs: phi(x) = max(x, 0) + 2^(min(x, 0)
 // log2 e), which is elu(x) + 1 with alpha = 1.
 //
+// This kernel serves d = 64 (all modes) and the gated mode at d = 128; the
+// other d = 128 modes run in la_causal_wide.cu.
+//
 // Sequence parallelism inside a head: a head's chunks are cut into segments
 // of `seg_chunks` chunks, and the value dimension into halves of 64 columns
 // (d = 128 gives two halves, each with all 128 key features).  A work item
 // is (head, segment, half); persistent CTAs take items from a ticket counter
 // (so a CTA only ever waits on items held by running CTAs).  A segment that
 // has successors first reduces its local decayed state (phase A:
-// Khat^T [V | 1] only, Khat_t = g^(L-1-t) phi(k_t) relative to its end) and publishes it; it then looks back over its
-// predecessors' published states (an inclusive prefix ends the walk) to get
-// its start state, publishes its own inclusive prefix, and runs the chunk
-// loop (phase B).  The phase-B re-read of K and V normally hits L2 (phase A
-// loads them with evict-last).
+// Khat^T [V | 1] only, Khat_t = g^(L-1-t) phi(k_t) relative to its end) and
+// publishes it at once.  Its start state is the decayed sum of all its
+// predecessors' local states, nearest first -- a fixed order, so repeated
+// calls are bit-identical -- and then it runs the chunk loop (phase B).
+// The phase-B re-read of K and V normally hits L2 (phase A loads them with
+// evict-last).
 //
 // Warp roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-9 feature-map transform, warps 10-13 score epilogue (mask,
@@ -78,7 +82,7 @@ constexpr int NX = DV + 16;  // extended N of the wide products
 
 struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
-    float *agg, *incl;  // [items][DK * DV + DK]: S rows (a-major), then z
+    float *agg;         // [items][DK * DV + DK]: S rows (a-major), then z
     int *flags;         // [items]
     float *S_out, *z_out;  // final state [BH][DK][DK] / [BH][DK], or NULL
     int phi, norm;         // elu(x) + 1 on q, k (else identity); divide by den
@@ -133,7 +137,7 @@ struct Small {
     uint64_t khat_ready[2];
     uint64_t item_full[2], item_empty[2];
     int ring[2];
-    int lb_flag[32], lb_n;  // look-back decision of the current item
+    int lb_n;  // look-back decision of the current item
     float tg_l[8], eg_l[4];  // mode 2: per-warp gate sums (transform, state roles)
     int tg_z[8], eg_z[4];
     uint32_t tmem_base;
@@ -895,56 +899,47 @@ struct SMap {
           hasz(DK == 64 ? lane < 64 : true) {}
 };
 
-// Decoupled look-back, step 1 (one warp): lane k watches segment seg-1-k.
-// The predecessors to combine run back from seg-1 to the nearest one that
-// has published its inclusive prefix (or to segment 0), and each of them
-// must have published at least its local aggregate.  The count and each
-// one's flag are left in shared memory for the warpgroup.  A chain longer
-// than 32 waits for one of the 32 nearest to publish its inclusive prefix
-// (each does, in segment order, so the wait ends).  With `wait` false it
-// looks once and leaves -1 if the chain is not decided yet.
+// Look-back, step 1 (one warp): decided once every predecessor (segments
+// 0 .. seg-1 of the head and half) has published its local state; 32 flags
+// per look.  Leaves seg in lb_n, or -1 when `wait` is false and some
+// predecessor has not published yet.
 __device__ __forceinline__ void resolve_lookback(Small &sm, const Params &p,
                                                  const Item &it, const Ctx &cx,
                                                  int lane, bool wait) {
-    if (it.seg == 0) {
-        if (lane == 0) sm.lb_n = 0;
-        return;
-    }
-    const int k = it.seg - 1 - lane;
-    const int *fp = p.flags + item_index(it.bh, k < 0 ? 0 : k, it.half, p);
-    const long long dl = clock64() + cx.timeout;
-    int f = FLAG_INCL, n = 0;
-    for (;;) {
-        f = k < 0 ? FLAG_INCL : load_flag(fp);
-        const unsigned stop = __ballot_sync(~0u, f >= FLAG_INCL);
-        const unsigned ready = __ballot_sync(~0u, f >= FLAG_AGG);
-        if (stop) {
-            const int ls = __ffs(stop) - 1;
-            const unsigned need = (2u << ls) - 1u;  // lanes 0..ls
-            if ((ready & need) == need) {
-                n = it.seg - 1 - ls < 0 ? ls : ls + 1;
+    int n = it.seg;
+    long long dl = 0;
+    for (int base = 0; base < it.seg && n >= 0; base += 32) {
+        const int s = base + lane;
+        const int *fp = p.flags + item_index(it.bh, s < it.seg ? s : 0, it.half, p);
+        for (;;) {
+            const int f = s < it.seg ? load_flag(fp) : FLAG_AGG;
+            if (__all_sync(~0u, f >= FLAG_AGG)) break;
+            if (!wait) {
+                n = -1;
                 break;
             }
+            if (__any_sync(~0u, *cx.abort != 0)) {
+                base = it.seg;  // aborted: the kernel finishes with invalid output
+                break;
+            }
+            const long long now = __shfl_sync(~0u, clock64(), 0);
+            if (dl == 0) {
+                dl = now + cx.timeout;
+            } else if (now > dl) {
+                if (lane == 0)
+                    raise_timeout(cx, 0x80000u | ((uint32_t)(reinterpret_cast<uintptr_t>(fp) >> 2) & 0x7FFFFu));
+                base = it.seg;
+                break;
+            }
+            __nanosleep(64);
         }
-        if (!wait) {
-            n = -1;
-            break;
-        }
-        const bool ab = __any_sync(~0u, *cx.abort != 0);
-        const bool late = __shfl_sync(~0u, (int)(clock64() > dl), 0) != 0;
-        if (ab || late) {
-            if (late && !ab && lane == 0)
-                raise_timeout(cx, 0x80000u | ((uint32_t)(reinterpret_cast<uintptr_t>(fp) >> 2) & 0x7FFFFu));
-            break;
-        }
-        __nanosleep(64);
     }
-    if (lane < n) sm.lb_flag[lane] = f;
     if (lane == 0) sm.lb_n = n;
 }
 
 // Look-back, step 2 (every thread): its 32 columns (half h) of row a of
-// sum_m g^(L m) state(seg-1-m) over the decided predecessors, and z[a].
+// sum_{m = 0..nlb-1} g^(L m) local(seg-1-m), nearest predecessor first (a
+// fixed order, so the start state does not depend on timing), and z[a].
 template <int DK, int kMode>
 __device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
                                              const Item &it, int nlb, int a,
@@ -957,8 +952,7 @@ __device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
     float w = 1.f;
     for (int m = 0; m < nlb; ++m) {
         const int pi = item_index(it.bh, it.seg - 1 - m, it.half, p);
-        const float *src =
-            (sm.lb_flag[m] == FLAG_INCL ? p.incl : p.agg) + (size_t)pi * L::STATE;
+        const float *src = p.agg + (size_t)pi * L::STATE;
         const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV + 32 * h);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -1021,7 +1015,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
         float gL = gpow(lg, p.seg_chunks * C);
         if (kMode == 2 && it.hasA) {
             // the segment's product of gates: scales its start state into
-            // its inclusive prefix, and is published for its successors
+            // what its successors' look-back applies across it, published
             float L2;
             int Z;
             gate_totals(L2, Z, p, it.bh, it.c0 * C, min(it.c1 * C, p.N), et, 128,
@@ -1030,7 +1024,6 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             if (et == 0) p.gprod[t] = gL;  // visible with the item's flags
         }
         float *agg = p.agg + (size_t)t * L::STATE;
-        float *incl = p.incl + (size_t)t * L::STATE;
         const int n0 = min(C, p.N - it.c0 * C);
         float f0 = gpow(lg, n0);
         // Look-back, first try: if the predecessors have already published,
@@ -1060,6 +1053,29 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
             tc_fence_after();
+            // publish the segment's local state at once
+#pragma unroll
+            for (int hh = 0; hh < SM::NH; ++hh) {
+                const int h = h0 + hh;
+                uint32_t v[32];
+                tmem_ld32(lb + TM_S + 32 * h, v);
+                tmem_wait_ld();
+                reg_fence(v);
+                float4 *dst = reinterpret_cast<float4 *>(agg + a * DV + 32 * h);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
+                                         u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+            }
+            if (hasz) {
+                uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                tmem_wait_ld();
+                reg_fence(zl);
+                agg[DK * DV + a] = u2f(zl);
+            }
+            __threadfence();
+            named_bar_sync(BAR_E2, 128);
+            if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
         }
         if (kMode == 2) {
             // the first chunk's product of gates (its transform wrote the
@@ -1070,8 +1086,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                            n0 - 1, -1);
         }
         if (early) {
-            // inclusive prefix = g^L S_start + local state, and the phase-B
-            // start state; the prefix is published without an aggregate
+            // the phase-B start state from the sums parked during phase A
 #pragma unroll 1
             for (int hh = 0; hh < SM::NH; ++hh) {
                 const int h = h0 + hh;
@@ -1087,23 +1102,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                     acc[4 * e + 3] = u.w;
                 }
                 uint32_t v[32];
-                tmem_ld32(lb + TM_S + 32 * h, v);
-                tmem_wait_ld();
-                reg_fence(v);
-                float4 *dst = reinterpret_cast<float4 *>(incl + a * DV + 32 * h);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = make_float4(fmaf(gL, acc[4 * e], u2f(v[4 * e])),
-                                         fmaf(gL, acc[4 * e + 1], u2f(v[4 * e + 1])),
-                                         fmaf(gL, acc[4 * e + 2], u2f(v[4 * e + 2])),
-                                         fmaf(gL, acc[4 * e + 3], u2f(v[4 * e + 3])));
-                if (zh) {
-                    uint32_t zl = tmem_ld1(lb + TM_S + DV);
-                    tmem_wait_ld();
-                    reg_fence(zl);
-                    incl[DK * DV + a] = fmaf(gL, accz_e, u2f(zl));
-                    tmem_put_z(lb + TM_S + DV, f0 * accz_e);
-                }
+                if (zh) tmem_put_z(lb + TM_S + DV, f0 * accz_e);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f0 * acc[e]);
                 tmem_st32(lb + TM_S + 32 * h, v);
@@ -1113,31 +1112,6 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             }
             if (hasz) store_zrow(sbz, a, accz_e);
         } else {
-            if (it.hasA) {
-                // publish the segment's local state (its aggregate)
-#pragma unroll
-                for (int hh = 0; hh < SM::NH; ++hh) {
-                    const int h = h0 + hh;
-                    uint32_t v[32];
-                    tmem_ld32(lb + TM_S + 32 * h, v);
-                    tmem_wait_ld();
-                    reg_fence(v);
-                    float4 *dst = reinterpret_cast<float4 *>(agg + a * DV + 32 * h);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
-                                             u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
-                }
-                if (hasz) {
-                    uint32_t zl = tmem_ld1(lb + TM_S + DV);
-                    tmem_wait_ld();
-                    reg_fence(zl);
-                    agg[DK * DV + a] = u2f(zl);
-                }
-                __threadfence();
-                named_bar_sync(BAR_E2, 128);
-                if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
-            }
             // look-back, waiting for the predecessors
             if (warp == kWarpE2) resolve_lookback(sm, p, it, cx, lane, true);
             named_bar_sync(BAR_E2, 128);
@@ -1148,27 +1122,6 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 const bool zh = hasz && hh == 0;
                 float acc[32], accz;
                 lookback_sum<DK, kMode>(sm, p, it, nlb, a, h, zh, gL, acc, accz);
-                if (it.hasA) {
-                    // inclusive prefix = g^L S_start + local state (published
-                    // below, once phase B has its start state)
-                    uint32_t v[32];
-                    tmem_ld32(lb + TM_S + 32 * h, v);
-                    tmem_wait_ld();
-                    reg_fence(v);
-                    float4 *dst = reinterpret_cast<float4 *>(incl + a * DV + 32 * h);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(fmaf(gL, acc[4 * e], u2f(v[4 * e])),
-                                             fmaf(gL, acc[4 * e + 1], u2f(v[4 * e + 1])),
-                                             fmaf(gL, acc[4 * e + 2], u2f(v[4 * e + 2])),
-                                             fmaf(gL, acc[4 * e + 3], u2f(v[4 * e + 3])));
-                    if (zh) {
-                        uint32_t zl = tmem_ld1(lb + TM_S + DV);
-                        tmem_wait_ld();
-                        reg_fence(zl);
-                        incl[DK * DV + a] = fmaf(gL, accz, u2f(zl));
-                    }
-                }
                 // phase-B start: TMEM [S | z] = g^n0 [S_start | z_start], and
                 // the bf16 [S_start | z_start] operand
                 uint32_t v[32];
@@ -1187,11 +1140,6 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
         tc_fence_before();
         named_bar_sync(BAR_E2, 128);
         if (et == 0) mbar_arrive(&sm.sb_ready);
-        if (it.hasA) {
-            __threadfence();
-            named_bar_sync(BAR_E2, 128);
-            if (et == 0) publish_flag(p.flags + t, FLAG_INCL);
-        }
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             if (c + 1 < it.c1) {
                 // state epilogue: [S | z] of chunk c+1 as the bf16 operand,
@@ -1398,7 +1346,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct CausalPlan {
     int seg_chunks, nseg, nchunks, nhalf;
     long long items;
-    size_t off_flags, off_agg, off_incl, off_gprod, total;
+    size_t off_flags, off_agg, off_gprod, total;
 };
 
 template <int DK, int kMode>
@@ -1417,8 +1365,7 @@ CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms) {
     pl.off_flags = 256;
     pl.off_agg = align_up(pl.off_flags + sizeof(int) * (size_t)pl.items, 256);
     const size_t state_bytes = (pl.nseg > 1) ? sizeof(float) * L::STATE * (size_t)pl.items : 0;
-    pl.off_incl = align_up(pl.off_agg + state_bytes, 256);
-    pl.off_gprod = align_up(pl.off_incl + state_bytes, 256);
+    pl.off_gprod = align_up(pl.off_agg + state_bytes, 256);
     pl.total = pl.off_gprod + (kMode == 2 ? sizeof(float) * (size_t)pl.items : 0);
     return pl;
 }
@@ -1472,7 +1419,6 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.ctrl = reinterpret_cast<int *>(w8);
     p.flags = reinterpret_cast<int *>(w8 + pl.off_flags);
     p.agg = reinterpret_cast<float *>(w8 + pl.off_agg);
-    p.incl = reinterpret_cast<float *>(w8 + pl.off_incl);
     p.gprod = reinterpret_cast<float *>(w8 + pl.off_gprod);
     p.status = status;
     e = tc_zero_words(ws, pl.off_agg, stream);
@@ -1599,15 +1545,14 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     p.nhalf = DK / DV;
     int seg = auto_segment_chunks<kMode != 0>(BH * p.nhalf, p.nchunks, sms);
     // lengthen segments until the workspace fits the static scratch
-    size_t off_agg = 0, off_incl = 0, total = 0;
+    size_t off_agg = 0, total = 0;
     long long items = 0;
     for (;;) {
         const int nseg = (p.nchunks + seg - 1) / seg;
         items = (long long)BH * nseg * p.nhalf;
         off_agg = align_up(256 + sizeof(int) * (size_t)items, 256);
         const size_t sb = nseg > 1 ? sizeof(float) * L::STATE * (size_t)items : 0;
-        off_incl = align_up(off_agg + sb, 256);
-        total = off_incl + sb;
+        total = off_agg + sb;
         if (total <= (size_t)LA_NOALLOC_SCRATCH_BYTES || seg >= p.nchunks) break;
         seg = seg * 2 < p.nchunks ? seg * 2 : p.nchunks;
     }
@@ -1624,7 +1569,6 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     p.ctrl = reinterpret_cast<int *>(scratch);
     p.flags = reinterpret_cast<int *>(scratch + 256);
     p.agg = reinterpret_cast<float *>(scratch + off_agg);
-    p.incl = reinterpret_cast<float *>(scratch + off_incl);
     p.status = status;
     // the counter and flags must start at zero; the states need no clearing
     if ((e = tc_zero_words(scratch, off_agg, stream)) != cudaSuccess)
