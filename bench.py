@@ -218,10 +218,6 @@ KNOWN_TRAFFIC = {
     # kernel_sources_digest(kernel) at capture time)
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
         {"sources": "78d9d80b358cae4a", "bytes": 100798720 + 4932096},
-    ("causal_kernel<128,0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "78d9d80b358cae4a", "bytes": 1312434688 + 234056448},
-    ("causal_kernel<128,1>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "78d9d80b358cae4a", "bytes": 409565184 + 131761152},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
         {"sources": "8023d72c789a91db", "bytes": 100728320 + 2898688},
 }
@@ -232,6 +228,8 @@ KNOWN_TRAFFIC = {
 # while their digest is unchanged.
 KERNEL_SOURCES = {
     "causal_kernel": ("la_causal_tc.cu", "la_tc_common.cuh", "la_tc_ptx.cuh", "la_tc_host.h"),
+    "causal_wide_kernel": ("la_causal_wide.cu", "la_tc_common.cuh", "la_tc_ptx.cuh",
+                           "la_tc_host.h"),
     "noncausal_kernel": ("la_noncausal_tc.cu", "la_tc_common.cuh", "la_tc_ptx.cuh", "la_tc_host.h"),
 }
 
@@ -281,7 +279,7 @@ def chunk_flops(B, H, N, d, C):
 # ------------------------------------------------------------------ our arm
 
 
-MAIN_KERNEL = "causal_kernel<128,0>"
+MAIN_KERNEL = "causal_wide_kernel<0>"
 MID_KERNEL = "causal_kernel<64,0>"
 
 
@@ -471,7 +469,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
              kernel="noncausal_kernel<64>")
     wd = wl.WORKLOADS["bf16_decay_b4h8_n16384_d128"]
     fwd_path("bf16_decay_b4h8_n16384_d128 causal", wd.name, True,
-             decay=list(wd.decay), kernel="causal_kernel<128,1>")
+             decay=list(wd.decay), kernel="causal_wide_kernel<1>")
     fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
     fwd_path(f"{MID} causal with final state", MID, True, inputs=mid_inputs(),
              state=True)

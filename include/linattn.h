@@ -346,6 +346,29 @@ int la_abi_version(void);
  * all streams) since it was loaded; for measurement and launch accounting. */
 unsigned long long la_kernel_launch_count(void);
 
+/*
+ * Testing hooks.  The pages have no counterpart: these exist so that the
+ * library's own tests can drive its failure paths without faulting a GPU.
+ * Each applies to the calling thread only and is consumed by the next call
+ * it affects.
+ *
+ * la_debug_inject_timeout -- the next d = 128 causal tensor-core launch
+ * (la_forward and friends with bf16, d = 128, no gates) bounds every wait by
+ * `wait_cycles` clock cycles (>= 4096) instead of about two seconds, and
+ * segment `hold_segment` of every head never publishes its local state
+ * (-1: all publish).  Its successors' waits then run out: the launch records
+ * LA_ERR_TIMEOUT in the device status word, every later wait of the launch
+ * passes through, it finishes (outputs invalid) and la_check_device_status
+ * reports LA_ERR_TIMEOUT.  LA_ERR_INVALID_ARG for wait_cycles < 4096.
+ *
+ * la_debug_fail_next_allocs -- the next `n` stream-ordered workspace
+ * allocations of the tensor-core launches (made when no workspace is passed)
+ * fail: those calls return LA_ERR_NO_MEMORY and enqueue nothing.  n = 0
+ * clears the hook; LA_ERR_INVALID_ARG for n < 0.
+ */
+la_status la_debug_inject_timeout(long long wait_cycles, int hold_segment);
+la_status la_debug_fail_next_allocs(int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,8 @@ EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_forward_causal_noalloc", "la_forward_host",
             "la_forward_host_workspace_bytes", "la_forward_causal_state",
             "la_decode_step_ex", "la_forward_variant", "la_decode_step_variant",
-            "la_forward_gated", "la_decode_step_gated", "la_decode_step_delta")
+            "la_forward_gated", "la_decode_step_gated", "la_decode_step_delta",
+            "la_debug_inject_timeout", "la_debug_fail_next_allocs")
 
 FEATURE_MAPS = {"elu1": 0, "identity": 1}
 
@@ -82,6 +83,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                     ctypes.c_size_t, V]
     lib.la_forward_host_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.la_forward_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.la_debug_inject_timeout.argtypes = [ctypes.c_longlong, I]
+    lib.la_debug_fail_next_allocs.argtypes = [I]
     lib.la_check_device_status.argtypes = [V]
     lib.la_status_string.argtypes = [I]
     lib.la_status_string.restype = ctypes.c_char_p
@@ -94,6 +97,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
               "la_decode_step_ex", "la_forward_causal_state",
               "la_forward_variant", "la_decode_step_variant",
               "la_forward_gated", "la_decode_step_gated", "la_decode_step_delta",
+              "la_debug_inject_timeout", "la_debug_fail_next_allocs",
               "la_check_device_status", "la_abi_version"):
         getattr(lib, n).restype = I
     if path is None:

@@ -398,4 +398,19 @@ int la_abi_version(void) { return 1; }
 __attribute__((visibility("default")))
 unsigned long long la_kernel_launch_count(void) { return g_launches.load(); }
 
+__attribute__((visibility("default")))
+la_status la_debug_inject_timeout(long long wait_cycles, int hold_segment) {
+    if (wait_cycles < 4096)
+        return fail(LA_ERR_INVALID_ARG, "la_debug_inject_timeout: wait_cycles below 4096");
+    la::tc_debug_set_timeout(wait_cycles, hold_segment);
+    return LA_OK;
+}
+
+__attribute__((visibility("default")))
+la_status la_debug_fail_next_allocs(int n) {
+    if (n < 0) return fail(LA_ERR_INVALID_ARG, "la_debug_fail_next_allocs: negative n");
+    la::tc_debug_fail_allocs(n);
+    return LA_OK;
+}
+
 }  // extern "C"

@@ -136,6 +136,7 @@ struct Small {
     // issued after that observation)
     uint64_t khat_ready[2];
     uint64_t item_full[2], item_empty[2];
+    uint64_t fin;  // every product of the CTA has completed (exit)
     int ring[2];
     int lb_n;  // look-back decision of the current item
     float tg_l[8], eg_l[4];  // mode 2: per-warp gate sums (transform, state roles)
@@ -171,7 +172,7 @@ __device__ __forceinline__ int item_index(int bh, int seg, int half,
 __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
                                         int bar_id, int nthreads, bool leader) {
     const int r = tl & 1;
-    wait_bar(&sm.item_full[r], (tl >> 1) & 1, cx);
+    settle_wait(&sm.item_full[r], (tl >> 1) & 1);
     const int t = ((volatile int *)sm.ring)[r];  // -1 once a wait gave up
     if (bar_id) named_bar_sync(bar_id, nthreads);
     if (leader) mbar_arrive(&sm.item_empty[r]);
@@ -188,20 +189,29 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
     using L = Layout<DK, kMode>;
     const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
     int j = 0, tl = 0;
+    bool stop = false;  // a wait gave up: no further loads
     for (;;) {
         int t = atomicAdd(p.ctrl, 1);
-        if (t >= p.items || *cx.abort) t = -1;
+        if (t >= p.items || stop || *cx.abort) t = -1;
         const int r = tl & 1;
-        wait_bar(&sm.item_empty[r], ((tl >> 1) & 1) ^ 1, cx);
+        settle_wait(&sm.item_empty[r], ((tl >> 1) & 1) ^ 1);
         ((volatile int *)sm.ring)[r] = t;
         mbar_arrive(&sm.item_full[r]);
         ++tl;
         if (t < 0) break;
         const Item it = decode_item(t, p);
-        for (int pass = it.hasA ? 0 : 1; pass < 2; ++pass) {
+        for (int pass = it.hasA ? 0 : 1; pass < 2 && !stop; ++pass) {
             for (int c = it.c0; c < it.c1; ++c, ++j) {
                 const int st = j % L::STAGES;
-                wait_bar(&sm.empty[st], ((j / L::STAGES) & 1) ^ 1, cx);
+                const uint32_t par = ((j / L::STAGES) & 1) ^ 1;
+                if (!wait_bar(&sm.empty[st], par, cx)) {
+                    stop = true;
+                    break;
+                }
+                // one arming per phase: the slot's previous load has landed
+                // (it always has unless a wait gave up and let a consumer
+                // run ahead)
+                if (j >= L::STAGES) settle_wait(&sm.full[st], par);
                 uint8_t *base = smem + st * L::STAGE;
                 const uint64_t pol = pass == 0 ? keep : stream;
                 mbar_arrive_expect_tx(&sm.full[st], pass == 0
@@ -219,6 +229,9 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
             }
         }
     }
+    // the last load of each slot has landed before the CTA may exit
+    for (int x = j - L::STAGES; x < j; ++x)
+        if (x >= 0) settle_wait(&sm.full[x % L::STAGES], (x / L::STAGES) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -395,6 +408,9 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
         j += nB;
         nb += nB;
     }
+    // every product has completed before TMEM is released
+    mma_commit(&sm.fin);
+    settle_wait(&sm.fin, 0);
 }
 
 // ---------------------------------------------------------------- gates (mode 2)
@@ -1267,6 +1283,7 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
             mbar_init(&sm.item_full[r], 1);
             mbar_init(&sm.item_empty[r], 4);
         }
+        mbar_init(&sm.fin, 1);
         fence_mbar_init();
     }
     // constant operand blocks: the ones column of [V | 1], and the z block of
@@ -1412,7 +1429,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     if (ws) {
         if (ws_bytes < pl.total)
             return {LA_ERR_INVALID_ARG, cudaSuccess, "la_forward: workspace too small"};
-    } else if ((e = cudaMallocAsync(&ws, pl.total, stream)) != cudaSuccess) {
+    } else if ((e = tc_workspace_alloc(&ws, pl.total, stream)) != cudaSuccess) {
         return {LA_ERR_NO_MEMORY, e, "la_forward: workspace allocation"};
     }
     char *w8 = static_cast<char *>(ws);

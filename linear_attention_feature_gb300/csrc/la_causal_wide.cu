@@ -102,6 +102,7 @@ struct Params {
     int *ctrl;              // [0] ticket counter, [1] abort flag
     int *status;            // device status word
     long long timeout;      // clock cycles per bounded wait
+    int hold_seg;           // test hook: this segment never publishes (-1: none)
 };
 
 struct Small {
@@ -144,21 +145,12 @@ __device__ __forceinline__ int item_index(int bh, int seg, const Params &p) {
 __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
                                         int bar_id, int nthreads, bool leader) {
     const int r = tl & 1;
-    wait_bar(&sm.item_full[r], (tl >> 1) & 1, cx);
+    settle_wait(&sm.item_full[r], (tl >> 1) & 1);
     const int t = ((volatile int *)sm.ring)[r];  // -1 once a wait gave up
     if (bar_id) named_bar_sync(bar_id, nthreads);
     if (leader) mbar_arrive(&sm.item_empty[r]);
     ++tl;
     return t;
-}
-
-// A wait that ignores the abort flag (bounded by the same deadline): used
-// at exit, so that no TMA load or MMA is still in flight when the CTA's
-// shared memory and TMEM are released.
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctx &cx) {
-    const long long dl = clock64() + cx.timeout;
-    while (!mbar_try_wait(bar, parity) && clock64() <= dl) {
-    }
 }
 
 // ---------------------------------------------------------------- look-back
@@ -243,7 +235,7 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
         int t = atomicAdd(p.ctrl, 1);
         if (t >= p.items || *cx.abort) t = -1;
         const int r = tl & 1;
-        wait_bar_spin(&sm.item_empty[r], ((tl >> 1) & 1) ^ 1, cx);
+        settle_wait(&sm.item_empty[r], ((tl >> 1) & 1) ^ 1);
         ((volatile int *)sm.ring)[r] = t;
         mbar_arrive(&sm.item_full[r]);
         ++tl;
@@ -269,6 +261,9 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
             const int st = j % STAGES;
             const uint32_t par = ((j / STAGES) & 1) ^ 1;
             if (!wait_bar_spin(&sm.k_empty[st], par, cx)) break;
+            // one arming per phase: the slot's previous load has landed (it
+            // always has unless a wait gave up and let a consumer run ahead)
+            if (j >= STAGES) settle_wait(&sm.k_full[st], par);
             mbar_arrive_expect_tx(&sm.k_full[st], TILE);
             for (int kb = 0; kb < 2; ++kb)
                 tma_load_3d(smem + k_off(st) + kb * BLK, tk, &sm.k_full[st], 64 * kb,
@@ -276,6 +271,7 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
             ++jk;
             if (pass == 1) {
                 if (!wait_bar_spin(&sm.q_empty, (nq & 1) ^ 1, cx)) break;
+                if (nq > 0) settle_wait(&sm.q_full, (nq & 1) ^ 1);
                 mbar_arrive_expect_tx(&sm.q_full, TILE);
                 for (int kb = 0; kb < 2; ++kb)
                     tma_load_3d(smem + OFF_Q + kb * BLK, tq, &sm.q_full, 64 * kb, c * C,
@@ -289,6 +285,7 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
             if (out_c[st] >= 0) store_staged(smem, to, st, out_c[st], out_bh[st]);
             out_c[st] = pass == 1 ? c : -1;
             out_bh[st] = it.bh;
+            if (j >= STAGES) settle_wait(&sm.v_full[st], par);
             mbar_arrive_expect_tx(&sm.v_full[st], TILE);
             for (int kb = 0; kb < 2; ++kb)
                 tma_load_3d(smem + v_off(st) + kb * v_lbo(st), tv, &sm.v_full[st], 64 * kb,
@@ -307,10 +304,10 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
     tma_store_wait_all<0>();
     // the last loads of each slot have landed before the CTA may exit
     for (int x = jk - STAGES; x < jk; ++x)
-        if (x >= 0) drain_wait(&sm.k_full[x % STAGES], (x / STAGES) & 1, cx);
+        if (x >= 0) settle_wait(&sm.k_full[x % STAGES], (x / STAGES) & 1);
     for (int x = j - STAGES; x < j; ++x)
-        if (x >= 0) drain_wait(&sm.v_full[x % STAGES], (x / STAGES) & 1, cx);
-    if (nq > 0) drain_wait(&sm.q_full, (nq - 1) & 1, cx);
+        if (x >= 0) settle_wait(&sm.v_full[x % STAGES], (x / STAGES) & 1);
+    if (nq > 0) settle_wait(&sm.q_full, (nq - 1) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -416,7 +413,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
     }
     // every product has completed before TMEM is released
     mma_commit(&sm.fin);
-    drain_wait(&sm.fin, 0, cx);
+    settle_wait(&sm.fin, 0);
 }
 
 // ---------------------------------------------------------------- transform
@@ -740,7 +737,7 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
             p.agg[(size_t)t * STATE + D * D + a] = u2f(zl);
             __threadfence();
             named_bar_sync(BAR_E2, 128);
-            if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
+            if (et == 0 && it.seg != p.hold_seg) publish_flag(p.flags + t, FLAG_AGG);
         }
         // The start state: summed by the score warps during phase A (parked
         // in TMEM O), or here once every predecessor has published.
@@ -748,11 +745,12 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
         ++nl;
         tc_fence_after();
         const bool pred = it.seg > 0;
-        const bool early = sm.lb_early != 0;
-        if (pred && !early) {
-            if (warp == kWarpE2) preds_published(p, cx, it.bh, it.seg, lane, true);
-            named_bar_sync(BAR_E2, 128);
-        }
+        // one value per warp; the barrier below is passed whatever it is, so
+        // that the role's barrier count follows from the item alone
+        const bool early = __shfl_sync(~0u, sm.lb_early, 0) != 0;
+        if (pred && !early && warp == kWarpE2)
+            preds_published(p, cx, it.bh, it.seg, lane, true);
+        named_bar_sync(BAR_E2, 128);
 #pragma unroll 1
         for (int g = 0; g < 5; ++g) {
             // g = 4: the z column
@@ -1003,6 +1001,8 @@ TcResult launch_wide_with(const void *q, const void *k, const void *v, void *out
     p.nseg = pl.nseg;
     p.items = (int)pl.items;
     p.timeout = 1LL << 32;
+    p.hold_seg = -1;
+    tc_debug_take_timeout(&p.timeout, &p.hold_seg);
     p.S_out = S_out;
     p.z_out = z_out;
     p.phi = sh.phi;
@@ -1061,7 +1061,7 @@ TcResult launch_causal_wide(const void *q, const void *k, const void *v, void *o
     if (ws) {
         if (ws_bytes < pl.total)
             return {LA_ERR_INVALID_ARG, cudaSuccess, "la_forward: workspace too small"};
-    } else if ((e = cudaMallocAsync(&ws, pl.total, stream)) != cudaSuccess) {
+    } else if ((e = tc_workspace_alloc(&ws, pl.total, stream)) != cudaSuccess) {
         return {LA_ERR_NO_MEMORY, e, "la_forward: workspace allocation"};
     }
     TcResult r = launch_wide_with(q, k, v, out, sh, dk, pl, status, static_cast<char *>(ws),

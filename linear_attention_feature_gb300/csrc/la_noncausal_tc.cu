@@ -74,6 +74,7 @@ struct Small {
     uint64_t full[4], empty[4], xf[4];
     uint64_t s_full, s_free, sb_ready, o_full[2], o_empty[2];
     uint64_t item_full[2], item_empty[2];
+    uint64_t fin;  // every product of the CTA has completed (exit)
     int ring[2];
     uint32_t tmem_base;
 };
@@ -101,7 +102,7 @@ __device__ __forceinline__ Item decode_item(int t, const Params &p) {
 __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
                                         int bar_id, int nthreads, bool leader) {
     const int r = tl & 1;
-    wait_bar(&sm.item_full[r], (tl >> 1) & 1, cx);
+    settle_wait(&sm.item_full[r], (tl >> 1) & 1);
     const int t = ((volatile int *)sm.ring)[r];  // -1 once a wait gave up
     if (bar_id) named_bar_sync(bar_id, nthreads);
     if (leader) mbar_arrive(&sm.item_empty[r]);
@@ -117,11 +118,12 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
     const uint64_t pol = policy_evict_first();
     const int total = p.items1 + p.items2;
     int j = 0, tl = 0;
+    bool stop = false;  // a wait gave up: no further loads
     for (;;) {
         int t = atomicAdd(p.ctrl, 1);
-        if (t >= total || *cx.abort) t = -1;
+        if (t >= total || stop || *cx.abort) t = -1;
         const int r = tl & 1;
-        wait_bar(&sm.item_empty[r], ((tl >> 1) & 1) ^ 1, cx);
+        settle_wait(&sm.item_empty[r], ((tl >> 1) & 1) ^ 1);
         ((volatile int *)sm.ring)[r] = t;
         mbar_arrive(&sm.item_full[r]);
         ++tl;
@@ -129,7 +131,13 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
         const Item it = decode_item(t, p);
         for (int c = it.c0; c < it.c1; ++c, ++j) {
             const int st = j % L::STAGES;
-            wait_bar(&sm.empty[st], ((j / L::STAGES) & 1) ^ 1, cx);
+            const uint32_t par = ((j / L::STAGES) & 1) ^ 1;
+            if (!wait_bar(&sm.empty[st], par, cx)) {
+                stop = true;
+                break;
+            }
+            // one arming per phase: the slot's previous load has landed
+            if (j >= L::STAGES) settle_wait(&sm.full[st], par);
             uint8_t *base = smem + st * L::STAGE;
             if (it.pass2) {
                 mbar_arrive_expect_tx(&sm.full[st], L::TILE);
@@ -146,6 +154,9 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
             }
         }
     }
+    // the last load of each slot has landed before the CTA may exit
+    for (int x = j - L::STAGES; x < j; ++x)
+        if (x >= 0) settle_wait(&sm.full[x % L::STAGES], (x / L::STAGES) & 1);
 }
 
 template <int DK>
@@ -199,6 +210,9 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             }
         }
     }
+    // every product has completed before TMEM is released
+    mma_commit(&sm.fin);
+    settle_wait(&sm.fin, 0);
 }
 
 // phi over this thread's half of one row of a [128][DK] swizzled tile, in
@@ -424,6 +438,7 @@ noncausal_kernel(const __grid_constant__ CUtensorMap tq,
             mbar_init(&sm.item_full[b], 1);
             mbar_init(&sm.item_empty[b], 3);  // MMA, transform, epilogue
         }
+        mbar_init(&sm.fin, 1);
         fence_mbar_init();
     }
     // ones column of [V | 1]; the z block of [S | z] outside column 0 is zero
@@ -542,7 +557,7 @@ TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
     if (ws) {
         if (ws_bytes < pl.total)
             return {LA_ERR_INVALID_ARG, cudaSuccess, "la_forward: workspace too small"};
-    } else if ((e = cudaMallocAsync(&ws, pl.total, stream)) != cudaSuccess) {
+    } else if ((e = tc_workspace_alloc(&ws, pl.total, stream)) != cudaSuccess) {
         return {LA_ERR_NO_MEMORY, e, "la_forward: workspace allocation"};
     }
     char *w8 = static_cast<char *>(ws);

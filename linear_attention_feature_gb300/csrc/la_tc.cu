@@ -47,6 +47,36 @@ __global__ void zero_words_kernel(uint4 *p, size_t n) {
 
 }  // namespace
 
+namespace {
+thread_local long long t_debug_wait = 0;
+thread_local int t_debug_hold = -1;
+thread_local int t_debug_fail_allocs = 0;
+}  // namespace
+
+void tc_debug_set_timeout(long long wait_cycles, int hold_segment) {
+    t_debug_wait = wait_cycles;
+    t_debug_hold = hold_segment;
+}
+
+bool tc_debug_take_timeout(long long *wait_cycles, int *hold_segment) {
+    if (t_debug_wait <= 0) return false;
+    *wait_cycles = t_debug_wait;
+    *hold_segment = t_debug_hold;
+    t_debug_wait = 0;
+    t_debug_hold = -1;
+    return true;
+}
+
+void tc_debug_fail_allocs(int n) { t_debug_fail_allocs = n > 0 ? n : 0; }
+
+cudaError_t tc_workspace_alloc(void **ws, size_t bytes, cudaStream_t stream) {
+    if (t_debug_fail_allocs > 0) {
+        --t_debug_fail_allocs;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMallocAsync(ws, bytes, stream);
+}
+
 cudaError_t tc_zero_words(void *p, size_t bytes, cudaStream_t stream) {
     const size_t n = bytes / 16;
     if (n == 0) return cudaSuccess;

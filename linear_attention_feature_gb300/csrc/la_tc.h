@@ -43,6 +43,19 @@ size_t tc_workspace_bytes(const FwdShape &sh, int causal, bool decay,
 // back until they finish.
 cudaError_t tc_zero_words(void *p, size_t bytes, cudaStream_t stream);
 
+// Stream-ordered workspace allocation of the tensor-core launches
+// (cudaMallocAsync), which the allocation-failure test hook can make fail.
+cudaError_t tc_workspace_alloc(void **ws, size_t bytes, cudaStream_t stream);
+
+// Test hooks, per calling thread, each consumed by the next launch that
+// reads it (set through la_debug_inject_timeout / la_debug_fail_next_allocs):
+// the next d = 128 causal launch bounds every wait by `wait_cycles` and never
+// publishes segment `hold_segment`'s state (-1: every segment publishes);
+// the next `n` workspace allocations fail.
+void tc_debug_set_timeout(long long wait_cycles, int hold_segment);
+bool tc_debug_take_timeout(long long *wait_cycles, int *hold_segment);
+void tc_debug_fail_allocs(int n);
+
 // Non-causal two-pass kernel (la_noncausal_tc.cu).
 TcResult launch_noncausal_tc(const void *q, const void *k, const void *v,
                              void *out, const FwdShape &sh, int seg_chunks,

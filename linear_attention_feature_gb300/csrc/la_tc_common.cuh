@@ -70,6 +70,22 @@ __device__ __forceinline__ bool wait_bar_spin(uint64_t *bar, uint32_t parity,
     return wait_bar_poll(bar, parity, cx, true);
 }
 
+// A wait for the phase itself that ignores the abort flag (bounded all the
+// same, far above any wait limit).  Used where the real completion matters
+// whatever happened elsewhere: the item ring, whose entries all warps of a
+// role must read alike (their named-barrier counts follow from the item); a
+// TMA full barrier before it is armed again (one arrival per phase); and the
+// drain at exit, so that no TMA load or MMA is still in flight when the CTA's
+// shared memory and TMEM are released.
+constexpr long long kSettleCycles = 1LL << 34;
+
+__device__ __forceinline__ void settle_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return;
+    const long long dl = clock64() + kSettleCycles;
+    while (!mbar_try_wait_ns(bar, parity, kSuspendNs) && clock64() <= dl) {
+    }
+}
+
 // Reads a published-state flag (acquire, device scope).
 __device__ __forceinline__ int load_flag(const int *f) {
     int v;
