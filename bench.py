@@ -476,6 +476,9 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
     fwd_path("bf16_decay_b4h8_n16384_d128 retention", wd.name, True,
              decay=list(wd.decay), retention=True)
     fwd_path(f"{MID} gated", MID, True, inputs=mid_inputs(), gated=True)
+    # the same gated problem in fp32 (the CUDA-core kernels)
+    fwd_path(f"{MID} gated fp32", MID, True, elem=4, gated=True,
+             inputs=tuple(t.float() for t in mid_inputs()))
     mid.clear()
     try:
         res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,

@@ -94,10 +94,11 @@ typedef struct {
  *            (no TF32); bf16 inputs with d in {64, 128} run on the tcgen05
  *            tensor-core kernels, other d on the CUDA-core path.
  *
- * Workspace: the tensor-core kernels need a small stream-ordered scratch
- * (per-segment states and flags), allocated with cudaMallocAsync on `stream`
- * and freed with cudaFreeAsync on the same stream; LA_ERR_NO_MEMORY if that
- * fails.
+ * Workspace: the tensor-core kernels, and the CUDA-core kernels when they
+ * cut a sequence into segments (or reduce a non-causal state), need a small
+ * stream-ordered scratch (per-segment states and flags), allocated with
+ * cudaMallocAsync on `stream` and freed with cudaFreeAsync on the same
+ * stream; LA_ERR_NO_MEMORY if that fails.
  */
 la_status la_forward(const void *q, const void *k, const void *v, void *out,
                      int B, int H, int N, int d, int causal,
@@ -108,8 +109,9 @@ la_status la_forward(const void *q, const void *k, const void *v, void *out,
  * measurement.  `path`: 0 = automatic (what la_forward does), 1 = force the
  * fp32 CUDA-core kernels (any dtype), 2 = force the tensor-core kernels
  * (LA_ERR_UNSUPPORTED where they do not apply).  `segment_chunks`: 0 =
- * automatic, else the number of chunks per sequence segment that the
- * tensor-core kernels hand to one CTA (sequence parallelism inside a head).
+ * automatic, else the number of chunks per sequence segment that one CTA
+ * takes (sequence parallelism inside a head; chunks of 128 tokens on the
+ * tensor cores, of 32 on the CUDA cores).
  */
 la_status la_forward_ex(const void *q, const void *k, const void *v,
                         void *out, int B, int H, int N, int d, int causal,
@@ -362,9 +364,10 @@ unsigned long long la_kernel_launch_count(void);
  * reports LA_ERR_TIMEOUT.  LA_ERR_INVALID_ARG for wait_cycles < 4096.
  *
  * la_debug_fail_next_allocs -- the next `n` stream-ordered workspace
- * allocations of the tensor-core launches (made when no workspace is passed)
- * fail: those calls return LA_ERR_NO_MEMORY and enqueue nothing.  n = 0
- * clears the hook; LA_ERR_INVALID_ARG for n < 0.
+ * allocations of the forward kernels (tensor-core launches given no
+ * workspace, and CUDA-core launches over more than one segment per head, or
+ * non-causal) fail: those calls return LA_ERR_NO_MEMORY and enqueue nothing.
+ * n = 0 clears the hook; LA_ERR_INVALID_ARG for n < 0.
  */
 la_status la_debug_inject_timeout(long long wait_cycles, int hold_segment);
 la_status la_debug_fail_next_allocs(int n);

@@ -217,10 +217,14 @@ la_status la::forward_with_workspace(const void *q, const void *k, const void *v
         }
         return LA_OK;
     }
-    cudaError_t e = launch_simt_forward(q, k, v, out, sh, causal, dk, dtype,
-                                        S_out, z_out, gates, s);
-    if (e != cudaSuccess) return cuda_fail(e, "la_forward (CUDA-core kernel)");
-    note_launches(1);
+    int launches = 0;
+    TcResult r = launch_simt_forward(q, k, v, out, sh, causal, dk, dtype, S_out, z_out,
+                                     gates, segment_chunks, s, &launches);
+    note_launches(launches);
+    if (r.status != LA_OK) {
+        if (r.status == LA_ERR_CUDA) return cuda_fail(r.cuda, r.where);
+        return fail(r.status, r.where);
+    }
     return LA_OK;
 }
 

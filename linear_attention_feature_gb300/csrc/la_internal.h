@@ -30,16 +30,6 @@ struct FwdShape {
     long long BH() const { return (long long)B * H; }
 };
 
-// ---- CUDA-core (fp32 FMA) forward: any d in 1..LA_MAX_D, fp32 or bf16 ----
-// S_out / z_out (causal only, may be NULL): the final state [BH][d][d] /
-// [BH][d] in fp32.  gates (causal only, may be NULL): a device [BH][N]
-// scalar gate per token, used instead of the per-head decay.
-cudaError_t launch_simt_forward(const void *q, const void *k, const void *v,
-                                void *out, const FwdShape &sh, int causal,
-                                const DecayArgs &decay, la_dtype dtype,
-                                float *S_out, float *z_out, const float *gates,
-                                cudaStream_t stream);
-
 // ---- delta-rule decode step (S only; beta, alpha device [BH], alpha may
 // be NULL) ----
 cudaError_t launch_delta_step(float *S, const void *q, const void *k,

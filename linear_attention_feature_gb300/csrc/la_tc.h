@@ -31,6 +31,19 @@ TcResult tc_forward(const void *q, const void *k, const void *v, void *out,
                     float *S_out, float *z_out, const float *gates,
                     cudaStream_t stream);
 
+// CUDA-core (fp32 FMA) forward: any d in 1..LA_MAX_D, fp32 or bf16.
+// S_out / z_out (causal only, may be NULL): the final state [BH][d][d] /
+// [BH][d] in fp32.  gates (causal only, may be NULL): a device [BH][N]
+// scalar gate per token, used instead of the per-head decay.
+// `segment_chunks` (chunks of 32 tokens per segment; 0 = automatic) sets the
+// sequence parallelism; more than one segment per head takes a
+// stream-ordered workspace (tc_workspace_alloc).  `launches` receives the
+// number of kernels enqueued.
+TcResult launch_simt_forward(const void *q, const void *k, const void *v, void *out,
+                             const FwdShape &sh, int causal, const DecayArgs &decay,
+                             la_dtype dtype, float *S_out, float *z_out, const float *gates,
+                             int segment_chunks, cudaStream_t stream, int *launches);
+
 // Scratch bytes one tensor-core forward needs on a device with `sms` SMs.
 size_t tc_workspace_bytes(const FwdShape &sh, int causal, bool decay,
                           int segment_chunks, int sms);
