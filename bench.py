@@ -216,10 +216,14 @@ KNOWN_TRAFFIC = {
     # (FORM causal, decay or noncausal; dram__bytes_read.sum +
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
+    ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
+        {"sources": "4a2feea3c70d3b46", "bytes": 1342404608 + 231395072},
+    ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
+        {"sources": "4a2feea3c70d3b46", "bytes": 644021504 + 97349120},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "78d9d80b358cae4a", "bytes": 100798720 + 4932096},
+        {"sources": "f5fdbfe66a4b2ed2", "bytes": 100769280 + 4836864},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
-        {"sources": "8023d72c789a91db", "bytes": 100728320 + 2898688},
+        {"sources": "2cf08a0e48ec3da1", "bytes": 100713472 + 2732544},
 }
 
 

@@ -41,7 +41,7 @@ def test_causal_tc_ragged(d, N):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("seg", [1, 2, 3])
+@pytest.mark.parametrize("seg", [1, 2, 3, 5, 7])
 def test_causal_tc_many_segments(d, seg):
     q, k, v = wl.make_qkv(1, 4, 1500, d, "bf16", seed=seg)
     y = run_tc(q, k, v, seg=seg)
@@ -49,7 +49,7 @@ def test_causal_tc_many_segments(d, seg):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("seg", [1, 4, 0])
+@pytest.mark.parametrize("seg", [1, 4, 0, 5])
 def test_causal_tc_decay(d, seg):
     H = 4
     dec = [0.0, 0.5, 0.96875, 1.0]
