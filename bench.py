@@ -218,8 +218,6 @@ KNOWN_TRAFFIC = {
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
         {"sources": "4a2feea3c70d3b46", "bytes": 1342404608 + 231395072},
-    ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "4a2feea3c70d3b46", "bytes": 644021504 + 97349120},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
         {"sources": "f5fdbfe66a4b2ed2", "bytes": 100769280 + 4836864},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
@@ -473,7 +471,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
              kernel="noncausal_kernel<64>")
     wd = wl.WORKLOADS["bf16_decay_b4h8_n16384_d128"]
     fwd_path("bf16_decay_b4h8_n16384_d128 causal", wd.name, True,
-             decay=list(wd.decay), kernel="causal_wide_kernel<1>")
+             decay=list(wd.decay), kernel="causal_wide_kernel<2>")
     fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
     fwd_path(f"{MID} causal with final state", MID, True, inputs=mid_inputs(),
              state=True)

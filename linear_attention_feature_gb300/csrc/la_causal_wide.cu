@@ -16,6 +16,16 @@
 // [V | 1] ends in a block whose column 0 is one, [S | z] in a block holding
 // z, so numerator and denominator come from the same bf16 operands.
 //
+// Decay modes.  Mode 1 computes P from the unweighted phi(Q), phi(K) and
+// weights the rows in place once P has read them (K rows in shared memory,
+// Q rows in TMEM).  Mode 2, used when every decay is at least 0.77, weights
+// both operands as soon as they are mapped and computes P from them:
+// Qhat_i . Khat_j = g^(i+1) g^(n-1-j) phi(q_i) . phi(k_j), so
+//   Pt_ij = g^-n (Qhat Khat^T)_ij   for j <= i,
+// one factor per chunk, and no product waits for a weighting pass.  The
+// powers involved stay in range for such decays (g^(2C-1) >= 2^-96 in P,
+// g^-C <= 2^49).
+//
 // Memory plan.  TMEM (480 of 512 columns): P (single buffer, Pt written
 // back in place), O | den (144), S | z (144) and phi(Q) (64 columns of bf16
 // pairs: the A operand of P and of Qhat [S | z], so Q needs no shared-memory
@@ -86,6 +96,7 @@ constexpr int OFF_SMALL = OFF_ONES + BLK;  // 224 KB
 // (8 g + u) * 128 + a.
 constexpr int STATE = D * D + D;
 constexpr int kPrefetch = 3;      // L2 prefetch distance in jobs
+constexpr float kFoldMin = 0.77f;  // smallest decay for the folded-weights mode
 // TMEM columns
 constexpr uint32_t TM_P = 0, TM_O = 128, TM_S = 272, TM_Q = 416, TM_COLS = 512;
 
@@ -374,7 +385,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             // its bf16 copy); with decay Khat, Qhat weighted in place
             wait_bar_spin(&sm.sb_ready, nsb & 1, cx);
             ++nsb;
-            if (kMode) wait_bar_spin(&sm.khat_ready, cp, cx);
+            if (kMode == 1) wait_bar_spin(&sm.khat_ready, cp, cx);
             wait_bar_spin(&sm.v_full[st], sp, cx);
             tc_fence_after();
             if (su) {
@@ -471,7 +482,12 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             const int n = min(C, p.N - c * C);
             uint8_t *kt = smem + k_off(st);
             wait_bar(&sm.k_full[st], (j / STAGES) & 1, cx);
-            transform_row<D>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
+            if (kMode == 2) {  // Khat_t = g^(n-1-t) phi(k_t) at once (rows past N -> 0)
+                const float wk = row >= n ? 0.f : gpow(lg, n - 1 - row);
+                transform_row_scaled<D>(kt, row, part, bf2_splat(wk), p.phi);
+            } else {
+                transform_row<D>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
+            }
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xfk[st]);
@@ -480,6 +496,11 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             wait_bar(&sm.q_full, nb & 1, cx);
             uint32_t w[32];
             phi_q_row(smem + OFF_Q, row, part, p.phi != 0, w);
+            if (kMode == 2) {  // Qhat_i = g^(i+1) phi(q_i) at once
+                const uint32_t wq = bf2_splat(gpow(lg, row + 1));
+#pragma unroll
+                for (int e = 0; e < 32; ++e) w[e] = bf2_mul(w[e], wq);
+            }
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.q_empty);
             wait_bar(&sm.q_free, (nb & 1) ^ 1, cx);
@@ -489,7 +510,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             tc_fence_before();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xfq);
-            if (kMode) {
+            if (kMode == 1) {
                 // once P(c) has read the unweighted rows: Khat_t =
                 // g^(n-1-t) phi(k_t) in place, Qhat_i = g^(i+1) phi(q_i) in TMEM
                 wait_bar(&sm.pfull, nb & 1, cx);
@@ -513,10 +534,12 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
 // ---------------------------------------------------------------- score + output
 
 // Causal mask and decay on P (fp32, TMEM), rounded to bf16 in place (the A
-// operand of Pt [V | 1]).  One thread per row (= TMEM lane).
+// operand of Pt [V | 1]).  One thread per row (= TMEM lane).  With the
+// weights folded into both operands (mode 2) P already holds
+// g^(n + i - j) phi(q_i) . phi(k_j), and `gn` = g^-n scales every entry.
 template <int kMode>
 __device__ __forceinline__ void score_chunk(Small &sm, const Ctx &cx, uint32_t lb,
-                                            int q, int lane, float lg, int nb) {
+                                            int q, int lane, float lg, float gn, int nb) {
     const uint32_t tp = lb + TM_P;
     const int row = q * 32 + lane;
     wait_bar(&sm.pfull, nb & 1, cx);
@@ -533,7 +556,11 @@ __device__ __forceinline__ void score_chunk(Small &sm, const Ctx &cx, uint32_t l
             tmem_wait_ld();
             reg_fence(v);
             if (blk < q) {
-                if (kMode) {
+                if (kMode == 2) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2)
+                        pk[e >> 1] = pack_bf16x2(u2f(v[e]) * gn, u2f(v[e + 1]) * gn);
+                } else if (kMode == 1) {
                     // g^(row - j) = g^(row - 32 blk - 31) g^(31 - e)
                     const float base = gpow(lg, row - 32 * blk - 31);
 #pragma unroll
@@ -550,9 +577,14 @@ __device__ __forceinline__ void score_chunk(Small &sm, const Ctx &cx, uint32_t l
                 for (int e = 0; e < 32; e += 2) {
                     // diagonal block: g^(i - j) = g^(lane - e), only where e <= lane
                     float x0 = 0.f, x1 = 0.f;
-                    if (e <= lane) x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
-                    if (e + 1 <= lane)
-                        x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1] : u2f(v[e + 1]);
+                    if (kMode == 2) {
+                        if (e <= lane) x0 = u2f(v[e]) * gn;
+                        if (e + 1 <= lane) x1 = u2f(v[e + 1]) * gn;
+                    } else {
+                        if (e <= lane) x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
+                        if (e + 1 <= lane)
+                            x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1] : u2f(v[e + 1]);
+                    }
                     pk[e >> 1] = pack_bf16x2(x0, x1);
                 }
             }
@@ -620,7 +652,7 @@ __device__ void score_output(uint8_t *smem, Small &sm, const Params &p, const Ct
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
-        if (kMode && et < 32) sm.gtab[et] = gpow(lg, et);
+        if (kMode == 1 && et < 32) sm.gtab[et] = gpow(lg, et);
         // The start state, if every predecessor has already published its
         // local state, summed now (phase A runs meanwhile) into TMEM O (row
         // `row` of S, and z in column D); the state warps take it from there.
@@ -660,7 +692,8 @@ __device__ void score_output(uint8_t *smem, Small &sm, const Params &p, const Ct
         for (int c = it.c0; c < it.c1; ++c, ++nb, ++j) {
             if (c > it.c0)
                 output_chunk(smem, sm, cx, lb, row, et, nb - 1, (j - 1) % STAGES, norm);
-            score_chunk<kMode>(sm, cx, lb, q, lane, lg, nb);
+            const float gn = kMode == 2 ? exp2f(-lg * (float)min(C, p.N - c * C)) : 1.f;
+            score_chunk<kMode>(sm, cx, lb, q, lane, lg, gn, nb);
         }
         output_chunk(smem, sm, cx, lb, row, et, nb - 1, (j - 1) % STAGES, norm);
     }
@@ -1015,7 +1048,13 @@ TcResult launch_wide_with(const void *q, const void *k, const void *v, void *out
     // published states need no clearing
     if ((e = tc_zero_words(ws, pl.off_agg, stream)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: workspace clear"};
-    auto kern = dk.has ? causal_wide_kernel<1> : causal_wide_kernel<0>;
+    // With every decay at least kFoldMin the weights fold into both operands
+    // (mode 2): the largest power in P, g^(2C - 1), stays above 2^-96 and
+    // g^-C below 2^49.
+    bool fold = dk.has != 0;
+    for (int h = 0; fold && h < dk.H; ++h) fold = dk.g[h] >= kFoldMin;
+    auto kern = !dk.has ? causal_wide_kernel<0>
+                        : (fold ? causal_wide_kernel<2> : causal_wide_kernel<1>);
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: kernel attribute"};

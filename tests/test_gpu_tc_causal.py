@@ -62,6 +62,17 @@ def test_causal_tc_decay(d, seg):
                                atol=1e-2)
 
 
+@pytest.mark.parametrize("N", [300, 700])
+@pytest.mark.parametrize("seg", [0, 1, 3])
+def test_causal_tc_decay_folded(N, seg):
+    """d = 128 with every decay >= 0.77 weights Q and K before P is formed
+    and rescales P by g^-n per chunk; decays at the threshold and at 1."""
+    dec = [0.77, 0.8, 0.96875, 1.0]
+    q, k, v = wl.make_qkv(2, 4, N, 128, "bf16", seed=60 + seg)
+    y = run_tc(q, k, v, decay=dec, seg=seg)
+    assert wl.max_row_rel_err(y, oracle.causal(q, k, v, dec, nthreads=8)) <= TOL
+
+
 def test_causal_tc_decay_schedule_long_heads():
     """The decay schedule g_h = 1 - 2^(-5-h) over 8 heads, several segments."""
     dec = list(wl.decay_schedule(8))
@@ -88,7 +99,8 @@ def test_causal_tc_constant_values(d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("decay", [None, [0.96875, 0.5, 0.999, 1.0]])
+@pytest.mark.parametrize("decay", [None, [0.96875, 0.5, 0.999, 1.0],
+                                   [0.96875, 0.8, 0.999, 1.0]])
 def test_causal_tc_repeated_calls_are_bit_identical(d, decay):
     """Every segment's start state is the decayed sum of its predecessors'
     published local states, added in a fixed order, so repeated calls give

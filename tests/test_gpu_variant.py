@@ -70,7 +70,7 @@ def ref_variant(q, k, v, causal, dec, fmap, norm):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [300, 2000])
-@pytest.mark.parametrize("dec", [None, [0.5, 0.9, 0.96875, 1.0]])
+@pytest.mark.parametrize("dec", [None, [0.5, 0.9, 0.96875, 1.0], [0.8, 0.9, 0.96875, 1.0]])
 def test_retention_tensor_cores(d, N, dec):
     q, k, v = (t.cuda() for t in wl.make_qkv(1, 4, N, d, "bf16", seed=80 + N))
     y = la.forward_variant(q, k, v, causal=True, decay=dec,
