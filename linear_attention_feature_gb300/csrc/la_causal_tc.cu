@@ -438,12 +438,35 @@ struct GateSlot {
     float colg[C];
 };
 constexpr float kGateSpan = 100.f;
+// Folded weights: a chunk whose weights all lie in range takes Qhat and
+// Khat as soon as they are mapped, P from them, and one factor per chunk in
+// the score epilogue (see chunk_folds).  Decay: g >= 0.77 (log2 below), so
+// that g^(2C-1) >= 2^-96; gates: no zero gate in the chunk and a product of
+// at least 2^-48, so that every power in P stays above 2^-96.  Only with
+// the elu + 1 feature map: its features are positive, so the bf16 rounding
+// of the weighted rows costs P a relative 2^-8 at most; with the identity
+// map the terms of q . k cancel and that rounding error would not shrink
+// with P.
+constexpr float kFoldLog2 = -0.3770f;  // log2(0.77)
+constexpr float kFoldGateLog2 = -48.f;
 static_assert(sizeof(GateSlot) <= 2048, "GateSlot outgrows its stage slot");
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Whether chunk weights fold into Q and K (mode 1: per head; mode 2: per
+// chunk, from its gate slot), and the factor of P then: Qhat_i . Khat_j =
+// w(i) w'(j) phi(q_i) . phi(k_j) = G prod_{u=j+1..i}, with G = g^n or the
+// chunk's gate product, so Pt = P / G.
+template <int kMode>
+__device__ __forceinline__ bool chunk_folds(float lg, const GateSlot &g, int n, int phi) {
+    if (!phi) return false;
+    if (kMode == 1) return lg >= kFoldLog2;
+    if (kMode == 2) return g.nz[n - 1] == 0 && g.lg2[n - 1] >= kFoldGateLog2;
+    return false;
 }
 
 // prod_{u=j+1..i} alpha_u within a chunk (j < i; j = -1: from the chunk's
@@ -567,19 +590,24 @@ __device__ __forceinline__ void gate_totals(float &L2, int &Z, const Params &p,
 // with gates prod_{u=t+1..n-1} alpha_u and prod_{u<=i} alpha_u.  The
 // inter-chunk read Qhat [S | z] then accumulates onto P~ [V | 1] directly.
 // All transform threads call.
+// A folded chunk was weighted when it was mapped: only the hand-off remains
+// (its wait on P keeps the transform at most one chunk ahead of the MMA
+// issuer's khat_ready waits).
 template <int DK, int kMode>
 __device__ __forceinline__ void weight_qk(uint8_t *smem, Small &sm, const Ctx &cx,
                                           float lg, int st, int n, int nb,
-                                          int row, int part, int et) {
+                                          int row, int part, int et, bool folded) {
     using L = Layout<DK, kMode>;
     wait_bar(&sm.pfull[nb & 1], (nb >> 1) & 1, cx);
-    const GateSlot &g = *reinterpret_cast<const GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
-    const float wk = row >= n ? 0.f
-                              : (kMode == 2 ? gate_prod(g, n - 1, row) : gpow(lg, n - 1 - row));
-    const float wq = kMode == 2 ? gate_prod(g, row, -1) : gpow(lg, row + 1);
-    scale_row<DK>(smem + st * L::STAGE + L::OFF_K, row, part, bf2_splat(wk));
-    scale_row<DK>(smem + st * L::STAGE + L::OFF_Q, row, part, bf2_splat(wq));
-    fence_async_shared();
+    if (!folded) {
+        const GateSlot &g = *reinterpret_cast<const GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
+        const float wk = row >= n ? 0.f
+                                  : (kMode == 2 ? gate_prod(g, n - 1, row) : gpow(lg, n - 1 - row));
+        const float wq = kMode == 2 ? gate_prod(g, row, -1) : gpow(lg, row + 1);
+        scale_row<DK>(smem + st * L::STAGE + L::OFF_K, row, part, bf2_splat(wk));
+        scale_row<DK>(smem + st * L::STAGE + L::OFF_Q, row, part, bf2_splat(wq));
+        fence_async_shared();
+    }
     named_bar_sync(BAR_T, kTThreads);
     if (et == 0) mbar_arrive(&sm.khat_ready[nb & 1]);
 }
@@ -646,6 +674,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         // release would then sit on the path, so it runs at once.
         constexpr bool kPipe = L::STAGES >= 3;
         int pst = -1, pn = 0, pnb = 0;
+        bool pfold = false;
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % L::STAGES;
             const float gcur = gnext;
@@ -656,20 +685,35 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             const int n = min(C, p.N - c * C);
             GateSlot &g = *reinterpret_cast<GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
             if (kMode == 2) gate_scan(g, sm, gcur, et);
-            transform_row<DK>(qt, row, part, false, p.phi);
-            transform_row<DK>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
+            const bool fold = chunk_folds<kMode>(lg, g, n, p.phi);
+            if (fold) {
+                // Qhat and Khat at once (rows past N -> 0)
+                const float wk = row >= n ? 0.f
+                                          : (kMode == 2 ? gate_prod(g, n - 1, row)
+                                                        : gpow(lg, n - 1 - row));
+                const float wq = kMode == 2 ? gate_prod(g, row, -1) : gpow(lg, row + 1);
+                transform_row_scaled<DK>(qt, row, part, bf2_splat(wq), p.phi);
+                transform_row_scaled<DK>(kt, row, part, bf2_splat(wk), p.phi);
+            } else {
+                transform_row<DK>(qt, row, part, false, p.phi);
+                transform_row<DK>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
+            }
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
-            if (kMode && !kPipe) weight_qk<DK, kMode>(smem, sm, cx, lg, st, n, nb, row, part, et);
+            if (kMode && !kPipe)
+                weight_qk<DK, kMode>(smem, sm, cx, lg, st, n, nb, row, part, et, fold);
             if (kMode && kPipe) {
-                if (pst >= 0) weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et);
+                if (pst >= 0)
+                    weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et, pfold);
                 pst = st;
                 pn = n;
                 pnb = nb;
+                pfold = fold;
             }
         }
-        if (kMode && pst >= 0) weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et);
+        if (kMode && pst >= 0)
+            weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et, pfold);
     }
 }
 
@@ -712,6 +756,12 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
                 gl_i = gs.lg2[row];
                 gz_i = gs.nz[row];
             }
+            // folded weights: P holds G x the weighted scores (G = g^n or
+            // the chunk's gate product), so every entry takes 1 / G
+            const int n = min(C, p.N - c * C);
+            const bool fold = chunk_folds<kMode>(lg, gs, n, p.phi);
+            float F = 1.f;
+            if (fold) F = kMode == 2 ? fast_exp2(-gs.lg2[n - 1]) : exp2f(-lg * (float)n);
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t pk[16];
@@ -723,7 +773,14 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
                     tmem_ld32(tp + 32 * blk, v);
                     tmem_wait_ld();
                     reg_fence(v);
-                    if (blk < q) {
+                    if (fold) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const bool in0 = blk < q || e <= lane, in1 = blk < q || e + 1 <= lane;
+                            pk[e >> 1] = pack_bf16x2(in0 ? u2f(v[e]) * F : 0.f,
+                                                     in1 ? u2f(v[e + 1]) * F : 0.f);
+                        }
+                    } else if (blk < q) {
                         if (kMode == 2) {
                             // prod_{u=col+1..row} alpha_u = (prod over
                             // u = e+1..row) colf[col], e the block's last token

@@ -18,7 +18,8 @@
 //
 // Decay modes.  Mode 1 computes P from the unweighted phi(Q), phi(K) and
 // weights the rows in place once P has read them (K rows in shared memory,
-// Q rows in TMEM).  Mode 2, used when every decay is at least 0.77, weights
+// Q rows in TMEM).  Mode 2, used with the elu + 1 map (positive features)
+// when every decay is at least 0.77, weights
 // both operands as soon as they are mapped and computes P from them:
 // Qhat_i . Khat_j = g^(i+1) g^(n-1-j) phi(q_i) . phi(k_j), so
 //   Pt_ij = g^-n (Qhat Khat^T)_ij   for j <= i,
@@ -1050,8 +1051,10 @@ TcResult launch_wide_with(const void *q, const void *k, const void *v, void *out
         return {LA_ERR_CUDA, e, "la_forward: workspace clear"};
     // With every decay at least kFoldMin the weights fold into both operands
     // (mode 2): the largest power in P, g^(2C - 1), stays above 2^-96 and
-    // g^-C below 2^49.
-    bool fold = dk.has != 0;
+    // g^-C below 2^49.  Only with the elu + 1 map: its positive features keep
+    // the rounding of the weighted rows at a relative 2^-8 of P, where the
+    // identity map's cancelling terms would not.
+    bool fold = dk.has != 0 && sh.phi != 0;
     for (int h = 0; fold && h < dk.H; ++h) fold = dk.g[h] >= kFoldMin;
     auto kern = !dk.has ? causal_wide_kernel<0>
                         : (fold ? causal_wide_kernel<2> : causal_wide_kernel<1>);

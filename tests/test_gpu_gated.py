@@ -163,3 +163,24 @@ def test_gated_tiny_gates_exceed_the_factored_range(d):
     la.check_device_status()
     ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy(), nthreads=4)
     assert wl.max_row_rel_err(y.cpu(), ref) <= wl.TOL["bf16"]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_gated_chunks_on_both_sides_of_the_fold_threshold(d):
+    # a chunk whose gate product is at least 2^-48 (and has no zero gate)
+    # takes the weights into Q and K at once; heads 0 and 1 sit just above
+    # and just below that product per 128-token chunk, head 2 mixes both
+    # from chunk to chunk, head 3 has gates in [0.7, 1)
+    N = 900
+    q, k, v = wl.make_qkv(1, 4, N, d, "bf16", seed=220 + d)
+    g = torch.Generator().manual_seed(221 + d)
+    a = torch.empty(1, 4, N)
+    a[0, 0] = 2.0 ** (-47.5 / 128)
+    a[0, 1] = 2.0 ** (-48.5 / 128)
+    a[0, 2] = torch.where((torch.arange(N) // 128) % 2 == 0,
+                          torch.tensor(2.0 ** (-40.0 / 128)), torch.tensor(2.0 ** (-60.0 / 128)))
+    a[0, 3] = 0.7 + 0.3 * torch.rand(N, generator=g)
+    y = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda())
+    la.check_device_status()
+    ref = oracle.causal_gated(q.float(), k.float(), v.float(), a.double().numpy(), nthreads=4)
+    assert wl.max_row_rel_err(y.cpu(), ref) <= wl.TOL["bf16"]

@@ -62,13 +62,15 @@ def test_causal_tc_decay(d, seg):
                                atol=1e-2)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [300, 700])
 @pytest.mark.parametrize("seg", [0, 1, 3])
-def test_causal_tc_decay_folded(N, seg):
-    """d = 128 with every decay >= 0.77 weights Q and K before P is formed
-    and rescales P by g^-n per chunk; decays at the threshold and at 1."""
-    dec = [0.77, 0.8, 0.96875, 1.0]
-    q, k, v = wl.make_qkv(2, 4, N, 128, "bf16", seed=60 + seg)
+def test_causal_tc_decay_folded(d, N, seg):
+    """Decays >= 0.77 weight Q and K before P is formed and rescale P by
+    g^-n per chunk (d = 128: when every head's decay is; d = 64: per head);
+    decays at the threshold, just below it and at 1."""
+    dec = [0.77, 0.7699, 0.96875, 1.0] if d == 64 else [0.77, 0.8, 0.96875, 1.0]
+    q, k, v = wl.make_qkv(2, 4, N, d, "bf16", seed=60 + seg)
     y = run_tc(q, k, v, decay=dec, seg=seg)
     assert wl.max_row_rel_err(y, oracle.causal(q, k, v, dec, nthreads=8)) <= TOL
 
