@@ -67,11 +67,13 @@ def _load():
     lib.ora_causal_state.argtypes = [P, P, P, P, L, L, L, P, I]
     lib.ora_causal_gated.argtypes = [P, P, P, P, P, L, L, L, I, I, I]
     lib.ora_delta_step.argtypes = [P, P, P, P, P, P, P, L, L]
+    lib.ora_delta_forward.argtypes = [P, P, P, P, P, P, P, L, L, L, I]
     lib.ora_decode_step.argtypes = [P, P, P, P, P, P, L, L, P, I]
     lib.ora_quadratic.argtypes = [P, P, P, P, L, L, L, P, I, I, P]
     lib.ora_chunked.argtypes = [P, P, P, P, L, L, L, P, L, L]
     for name in ("ora_noncausal_state", "ora_state_read", "ora_noncausal",
                  "ora_causal_state", "ora_causal_gated", "ora_delta_step",
+                 "ora_delta_forward",
                  "ora_recurrent_step", "ora_causal", "ora_decode_step",
                  "ora_quadratic", "ora_chunked"):
         getattr(lib, name).restype = I
@@ -214,6 +216,28 @@ def delta_step(S, q, k, v, beta, alpha=None):
                                   _ptr(a) if a is not None else None, _ptr(out),
                                   BH, d), "delta_step")
     return out
+
+
+def delta_forward(q, k, v, beta, alpha=None, S0=None, *, nthreads=1):
+    """The delta rule over sequences q, k, v [..., N, d]: token by token
+    S <- alpha_t S + beta_t k_t (v_t - alpha_t S^T k_t)^T (S[a][c], a key
+    feature), o_t = S^T q_t; beta, alpha [..., N] (alpha None: 1); S0
+    [..., d, d] the start state (None: zero).  Returns (out [..., N, d], S
+    after the last token)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    BH, N, d = _seq_shape(q)
+    b = np.ascontiguousarray(np.asarray(beta, dtype=np.float64).reshape(-1))
+    a = None if alpha is None else np.ascontiguousarray(
+        np.asarray(alpha, dtype=np.float64).reshape(-1))
+    if b.size != BH * N or (a is not None and a.size != BH * N):
+        raise ValueError("beta and alpha need one entry per token and head")
+    S = (np.zeros(q.shape[:-2] + (d, d)) if S0 is None
+         else np.array(_f64(S0), dtype=np.float64, order="C", copy=True))
+    out = np.empty_like(q)
+    _check(_load().ora_delta_forward(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(b),
+                                     _ptr(a) if a is not None else None, _ptr(out),
+                                     BH, N, d, int(nthreads)), "delta_forward")
+    return out, S
 
 
 def causal_state(k, v, decay=None, *, fmap=FMAP_ELU1):

@@ -356,6 +356,60 @@ int ora_delta_step(double *S, const double *q, const double *k,
     return 0;
 }
 
+/* The delta rule over whole sequences: the recurrence of ora_delta_step
+ * applied token after token ("Story of Attention - Part 5", section 7: the
+ * write rule S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T
+ * and the read o_t = S_t q_t), with one beta and one alpha per token.
+ * q, k, v, out [BH][N][d]; beta, alpha [BH][N] (alpha NULL: 1); S [BH][d][d]
+ * (S[a][c], a key feature) holds the start state and receives the state
+ * after the last token. */
+typedef struct {
+    double *S;
+    const double *q, *k, *v, *beta, *alpha;
+    double *out;
+    long N, d;
+    int err;
+} dfwd_ctx;
+
+static void dfwd_head(void *arg, long h) {
+    dfwd_ctx *c = (dfwd_ctx *)arg;
+    const long N = c->N, d = c->d;
+    double *S = c->S + h * d * d;
+    double *pred = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!pred) {
+        c->err = -2;
+        return;
+    }
+    for (long t = 0; t < N; ++t) {
+        const double *qt = c->q + (h * N + t) * d, *kt = c->k + (h * N + t) * d,
+                     *vt = c->v + (h * N + t) * d;
+        const double b = c->beta[h * N + t], a = c->alpha ? c->alpha[h * N + t] : 1.0;
+        for (long col = 0; col < d; ++col) {
+            double s = 0.0;
+            for (long r = 0; r < d; ++r) s += S[r * d + col] * kt[r];
+            pred[col] = s; /* S_{t-1} k_t */
+        }
+        for (long r = 0; r < d; ++r)
+            for (long col = 0; col < d; ++col)
+                S[r * d + col] = a * S[r * d + col] + b * kt[r] * (vt[col] - a * pred[col]);
+        for (long col = 0; col < d; ++col) {
+            double s = 0.0;
+            for (long r = 0; r < d; ++r) s += S[r * d + col] * qt[r];
+            c->out[(h * N + t) * d + col] = s; /* S_t q_t */
+        }
+    }
+    free(pred);
+}
+
+int ora_delta_forward(double *S, const double *q, const double *k, const double *v,
+                      const double *beta, const double *alpha, double *out, long BH,
+                      long N, long d, int nthreads) {
+    if (!S || !q || !k || !v || !beta || !out || BH < 0 || N < 0 || d <= 0) return -1;
+    dfwd_ctx c = {S, q, k, v, beta, alpha, out, N, d, 0};
+    for_each_head(dfwd_head, &c, BH, nthreads);
+    return c.err;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Masked parallel (quadratic) form -- the other bracketing of the same
  * product ("Linear Attention: Removing the Softmax Buys Associativity",

@@ -232,6 +232,54 @@ def test_gated_delta_rule_closed_form():
     np.testing.assert_allclose(o, P1 @ q, rtol=1e-13, atol=1e-13)
 
 
+def test_delta_forward_worked_example_as_a_sequence(golden):
+    # the page's single write, as a one-token sequence from the printed state
+    g = golden("deltanet_worked_example.json")
+    k, v = arr(g["k"])[None], arr(g["v"])[None]
+    out, S = oracle.delta_forward(k, k, v, [g["beta"]], S0=arr(g["S_prev"]).T)
+    np.testing.assert_array_equal(S, arr(g["S_next"]).T)
+    np.testing.assert_array_equal(out[0], arr(g["S_next_k"]))
+
+
+def test_delta_forward_stores_orthonormal_keys():
+    # beta = 1, orthonormal keys: each write stores its value without
+    # disturbing the others, so reading with the first key returns its value
+    # at every step (update, then read), and every key reads back its value
+    # at the end
+    rng = np.random.default_rng(62)
+    d = 6
+    K, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    V = rng.standard_normal((d, d))
+    q = np.repeat(K[:1], d, axis=0)
+    out, S = oracle.delta_forward(q, K, V, np.ones(d))
+    np.testing.assert_allclose(out, np.repeat(V[:1], d, axis=0), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(K @ S, V, rtol=1e-12, atol=1e-12)
+    # writing key 0 again with beta = 1 replaces its value
+    w = rng.standard_normal(d)
+    out2, S2 = oracle.delta_forward(K[:1], K[:1], w[None], [1.0], S0=S)
+    np.testing.assert_allclose(out2[0], w, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(K[1:] @ S2, V[1:], rtol=1e-12, atol=1e-12)
+
+
+def test_delta_forward_gate_zero_restarts_and_beta_zero_keeps():
+    rng = np.random.default_rng(63)
+    N, d = 9, 5
+    q, k, v = (rng.standard_normal((N, d)) for _ in range(3))
+    beta = rng.uniform(0.1, 1.0, N)
+    alpha = rng.uniform(0.5, 1.0, N)
+    alpha[4] = 0.0
+    out, S = oracle.delta_forward(q, k, v, beta, alpha)
+    # from a zero gate on, the earlier tokens are forgotten
+    out_tail, S_tail = oracle.delta_forward(q[4:], k[4:], v[4:], beta[4:], alpha[4:])
+    np.testing.assert_allclose(out[4:], out_tail, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(S, S_tail, rtol=1e-13, atol=1e-13)
+    # beta = 0 (no gate) never writes: the start state is read as it is
+    S0 = rng.standard_normal((d, d))
+    out0, S1 = oracle.delta_forward(q, k, v, np.zeros(N), S0=S0)
+    np.testing.assert_array_equal(S1, S0)
+    np.testing.assert_allclose(out0, q @ S0, rtol=1e-13, atol=1e-13)
+
+
 # --------------------------------------------------------------------------
 # data-dependent scalar gate per token (GLA-style; Gated DeltaNet's alpha_t)
 
