@@ -481,6 +481,33 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
     # the same gated problem in fp32 (the CUDA-core kernels)
     fwd_path(f"{MID} gated fp32", MID, True, elem=4, gated=True,
              inputs=tuple(t.float() for t in mid_inputs()))
+
+    # the delta rule over the same sequences (Gated DeltaNet: beta = 0.5,
+    # alpha_h = 1 - 2^(-5-h) for every token, unit-norm keys)
+    name = f"{MID} gated delta rule forward"
+    try:
+        w = wl.WORKLOADS[MID]
+        qq, kk, vv = mid_inputs()
+        kn = (kk.float() / kk.float().norm(dim=-1, keepdim=True)).to(kk.dtype)
+        beta = torch.full((w.B, w.H, w.N), 0.5, device=dev)
+        alpha = torch.tensor(wl.decay_schedule(w.H), dtype=torch.float32, device=dev)
+        alpha = alpha.view(1, w.H, 1).expand(w.B, w.H, w.N).contiguous()
+        oo = torch.empty_like(qq)
+        replay, _ = capture(lambda: la.forward_delta(qq, kn, vv, beta, alpha, out=oo))
+        steps = timed_steps(replay, Kx, Wx, world, flush)
+        la.check_device_status()
+        ms = max_over_ranks(sum(steps) / Kx, world)
+        res[name] = {"tokens_per_s": round(w.B * w.N * world / (ms * 1e-3), 1),
+                     "ms_per_step": round(ms, 4), "steps": Kx,
+                     "roofline": roofline_hbm(forward_bytes(w.B, w.H, w.N, w.d, 2)
+                                              + 8 * w.B * w.H * w.N, ms, peaks["hbm_gbs"]),
+                     "note": "recurrent form on CUDA cores, tokens in order: "
+                             "latency-bound, not HBM-bound"}
+        if keep is not None:
+            keep[name] = {"form": "delta_forward", "qkv": host_copy(qq, kn, vv),
+                          "y": oo.cpu(), "beta": beta.cpu(), "alpha": alpha.cpu()}
+    except Exception as e:  # keep the main line; report the failure
+        res[name] = {"error": f"{type(e).__name__}: {e}"}
     mid.clear()
     try:
         res["decode_b256h32_d128"] = run_decode(la, wl, dev, peaks, world, rank,
@@ -672,6 +699,12 @@ def leg_error(oracle, wl, leg, cores):
     """Max row-relative error of one kept leg against the oracle."""
     import numpy as np
     form = leg["form"]
+    if form == "delta_forward":
+        q, k, v = leg["qkv"]
+        ref, _ = oracle.delta_forward(q.float(), k.float(), v.float(),
+                                      leg["beta"].double().numpy(),
+                                      leg["alpha"].double().numpy(), nthreads=cores)
+        return wl.max_row_rel_err(leg["y"], ref), {}
     if form in ("decode", "delta"):
         qs, ks, vs = leg["q"], leg["k"], leg["v"]
         nh, d = qs.shape[1], qs.shape[2]

@@ -289,6 +289,30 @@ la_status la_decode_step_delta(float *S, const void *q, const void *k,
                                const float *alpha, int B, int H, int d,
                                la_dtype dtype, la_stream_t stream);
 
+/*
+ * la_forward_delta -- the delta rule of la_decode_step_delta over whole
+ * sequences ("Story of Attention - Part 5", section 7): for t = 1..N,
+ *   S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T,
+ *   o_t = S_t q_t,
+ * with one beta and one alpha per token and head.  The pages name a
+ * chunkwise form of this rule but do not give it; this is the recurrent form
+ * on CUDA cores in fp32 (value columns of a head in parallel, tokens in order).
+ *   q, k, v  [B][H][N][d] device, dtype `dtype`, read only.
+ *   out      [B][H][N][d] device, dtype `dtype`, written (o_t).
+ *   beta     DEVICE fp32 [B][H][N]: each token's update strength.
+ *   alpha    DEVICE fp32 [B][H][N]: each token's forget gate, or NULL for
+ *            alpha = 1 (plain DeltaNet).  beta and alpha are not checked.
+ *   S        DEVICE fp32 [B][H][d][d] (S[a][c], a key feature, as in
+ *            la_decode_step_delta) holding the state before the first token;
+ *            it receives the state after the last one, so that
+ *            la_decode_step_delta continues the sequences.  NULL: start from
+ *            zero and return no state.
+ *   B, H, N >= 0 (B*H*N == 0 is a no-op), d in 1..LA_MAX_D.
+ */
+la_status la_forward_delta(const void *q, const void *k, const void *v, void *out,
+                           const float *beta, const float *alpha, float *S, int B,
+                           int H, int N, int d, la_dtype dtype, la_stream_t stream);
+
 /* Size of the fixed device scratch used by la_forward_causal_noalloc. */
 #define LA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -33,7 +33,7 @@ EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_forward_host_workspace_bytes", "la_forward_causal_state",
             "la_decode_step_ex", "la_forward_variant", "la_decode_step_variant",
             "la_forward_gated", "la_decode_step_gated", "la_decode_step_delta",
-            "la_debug_inject_timeout", "la_debug_fail_next_allocs")
+            "la_debug_inject_timeout", "la_debug_fail_next_allocs", "la_forward_delta")
 
 FEATURE_MAPS = {"elu1": 0, "identity": 1}
 
@@ -83,6 +83,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                     ctypes.c_size_t, V]
     lib.la_forward_host_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.la_forward_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.la_forward_delta.argtypes = [V, V, V, V, V, V, V, I, I, I, I, I, V]
     lib.la_debug_inject_timeout.argtypes = [ctypes.c_longlong, I]
     lib.la_debug_fail_next_allocs.argtypes = [I]
     lib.la_check_device_status.argtypes = [V]
@@ -98,7 +99,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
               "la_forward_variant", "la_decode_step_variant",
               "la_forward_gated", "la_decode_step_gated", "la_decode_step_delta",
               "la_debug_inject_timeout", "la_debug_fail_next_allocs",
-              "la_check_device_status", "la_abi_version"):
+              "la_forward_delta", "la_check_device_status", "la_abi_version"):
         getattr(lib, n).restype = I
     if path is None:
         _lib = lib
@@ -281,6 +282,39 @@ def decode_step_delta(S, q, k, v, beta, alpha=None, out=None, *, stream=None):
             ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(beta.data_ptr()),
             ctypes.c_void_p(alpha.data_ptr() if alpha is not None else None),
             B, H, d, _dtype_code(q), _stream_ptr(stream, q.device))
+    _raise_if(st)
+    return out
+
+
+def forward_delta(q, k, v, beta, alpha=None, out=None, S=None, *, stream=None):
+    """The delta rule over sequences q, k, v [B, H, N, d] (DeltaNet; Gated
+    DeltaNet with `alpha`): beta, alpha [B, H, N] fp32 on the GPU, one per
+    token; S [B, H, d, d] fp32 (S[a][c], a key feature) the start state,
+    updated in place to the state after the last token (None: start from
+    zero).  Returns out [B, H, N, d] with o_t = S_t q_t."""
+    torch = _torch()
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    B, H, N, d = q.shape
+    for name, t in (("beta", beta), ("alpha", alpha)):
+        if t is not None and (tuple(t.shape) != (B, H, N) or t.dtype != torch.float32):
+            raise ValueError(f"{name} must be float32 [B, H, N]")
+    if S is not None and (tuple(S.shape) != (B, H, d, d) or S.dtype != torch.float32):
+        raise ValueError("S must be float32 [B, H, d, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_cuda(q, k, v, out, beta, *[t for t in (alpha, S) if t is not None])
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.la_forward_delta(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(beta.data_ptr()),
+            ctypes.c_void_p(alpha.data_ptr() if alpha is not None else None),
+            ctypes.c_void_p(S.data_ptr() if S is not None else None),
+            B, H, N, d, _dtype_code(q), _stream_ptr(stream, q.device))
     _raise_if(st)
     return out
 

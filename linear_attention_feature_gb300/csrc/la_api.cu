@@ -343,6 +343,29 @@ la_status la_decode_step_delta(float *S, const void *q, const void *k,
 }
 
 __attribute__((visibility("default")))
+la_status la_forward_delta(const void *q, const void *k, const void *v, void *out,
+                           const float *beta, const float *alpha, float *S, int B,
+                           int H, int N, int d, la_dtype dtype, la_stream_t stream) {
+    if (B < 0 || H < 0 || N < 0)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_delta: negative B, H or N");
+    if (d < 1 || d > LA_MAX_D)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_delta: d must be in 1..256");
+    if (!valid_dtype(dtype))
+        return fail(LA_ERR_INVALID_ARG, "la_forward_delta: unknown dtype");
+    const long long BH = (long long)B * H;
+    if (BH == 0 || N == 0) return LA_OK;
+    if (!q || !k || !v || !out || !beta)
+        return fail(LA_ERR_INVALID_ARG, "la_forward_delta: null pointer");
+    if (BH > 2147483647LL || (long long)N * d > (1LL << 40))
+        return fail(LA_ERR_UNSUPPORTED, "la_forward_delta: problem too large");
+    cudaError_t e = launch_delta_forward(q, k, v, out, beta, alpha, S, BH, N, d, dtype,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "la_forward_delta");
+    note_launches(1);
+    return LA_OK;
+}
+
+__attribute__((visibility("default")))
 la_status la_decode_step_ex(float *S, float *z, const void *q, const void *k,
                             const void *v, void *out, int B, int H, int d,
                             const float *decay, la_dtype dtype,

@@ -37,6 +37,14 @@ cudaError_t launch_delta_step(float *S, const void *q, const void *k,
                               const float *alpha, long long BH, int d,
                               la_dtype dtype, cudaStream_t stream);
 
+// ---- delta rule over whole sequences (beta, alpha device [BH][N], alpha may
+// be NULL; S device [BH][d][d] start and final state, or NULL for a zero
+// start) ----
+cudaError_t launch_delta_forward(const void *q, const void *k, const void *v, void *out,
+                                 const float *beta, const float *alpha, float *S,
+                                 long long BH, int N, int d, la_dtype dtype,
+                                 cudaStream_t stream);
+
 // ---- recurrent decode step ----
 // phi / norm as in FwdShape; gates (may be NULL): a device [BH] gate per
 // head for this step, used instead of the per-head decay.
