@@ -217,9 +217,11 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "4a2feea3c70d3b46", "bytes": 1342404608 + 231395072},
+        {"sources": "e54785596fcc6232", "bytes": 1341360384 + 231457280},
+    ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
+        {"sources": "e54785596fcc6232", "bytes": 643134720 + 96060672},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "f5fdbfe66a4b2ed2", "bytes": 100769280 + 4836864},
+        {"sources": "4a9054efd993e1d6", "bytes": 100766208 + 4866048},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
         {"sources": "2cf08a0e48ec3da1", "bytes": 100713472 + 2732544},
 }
