@@ -18,7 +18,10 @@
 // warp shuffles, and a token needs no block-wide barrier.  The read of token
 // t and the prediction for token t + 1 share one pass over the registers.
 // Tokens are staged in shared memory 32 at a time, and the outputs leave
-// through a staged tile.
+// through a staged tile.  Where rows are whole 16-byte vectors, the next
+// chunk's q, k, v, beta and alpha are copied in with cp.async while the
+// current chunk runs (double buffered, converted to fp32 in shared memory
+// when their turn comes); otherwise each chunk is loaded when it is needed.
 #include <cuda_bf16.h>
 
 #include "la_internal.h"
@@ -46,6 +49,28 @@ __device__ __forceinline__ float sum_rows(float x) {
     return x;
 }
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (unsigned)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     (unsigned)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 // Shared-memory floats of one CTA: k and q rows (8 row groups of R features,
 // each padded to R + 4 so that the row groups' 16-byte reads fall in
 // distinct banks), v and the outputs of this block's W columns, beta, alpha.
@@ -53,8 +78,13 @@ __host__ __device__ constexpr int delta_row(int R) { return 8 * (R + 4); }
 __host__ __device__ constexpr int delta_smem_floats(int R, int W) {
     return 2 * kT * delta_row(R) + 2 * kT * W + 2 * kT;
 }
+// With asynchronous staging, two raw chunks (k, q rows of d elements, v of
+// W columns, in the input type) and two raw beta / alpha rows follow.
+__host__ __device__ constexpr size_t delta_raw_elems(int d, int W) {
+    return (size_t)kT * (2 * d + W);
+}
 
-template <typename T, int R>
+template <typename T, int R, bool kAsync>
 __global__ void __launch_bounds__(256, 1)
 delta_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
                      const T *__restrict__ v, T *__restrict__ out,
@@ -68,6 +98,10 @@ delta_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
     float *ob = vb + kT * W;                         // [kT][W]
     float *bb = ob + kT * W;                         // [kT]
     float *ab = bb + kT;                             // [kT]
+    // asynchronous staging: raw chunk buffers b = 0, 1, then beta / alpha
+    T *raw = reinterpret_cast<T *>(ab + kT);
+    const size_t RAW = delta_raw_elems(d, W);
+    float *fraw = reinterpret_cast<float *>(raw + 2 * RAW);  // [2][2][kT]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long bh = blockIdx.x / nsplit;
@@ -86,8 +120,61 @@ delta_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
             s[i][jj] = (S && a < d && c < d) ? S[((size_t)bh * d + a) * d + c] : 0.f;
         }
 
+    constexpr int VE = 16 / (int)sizeof(T);  // elements per 16-byte copy
+    // issue the copies of chunk c into raw buffer b (asynchronous staging)
+    auto stage = [&](int c, int b) {
+        const int s0 = c * kT, m = min(kT, N - s0);
+        T *kr = raw + b * RAW, *qr = kr + kT * d, *vr = qr + kT * d;
+        const int nvr = d / VE, nvw = W / VE;
+        for (int i = tid; i < m * nvr; i += blockDim.x) {
+            const int t = i / nvr, e = (i - t * nvr) * VE;
+            const size_t off = base + (size_t)(s0 + t) * d + e;
+            cp_async16(kr + t * d + e, k + off);
+            cp_async16(qr + t * d + e, q + off);
+        }
+        for (int i = tid; i < m * nvw; i += blockDim.x) {
+            const int t = i / nvw, e = (i - t * nvw) * VE;
+            if (c0 + e < d) cp_async16(vr + t * W + e, v + base + (size_t)(s0 + t) * d + c0 + e);
+        }
+        for (int i = tid; i < m; i += blockDim.x) {
+            const size_t g = (size_t)bh * N + s0 + i;
+            cp_async4(fraw + (2 * b) * kT + i, beta + g);
+            if (alpha) cp_async4(fraw + (2 * b + 1) * kT + i, alpha + g);
+        }
+        cp_async_commit();
+    };
+    const int nchunk = (N + kT - 1) / kT;
+    if (kAsync) stage(0, 0);
+
     for (int t0 = 0; t0 < N; t0 += kT) {
         const int n = min(kT, N - t0);
+        if (kAsync) {
+            // the next chunk's copies go out first; this chunk's have landed
+            const int c = t0 / kT, b = c & 1;
+            if (c + 1 < nchunk) {
+                stage(c + 1, b ^ 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
+            const T *kr = raw + b * RAW, *qr = kr + kT * d, *vr = qr + kT * d;
+            for (int i = tid; i < n * 8 * R; i += blockDim.x) {
+                const int t = i / (8 * R), a = i - t * 8 * R;
+                const int slot = t * DP + (a / R) * RP + a % R;
+                kb[slot] = a < d ? to_f(kr[t * d + a]) : 0.f;
+                qb[slot] = a < d ? to_f(qr[t * d + a]) : 0.f;
+            }
+            for (int i = tid; i < n * W; i += blockDim.x) {
+                const int t = i / W, cc = i - t * W;
+                vb[i] = c0 + cc < d ? to_f(vr[t * W + cc]) : 0.f;
+            }
+            if (tid < n) {
+                bb[tid] = fraw[(2 * b) * kT + tid];
+                ab[tid] = alpha ? fraw[(2 * b + 1) * kT + tid] : 1.f;
+            }
+            __syncthreads();
+        } else {
         // stage the chunk: k and q (every feature, zero past d), v of this
         // block's columns, beta and alpha
         for (int i = tid; i < kT * 8 * R; i += blockDim.x) {
@@ -112,6 +199,7 @@ delta_forward_kernel(const T *__restrict__ q, const T *__restrict__ k,
             ab[tid] = tid < n && alpha ? alpha[g] : 1.f;
         }
         __syncthreads();
+        }
 
         // the prediction S_{t-1} k_t for the chunk's first token
         float pred[4] = {0.f, 0.f, 0.f, 0.f};
@@ -197,8 +285,17 @@ template <typename T, int R>
 cudaError_t launch_r(const void *q, const void *k, const void *v, void *out,
                      const float *beta, const float *alpha, float *S, long long BH,
                      int N, int d, int W, int nsplit, cudaStream_t stream) {
-    const size_t smem = sizeof(float) * (size_t)delta_smem_floats(R, W);
-    auto kern = delta_forward_kernel<T, R>;
+    // asynchronous staging needs whole 16-byte rows of q, k, v and room for
+    // two raw chunks
+    constexpr int VE = 16 / (int)sizeof(T);
+    const size_t base_bytes = sizeof(float) * (size_t)delta_smem_floats(R, W);
+    const size_t async_bytes = base_bytes + 2 * sizeof(T) * delta_raw_elems(d, W) +
+                               sizeof(float) * 4 * kT;
+    const bool async = d % VE == 0 && async_bytes <= 220 * 1024 &&
+                       (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v)) % 16 == 0;
+    const size_t smem = async ? async_bytes : base_bytes;
+    auto kern = async ? delta_forward_kernel<T, R, true> : delta_forward_kernel<T, R, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
