@@ -98,3 +98,26 @@ def test_noalloc_rejects_what_it_cannot_run(lib):
     # 5M heads: even the per-item flags exceed the 16 MiB scratch
     assert noalloc(lib, big, big.clone(), big.clone(), big_out) == 2
     assert "more workspace" in lib.la_last_error().decode()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_noalloc_makes_no_workspace_allocation(lib, d):
+    # with the next workspace allocation set to fail, an allocating call
+    # would return LA_ERR_NO_MEMORY; the allocation-free call succeeds and
+    # leaves the hook armed, which the ordinary call after it then consumes
+    lib.la_debug_fail_next_allocs.argtypes = [ctypes.c_int]
+    lib.la_debug_fail_next_allocs.restype = ctypes.c_int
+    q, k, v = (t.cuda() for t in wl.make_qkv(1, 4, 1300, d, "bf16", seed=21))
+    out = torch.empty_like(q)
+    assert lib.la_debug_fail_next_allocs(1) == 0
+    try:
+        assert noalloc(lib, q, k, v, out) == 0, lib.la_last_error().decode()
+        la.check_device_status()
+        with pytest.raises(la.LinAttnError) as ei:
+            la.forward(q, k, v, causal=True)
+        assert ei.value.status == 4
+    finally:
+        lib.la_debug_fail_next_allocs(0)
+    ref = la.forward(q, k, v, causal=True)
+    la.check_device_status()
+    assert wl.max_row_rel_err(out.cpu(), ref.cpu()) <= TOL
