@@ -56,7 +56,8 @@ size_t tc_workspace_bytes(const FwdShape &sh, int causal, bool decay,
 // back until they finish.
 cudaError_t tc_zero_words(void *p, size_t bytes, cudaStream_t stream);
 
-// Stream-ordered workspace allocation of the tensor-core launches
+// Stream-ordered workspace allocation of the forward launches (tensor-core
+// kernels, and the CUDA-core kernels when they cut sequences into segments)
 // (cudaMallocAsync), which the allocation-failure test hook can make fail.
 cudaError_t tc_workspace_alloc(void **ws, size_t bytes, cudaStream_t stream);
 
