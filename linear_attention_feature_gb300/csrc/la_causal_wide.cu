@@ -19,13 +19,13 @@
 // Decay modes.  Mode 1 computes P from the unweighted phi(Q), phi(K) and
 // weights the rows in place once P has read them (K rows in shared memory,
 // Q rows in TMEM).  Mode 2, used with the elu + 1 map (positive features)
-// when every decay is at least 0.77, weights
-// both operands as soon as they are mapped and computes P from them:
-// Qhat_i . Khat_j = g^(i+1) g^(n-1-j) phi(q_i) . phi(k_j), so
-//   Pt_ij = g^-n (Qhat Khat^T)_ij   for j <= i,
-// one factor per chunk, and no product waits for a weighting pass.  The
-// powers involved stay in range for such decays (g^(2C-1) >= 2^-96 in P,
-// g^-C <= 2^49).
+// when every decay is at least 0.77, weights both operands as soon as they
+// are mapped: Khat_j = g^(n-1-j) phi(k_j) and Q'_i = g^(i+1-n) phi(q_i), so
+// that P = Q' Khat^T is already g^(i-j) phi(q_i) . phi(k_j) (only the mask
+// remains), while the bf16 state operand carries g^n: Q' (g^n [S | z]) =
+// Qhat [S | z].  No product waits for a weighting pass, and the powers stay
+// in range for such decays (g^-(C-1) <= 2^48 in Q', P's masked entries up
+// to g^-(C-1) times a score).
 //
 // Memory plan.  TMEM (480 of 512 columns): P (single buffer, Pt written
 // back in place), O | den (144), S | z (144) and phi(Q) (64 columns of bf16
@@ -497,8 +497,8 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             wait_bar(&sm.q_full, nb & 1, cx);
             uint32_t w[32];
             phi_q_row(smem + OFF_Q, row, part, p.phi != 0, w);
-            if (kMode == 2) {  // Qhat_i = g^(i+1) phi(q_i) at once
-                const uint32_t wq = bf2_splat(gpow(lg, row + 1));
+            if (kMode == 2) {  // Q'_i = g^(i+1-n) phi(q_i) at once
+                const uint32_t wq = bf2_splat(gpow(lg, row + 1 - n));
 #pragma unroll
                 for (int e = 0; e < 32; ++e) w[e] = bf2_mul(w[e], wq);
             }
@@ -537,10 +537,10 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
 // Causal mask and decay on P (fp32, TMEM), rounded to bf16 in place (the A
 // operand of Pt [V | 1]).  One thread per row (= TMEM lane).  With the
 // weights folded into both operands (mode 2) P already holds
-// g^(n + i - j) phi(q_i) . phi(k_j), and `gn` = g^-n scales every entry.
+// g^(i - j) phi(q_i) . phi(k_j): only the mask remains.
 template <int kMode>
 __device__ __forceinline__ void score_chunk(Small &sm, const Ctx &cx, uint32_t lb,
-                                            int q, int lane, float lg, float gn, int nb) {
+                                            int q, int lane, float lg, int nb) {
     const uint32_t tp = lb + TM_P;
     const int row = q * 32 + lane;
     wait_bar(&sm.pfull, nb & 1, cx);
@@ -557,11 +557,7 @@ __device__ __forceinline__ void score_chunk(Small &sm, const Ctx &cx, uint32_t l
             tmem_wait_ld();
             reg_fence(v);
             if (blk < q) {
-                if (kMode == 2) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2)
-                        pk[e >> 1] = pack_bf16x2(u2f(v[e]) * gn, u2f(v[e + 1]) * gn);
-                } else if (kMode == 1) {
+                if (kMode == 1) {
                     // g^(row - j) = g^(row - 32 blk - 31) g^(31 - e)
                     const float base = gpow(lg, row - 32 * blk - 31);
 #pragma unroll
@@ -578,14 +574,9 @@ __device__ __forceinline__ void score_chunk(Small &sm, const Ctx &cx, uint32_t l
                 for (int e = 0; e < 32; e += 2) {
                     // diagonal block: g^(i - j) = g^(lane - e), only where e <= lane
                     float x0 = 0.f, x1 = 0.f;
-                    if (kMode == 2) {
-                        if (e <= lane) x0 = u2f(v[e]) * gn;
-                        if (e + 1 <= lane) x1 = u2f(v[e + 1]) * gn;
-                    } else {
-                        if (e <= lane) x0 = kMode ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
-                        if (e + 1 <= lane)
-                            x1 = kMode ? u2f(v[e + 1]) * sm.gtab[lane - e - 1] : u2f(v[e + 1]);
-                    }
+                    if (e <= lane) x0 = kMode == 1 ? u2f(v[e]) * sm.gtab[lane - e] : u2f(v[e]);
+                    if (e + 1 <= lane)
+                        x1 = kMode == 1 ? u2f(v[e + 1]) * sm.gtab[lane - e - 1] : u2f(v[e + 1]);
                     pk[e >> 1] = pack_bf16x2(x0, x1);
                 }
             }
@@ -693,8 +684,7 @@ __device__ void score_output(uint8_t *smem, Small &sm, const Params &p, const Ct
         for (int c = it.c0; c < it.c1; ++c, ++nb, ++j) {
             if (c > it.c0)
                 output_chunk(smem, sm, cx, lb, row, et, nb - 1, (j - 1) % STAGES, norm);
-            const float gn = kMode == 2 ? exp2f(-lg * (float)min(C, p.N - c * C)) : 1.f;
-            score_chunk<kMode>(sm, cx, lb, q, lane, lg, gn, nb);
+            score_chunk<kMode>(sm, cx, lb, q, lane, lg, nb);
         }
         output_chunk(smem, sm, cx, lb, row, et, nb - 1, (j - 1) % STAGES, norm);
     }
@@ -810,11 +800,18 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
                 start_sum(p, it.bh, it.seg, a, g, gL, pv);
             }
             if (g == 4) {
-                store_zb(sb, a, pv[0]);
+                store_zb(sb, a, kMode == 2 ? f0 * pv[0] : pv[0]);
                 tmem_put_z(lb + TM_S + D, f0 * pv[0]);
                 continue;
             }
-            store_sb32(sb, a, g, pv);
+            if (kMode == 2) {  // the operand carries g^n (see the feature map)
+                float ps[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ps[e] = f0 * pv[e];
+                store_sb32(sb, a, g, ps);
+            } else {
+                store_sb32(sb, a, g, pv);
+            }
             // phase-B start: TMEM S = g^n0 S_start
             uint32_t w[32];
 #pragma unroll
@@ -843,18 +840,21 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
                     reg_fence(v);
                     float x[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = u2f(v[e]);
+                    for (int e = 0; e < 32; ++e) x[e] = kMode == 2 ? f * u2f(v[e]) : u2f(v[e]);
                     store_sb32(sb, a, g, x);
-                    if (kMode) {
+                    if (kMode == 1) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f * x[e]);
-                        tmem_st32(lb + TM_S + 32 * g, v);
+                    } else if (kMode == 2) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(x[e]);
                     }
+                    if (kMode) tmem_st32(lb + TM_S + 32 * g, v);
                 }
                 uint32_t zr = tmem_ld1(lb + TM_S + D);
                 tmem_wait_ld();
                 reg_fence(zr);
-                store_zb(sb, a, u2f(zr));
+                store_zb(sb, a, kMode == 2 ? f * u2f(zr) : u2f(zr));
                 if (kMode) {
                     tmem_put_z(lb + TM_S + D, f * u2f(zr));
                     tmem_wait_st();
