@@ -217,9 +217,9 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "e54785596fcc6232", "bytes": 1341360384 + 231457280},
+        {"sources": "7b690a320f563586", "bytes": 1344817664 + 231275776},
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "e54785596fcc6232", "bytes": 643134720 + 96060672},
+        {"sources": "7b690a320f563586", "bytes": 650430976 + 96073984},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
         {"sources": "4a9054efd993e1d6", "bytes": 100766208 + 4866048},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
