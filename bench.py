@@ -13,7 +13,9 @@ under "paths".  Rank 0 prints one JSON line.
 Timing: each step is captured once in a CUDA graph (so that host-side
 launch work does not sit between the events); W untimed warm-up replays, then
 K replays, each bracketed by CUDA events on the stream the library launches
-on, with a 256 MiB write between steps to flush L2; barrier + synchronize on
+on, with L2 flushed between steps (a 256 MiB buffer written, then another
+256 MiB read, so that the flush leaves no dirty lines whose write-back would
+fall inside the next timed step); barrier + synchronize on
 both sides of the timed region; the max over ranks is taken.  `value` = tokens (B*N per step, summed over ranks) per
 second.  `e2e` repeats the main step through the C ABI with pinned host
 buffers, the host->device copies of q, k, v and the device->host copy of the
@@ -309,9 +311,15 @@ def run_ours(args):
     K, W = args.steps, args.warmup
     dev = torch.device("cuda", torch.cuda.current_device())
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_acc = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush():
+        # Written, the buffer evicts every line the step used; the read of a
+        # second buffer then writes the first one's dirty lines back before
+        # the next step starts (else about 100 MB of write-back lands in it).
         flush_buf.zero_()
+        torch.sum(flush_rd, dim=0, out=flush_acc)
 
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
@@ -385,7 +393,8 @@ def run_ours(args):
                        "N": w.N, "d": w.d, "global_batch": w.B * world,
                        "seq_len": w.N, "parallelism": f"replicas{world}",
                        "inputs": "N(0,1)/sqrt(d), bf16, seed=rank",
-                       "l2": "flushed between timed steps (256 MiB write)"},
+                       "l2": "flushed between timed steps (256 MiB written, "
+                             "then another 256 MiB read)"},
             "roofline": roof, "tensor": tens, "chunk": C,
             "max_rel_err": errs.get("main"), "tolerance": wl.TOL["bf16"],
             "e2e": e2e, "gpu_launches": launches,
