@@ -219,13 +219,13 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "7b690a320f563586", "bytes": 1344817664 + 231275776},
+        {"sources": "455081baf3d5de00", "bytes": 1399536384 + 232814592},
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "7b690a320f563586", "bytes": 650430976 + 96073984},
+        {"sources": "455081baf3d5de00", "bytes": 664609280 + 98148608},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "4a9054efd993e1d6", "bytes": 100766208 + 4866048},
+        {"sources": "6448d94c44ffe7ac", "bytes": 100792064 + 5699328},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
-        {"sources": "2cf08a0e48ec3da1", "bytes": 100713472 + 2732544},
+        {"sources": "dbac54d2b2bcf2fd", "bytes": 100719104 + 3564800},
 }
 
 

@@ -445,6 +445,15 @@ __device__ __forceinline__ void phi_q_row(const uint8_t *tile, int row, int part
     }
 }
 
+// phi(K) times w on this thread's half of a K row, in place; one copy of
+// the code for every call site (the feature map's warps share their
+// instruction cache with the MMA issuer and the epilogues).  w = 1 leaves
+// phi(K) exact; w = 0 zeroes the rows past the sequence end.
+static __device__ __noinline__ void feature_k_row(uint8_t *kt, int row, int part,
+                                                  uint32_t w2, bool phi) {
+    transform_row_scaled<D>(kt, row, part, w2, phi);
+}
+
 template <int kMode>
 __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                           const Ctx &cx, const DecayArgs &dk, uint32_t tmem) {
@@ -469,9 +478,9 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                 const int tok = c * C + row;
                 if (kMode || tok >= p.N) {
                     const float w = tok < p.N ? gpow(lg, seg_end - 1 - tok) : 0.f;
-                    transform_row_scaled<D>(kt, row, part, bf2_splat(w), p.phi);
+                    feature_k_row(kt, row, part, bf2_splat(w), p.phi != 0);
                 } else {
-                    transform_row<D>(kt, row, part, false, p.phi);
+                    feature_k_row(kt, row, part, kBf16One2, p.phi != 0);
                 }
                 fence_async_shared();
                 named_bar_sync(BAR_T, kTThreads);
@@ -485,9 +494,10 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             wait_bar(&sm.k_full[st], (j / STAGES) & 1, cx);
             if (kMode == 2) {  // Khat_t = g^(n-1-t) phi(k_t) at once (rows past N -> 0)
                 const float wk = row >= n ? 0.f : gpow(lg, n - 1 - row);
-                transform_row_scaled<D>(kt, row, part, bf2_splat(wk), p.phi);
+                feature_k_row(kt, row, part, bf2_splat(wk), p.phi != 0);
             } else {
-                transform_row<D>(kt, row, part, row >= n, p.phi);  // rows past N -> 0
+                // rows past N -> 0
+                feature_k_row(kt, row, part, row >= n ? 0u : kBf16One2, p.phi != 0);
             }
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
@@ -545,7 +555,7 @@ __device__ __forceinline__ void score_chunk(Small &sm, const Ctx &cx, uint32_t l
     const int row = q * 32 + lane;
     wait_bar(&sm.pfull, nb & 1, cx);
     tc_fence_after();
-#pragma unroll
+#pragma unroll 1
     for (int blk = 0; blk < 4; ++blk) {
         uint32_t pk[16];
         if (blk > q) {
@@ -606,7 +616,7 @@ __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm, const Ctx
         inv = 1.f / u2f(dr);
     }
     uint8_t *vs = smem + v_off(st);
-#pragma unroll
+#pragma unroll 1
     for (int g = 0; g < 4; ++g) {
         uint32_t o[32];
         tmem_ld32(lb + TM_O + 32 * g, o);

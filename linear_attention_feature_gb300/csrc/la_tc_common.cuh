@@ -37,8 +37,8 @@ __device__ __forceinline__ void raise_timeout(const Ctx &cx, uint32_t where) {
 // the first of those checks.
 constexpr uint32_t kSuspendNs = 64;
 
-__device__ __forceinline__ bool wait_bar_poll(uint64_t *bar, uint32_t parity,
-                                              const Ctx &cx, bool spin) {
+static __device__ __noinline__ bool wait_bar_poll(uint64_t *bar, uint32_t parity,
+                                                  const Ctx &cx, bool spin) {
     long long dl = 0;
     for (int n = 1;; ++n) {
         if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait_ns(bar, parity, kSuspendNs))
@@ -79,11 +79,15 @@ __device__ __forceinline__ bool wait_bar_spin(uint64_t *bar, uint32_t parity,
 // shared memory and TMEM are released.
 constexpr long long kSettleCycles = 1LL << 34;
 
-__device__ __forceinline__ void settle_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_test_wait(bar, parity)) return;
+static __device__ __noinline__ void settle_wait_poll(uint64_t *bar, uint32_t parity) {
     const long long dl = clock64() + kSettleCycles;
     while (!mbar_try_wait_ns(bar, parity, kSuspendNs) && clock64() <= dl) {
     }
+}
+
+__device__ __forceinline__ void settle_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return;
+    settle_wait_poll(bar, parity);
 }
 
 // Reads a published-state flag (acquire, device scope).
