@@ -219,9 +219,9 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "455081baf3d5de00", "bytes": 1399536384 + 232814592},
+        {"sources": "91c7d553a111171c", "bytes": 1182873600 + 218743296},
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "455081baf3d5de00", "bytes": 664609280 + 98148608},
+        {"sources": "91c7d553a111171c", "bytes": 577628416 + 83308032},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
         {"sources": "6448d94c44ffe7ac", "bytes": 100792064 + 5699328},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):

@@ -96,7 +96,7 @@ constexpr int OFF_SMALL = OFF_ONES + BLK;  // 224 KB
 // number u of the 32-column group g of row a sits at float4 index
 // (8 g + u) * 128 + a.
 constexpr int STATE = D * D + D;
-constexpr int kPrefetch = 3;      // L2 prefetch distance in jobs
+constexpr int kPrefetch = 1;      // phase-A L2 prefetch distance in jobs
 constexpr float kFoldMin = 0.77f;  // smallest decay for the folded-weights mode
 // TMEM columns
 constexpr uint32_t TM_P = 0, TM_O = 128, TM_S = 272, TM_Q = 416, TM_COLS = 512;
@@ -223,7 +223,9 @@ __device__ __forceinline__ void start_sum(const Params &p, int bh, int seg, int 
 // ---------------------------------------------------------------- producer
 
 // One job per chunk: phase A jobs load K and V (kept in L2 for phase B),
-// phase B jobs load K, Q and V.  Tiles kPrefetch jobs ahead go to L2 first.
+// phase B jobs load K, Q and V.  Phase A's tiles go to L2 kPrefetch jobs
+// ahead.  Phase B's are not prefetched: with every SM streaming, prefetched
+// lines were evicted before their loads came, and read twice.
 // A V slot that a phase-B chunk used holds that chunk's output once the
 // output epilogue releases it: the producer writes it out (two TMA stores)
 // and waits until they have read the slot before it loads into it again.
@@ -238,8 +240,7 @@ __device__ __forceinline__ void store_staged(uint8_t *smem, const CUtensorMap *t
 __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &cx,
                          const CUtensorMap *tq, const CUtensorMap *tk,
                          const CUtensorMap *tv, const CUtensorMap *to) {
-    const uint64_t keep = policy_evict_last(), stream = policy_evict_first(),
-                   normal = policy_evict_normal();
+    const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
     int j = 0, jk = 0, nq = 0, tl = 0;
     // per V slot: the output chunk and head staged there (-1: none)
     int out_c[STAGES] = {-1, -1}, out_bh[STAGES] = {0, 0};
@@ -260,10 +261,11 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
             if (x < nJ) {  // prefetch of job x, then the loads of job x - kPrefetch
                 const int pass = x < nA ? 0 : 1;
                 const int c = it.c0 + (pass == 0 ? x : x - nA);
-                for (int kb = 0; kb < 2; ++kb) {
-                    if (pass == 1) tma_prefetch_3d(tq, 64 * kb, c * C, it.bh, normal);
-                    tma_prefetch_3d(tk, 64 * kb, c * C, it.bh, pass == 0 ? keep : normal);
-                    tma_prefetch_3d(tv, 64 * kb, c * C, it.bh, pass == 0 ? keep : normal);
+                if (pass == 0) {
+                    for (int kb = 0; kb < 2; ++kb) {
+                        tma_prefetch_3d(tk, 64 * kb, c * C, it.bh, keep);
+                        tma_prefetch_3d(tv, 64 * kb, c * C, it.bh, keep);
+                    }
                 }
             }
             const int y = x - kPrefetch;
