@@ -223,7 +223,7 @@ KNOWN_TRAFFIC = {
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
         {"sources": "91c7d553a111171c", "bytes": 577628416 + 83308032},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "6448d94c44ffe7ac", "bytes": 100792064 + 5699328},
+        {"sources": "86beacb004dd8e61", "bytes": 100760832 + 5021696},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
         {"sources": "dbac54d2b2bcf2fd", "bytes": 100719104 + 3564800},
 }

@@ -27,17 +27,22 @@
 // other d = 128 modes run in la_causal_wide.cu.
 //
 // Sequence parallelism inside a head: a head's chunks are cut into segments
-// of `seg_chunks` chunks, and the value dimension into halves of 64 columns
-// (d = 128 gives two halves, each with all 128 key features).  A work item
-// is (head, segment, half); persistent CTAs take items from a ticket counter
-// (so a CTA only ever waits on items held by running CTAs).  A segment that
-// has successors first reduces its local decayed state (phase A:
-// Khat^T [V | 1] only, Khat_t = g^(L-1-t) phi(k_t) relative to its end) and
-// publishes it at once.  Its start state is the decayed sum of all its
-// predecessors' local states, nearest first -- a fixed order, so repeated
-// calls are bit-identical -- and then it runs the chunk loop (phase B).
-// The phase-B re-read of K and V normally hits L2 (phase A loads them with
-// evict-last).
+// (segment 0 of `seg0` chunks, the others of `seg_chunks`), and the value
+// dimension into halves of 64 columns (d = 128 gives two halves, each with
+// all 128 key features).  A work item is (head, segment, half); persistent
+// CTAs take items from a ticket counter (so a CTA only ever waits on items
+// held by running CTAs).  Segment 0 starts from the zero state and runs the
+// chunk loop (phase B) at once.  A later segment s first reduces its
+// predecessor's chunks to that segment's local decayed state (phase A:
+// Khat^T [V | 1] only, Khat_t = g^(L-1-t) phi(k_t) relative to the end of
+// that range, which is its own start); it keeps that state in TMEM as the
+// first term of its start state and publishes it when a later segment
+// needs it.  The other terms are the states published by segments
+// 1 .. s-1 (the local states of segments s-2 .. 0), decayed and added
+// nearest first -- a fixed order, so repeated calls are bit-identical.
+// A segment's phase B and its successor's phase A read the same K and V
+// tiles from the start of the launch, so the later read often finds them in
+// L2 (phase A loads them with evict-last).
 //
 // Warp roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-9 feature-map transform, warps 10-13 score epilogue (mask,
@@ -82,6 +87,7 @@ constexpr int NX = DV + 16;  // extended N of the wide products
 
 struct Params {
     int BH, H, N, nchunks, seg_chunks, nseg, nhalf, items;
+    int seg0;           // chunks of segment 0 (later segments: seg_chunks)
     float *agg;         // [items][DK * DV + DK]: S rows (a-major), then z
     int *flags;         // [items]
     float *S_out, *z_out;  // final state [BH][DK][DK] / [BH][DK], or NULL
@@ -144,9 +150,16 @@ struct Small {
     uint32_t tmem_base;
 };
 
+// A work item: segment `seg` of head `bh` (value-column half `half`),
+// chunks [c0, c1).  Segment 0 spans seg0 chunks, later ones seg_chunks.
+// Phase A of segment s >= 1 reduces its predecessor's chunks [a0, a1 = c0)
+// to that segment's local state, weighted relative to c0: the first term of
+// its own start state, kept in TMEM.  It publishes that state (pub) when a
+// later segment needs it too.  Segment 0 starts from zero and runs phase B
+// at once.
 struct Item {
-    int bh, seg, half, c0, c1;
-    bool hasA;
+    int bh, seg, half, c0, c1, a0, a1;
+    bool hasA, pub;
 };
 
 __device__ __forceinline__ Item decode_item(int t, const Params &p) {
@@ -155,9 +168,12 @@ __device__ __forceinline__ Item decode_item(int t, const Params &p) {
     const int u = t / p.nhalf;
     it.bh = u % p.BH;
     it.seg = u / p.BH;
-    it.c0 = it.seg * p.seg_chunks;
-    it.c1 = min(it.c0 + p.seg_chunks, p.nchunks);
-    it.hasA = it.seg < p.nseg - 1;
+    it.c0 = it.seg == 0 ? 0 : p.seg0 + (it.seg - 1) * p.seg_chunks;
+    it.c1 = min(it.seg == 0 ? p.seg0 : it.c0 + p.seg_chunks, p.nchunks);
+    it.a0 = it.seg <= 1 ? 0 : p.seg0 + (it.seg - 2) * p.seg_chunks;
+    it.a1 = it.c0;
+    it.hasA = it.seg > 0;
+    it.pub = it.seg > 0 && it.seg < p.nseg - 1;
     return it;
 }
 
@@ -201,7 +217,8 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         for (int pass = it.hasA ? 0 : 1; pass < 2 && !stop; ++pass) {
-            for (int c = it.c0; c < it.c1; ++c, ++j) {
+            const int cb = pass == 0 ? it.a0 : it.c0, ce = pass == 0 ? it.a1 : it.c1;
+            for (int c = cb; c < ce; ++c, ++j) {
                 const int st = j % L::STAGES;
                 const uint32_t par = ((j / L::STAGES) & 1) ^ 1;
                 if (!wait_bar(&sm.empty[st], par, cx)) {
@@ -269,8 +286,10 @@ __device__ __forceinline__ void try_issue_next_p(uint8_t *smem, Small &sm,
     using L = Layout<DK, kMode>;
     if (p_next != qi + 1 || qi + 1 >= nB) return;
     const int st1 = (jj + 1) % L::STAGES, b1 = (nbq + 1) & 1;
-    if (mbar_try_wait(&sm.xf[st1], ((jj + 1) / L::STAGES) & 1) &&
-        mbar_try_wait(&sm.pv_done[b1], (((nbq + 1) >> 1) & 1) ^ 1)) {
+    // test_wait never suspends the thread (try_wait may, for a
+    // system-dependent time, when the phase is not complete)
+    if (mbar_test_wait(&sm.xf[st1], ((jj + 1) / L::STAGES) & 1) &&
+        mbar_test_wait(&sm.pv_done[b1], (((nbq + 1) >> 1) & 1) ^ 1)) {
         issue_p<DK, kMode>(smem, sm, cx, tmem, jj + 1, nbq + 1);
         ++p_next;
     }
@@ -299,7 +318,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
             // phase A: the segment's local state.  S's columns are free: the
             // previous item read them before its last sb_ready.  Phase-A
             // stages have no output, so both of their releases come from here.
-            for (int c = it.c0; c < it.c1; ++c, ++j) {
+            for (int c = it.a0; c < it.a1; ++c, ++j) {
                 const int st = j % L::STAGES;
                 wait_bar(&sm.xf[st], (j / L::STAGES) & 1, cx);
                 tc_fence_after();
@@ -309,8 +328,8 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, lboA, 1024),
                            sdesc_sw128(vb + ks * 2048, onesx - vb, 1024), idSU,
-                           (c > it.c0 || ks > 0) ? 1u : 0u);
-                if (c == it.c1 - 1) mma_commit(&sm.s_full);
+                           (c > it.a0 || ks > 0) ? 1u : 0u);
+                if (c == it.a1 - 1) mma_commit(&sm.s_full);
                 mma_commit(&sm.empty[st]);
                 mma_commit(&sm.empty[st]);
             }
@@ -626,21 +645,23 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         const float lg = head_log2g(dk, it.bh);
         float gnext = 1.f;  // mode 2: gates of the next chunk this role transforms
         if (it.hasA) {
-            // phase A: Khat_t = g^(L-1-t) phi(k_t), t relative to the segment
-            // end; with gates Khat_t = prod_{u>t in the segment} alpha_u phi(k_t)
-            const int seg_end = min(it.c1 * C, p.N);
+            // phase A over the predecessor's chunks [a0, a1): Khat_t =
+            // g^(a1 C - 1 - t) phi(k_t), t relative to the end of that range
+            // (the item's own start); with gates Khat_t = prod_{u>t in the
+            // range} alpha_u phi(k_t).  Every chunk of the range is full.
+            const int seg_end = it.a1 * C;
             float L2 = 0.f, off2 = 0.f;
             int Z = 0, offz = 0;
             if (kMode == 2) {
-                gnext = gate_load(p, it.bh, it.c0, et);
-                gate_totals(L2, Z, p, it.bh, it.c0 * C, seg_end, et, kTThreads,
+                gnext = gate_load(p, it.bh, it.a0, et);
+                gate_totals(L2, Z, p, it.bh, it.a0 * C, seg_end, et, kTThreads,
                             sm.tg_l, sm.tg_z, BAR_T);
             }
-            for (int c = it.c0; c < it.c1; ++c, ++j) {
+            for (int c = it.a0; c < it.a1; ++c, ++j) {
                 const int st = j % L::STAGES;
-                // the next chunk's gates (phase B restarts at c0)
+                // the next chunk's gates (after the range: phase B's first, c0 = a1)
                 const float gcur = gnext;
-                if (kMode == 2) gnext = gate_load(p, it.bh, c + 1 < it.c1 ? c + 1 : it.c0, et);
+                if (kMode == 2) gnext = gate_load(p, it.bh, c + 1, et);
                 wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
                 uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
                 const int tok = c * C + row;
@@ -740,7 +761,7 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
             if (et < 32) sm.gtab[et] = gpow(lg, et);
             named_bar_sync(BAR_E1, 128);
         }
-        if (it.hasA) j += it.c1 - it.c0;  // phase-A jobs
+        if (it.hasA) j += it.a1 - it.a0;  // phase-A jobs
         for (int c = it.c0; c < it.c1; ++c, ++nb, ++j) {
             const int b = nb & 1;
             const uint32_t tp = lb + TM_P + 128u * b;
@@ -972,18 +993,18 @@ struct SMap {
           hasz(DK == 64 ? lane < 64 : true) {}
 };
 
-// Look-back, step 1 (one warp): decided once every predecessor (segments
-// 0 .. seg-1 of the head and half) has published its local state; 32 flags
-// per look.  Leaves seg in lb_n, or -1 when `wait` is false and some
-// predecessor has not published yet.
+// Look-back, step 1 (one warp): decided once segments 1 .. seg-1 of the
+// head and half (which hold the local states of segments 0 .. seg-2) have
+// all published; 32 flags per look.  Leaves seg - 1 in lb_n, or -1 when
+// `wait` is false and one of them has not published yet.
 __device__ __forceinline__ void resolve_lookback(Small &sm, const Params &p,
                                                  const Item &it, const Ctx &cx,
                                                  int lane, bool wait) {
-    int n = it.seg;
+    int n = it.seg > 0 ? it.seg - 1 : 0;
     long long dl = 0;
-    for (int base = 0; base < it.seg && n >= 0; base += 32) {
+    for (int base = 1; base < it.seg && n >= 0; base += 32) {
         const int s = base + lane;
-        const int *fp = p.flags + item_index(it.bh, s < it.seg ? s : 0, it.half, p);
+        const int *fp = p.flags + item_index(it.bh, s < it.seg ? s : 1, it.half, p);
         for (;;) {
             const int f = s < it.seg ? load_flag(fp) : FLAG_AGG;
             if (__all_sync(~0u, f >= FLAG_AGG)) break;
@@ -1011,18 +1032,21 @@ __device__ __forceinline__ void resolve_lookback(Small &sm, const Params &p,
 }
 
 // Look-back, step 2 (every thread): its 32 columns (half h) of row a of
-// sum_{m = 0..nlb-1} g^(L m) local(seg-1-m), nearest predecessor first (a
-// fixed order, so the start state does not depend on timing), and z[a].
+// sum_{m = 0..nlb-1} w_m local(seg-2-m), nearest first (a fixed order, so
+// the start state does not depend on timing), and z[a].  local(j) is in the
+// slot of segment j + 1.  w_0 = w0 is the decay across the item's own
+// phase-A range (segment seg-1); each further term is decayed across one more
+// segment: g^(L C), or with gates the product its holder published.
 template <int DK, int kMode>
 __device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
                                              const Item &it, int nlb, int a,
-                                             int h, bool zh, float gL,
+                                             int h, bool zh, float gL, float w0,
                                              float (&acc)[32], float &accz) {
     using L = Layout<DK, kMode>;
 #pragma unroll
     for (int e = 0; e < 32; ++e) acc[e] = 0.f;
     accz = 0.f;
-    float w = 1.f;
+    float w = w0;
     for (int m = 0; m < nlb; ++m) {
         const int pi = item_index(it.bh, it.seg - 1 - m, it.half, p);
         const float *src = p.agg + (size_t)pi * L::STATE;
@@ -1036,8 +1060,25 @@ __device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
             acc[4 * e + 3] = fmaf(w, u.w, acc[4 * e + 3]);
         }
         if (zh) accz = fmaf(w, __ldcg(src + DK * DV + a), accz);
-        // the next one back is decayed across this predecessor's segment too
         w *= kMode == 2 ? __ldcg(p.gprod + pi) : gL;
+    }
+}
+
+// The item's own phase-A result (TMEM S, this thread's 32 columns of half
+// h, and z[a]) added to a look-back sum: the start state's first term.
+__device__ __forceinline__ void add_own_state(uint32_t lb, int h, bool zh,
+                                              float (&acc)[32], float &accz) {
+    uint32_t v[32];
+    tmem_ld32(lb + TM_S + 32 * h, v);
+    tmem_wait_ld();
+    reg_fence(v);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = u2f(v[e]) + acc[e];
+    if (zh) {
+        uint32_t zl = tmem_ld1(lb + TM_S + DV);
+        tmem_wait_ld();
+        reg_fence(zl);
+        accz = u2f(zl) + accz;
     }
 }
 
@@ -1085,25 +1126,31 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
-        float gL = gpow(lg, p.seg_chunks * C);
+        // The decay across one segment of seg_chunks chunks: every segment a
+        // look-back reaches across (1 .. seg-1) has that length.  w0 is the
+        // decay across the item's own phase-A range; with gates the product
+        // of its gates, published with the state for the segments after it.
+        const float gL = gpow(lg, p.seg_chunks * C);
+        float w0 = gL;
         if (kMode == 2 && it.hasA) {
-            // the segment's product of gates: scales its start state into
-            // what its successors' look-back applies across it, published
             float L2;
             int Z;
-            gate_totals(L2, Z, p, it.bh, it.c0 * C, min(it.c1 * C, p.N), et, 128,
+            gate_totals(L2, Z, p, it.bh, it.a0 * C, it.a1 * C, et, 128,
                         sm.eg_l, sm.eg_z, BAR_E2);
-            gL = Z == 0 ? exp2f(L2) : 0.f;
-            if (et == 0) p.gprod[t] = gL;  // visible with the item's flags
+            w0 = Z == 0 ? exp2f(L2) : 0.f;
+            if (et == 0 && it.pub) p.gprod[t] = w0;  // visible with the item's flags
         }
         float *agg = p.agg + (size_t)t * L::STATE;
         const int n0 = min(C, p.N - it.c0 * C);
         float f0 = gpow(lg, n0);
-        // Look-back, first try: if the predecessors have already published,
-        // sum their states now, while phase A runs, into the threads' slots.
+        // The start state: the item's own phase-A result (TMEM S) plus the
+        // states that segments 1 .. seg-1 published.  Look-back, first try:
+        // if those have already published, sum them now, while phase A
+        // runs, into the threads' slots.
+        const bool lbk = it.seg >= 2;
         bool early = false;
         float accz_e = 0.f;
-        if (it.hasA) {
+        if (lbk) {
             if (warp == kWarpE2) resolve_lookback(sm, p, it, cx, lane, false);
             named_bar_sync(BAR_E2, 128);
             const int nlb = sm.lb_n;
@@ -1113,7 +1160,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 for (int hh = 0; hh < SM::NH; ++hh) {
                     float acc[32], accz;
                     lookback_sum<DK, kMode>(sm, p, it, nlb, a, h0 + hh,
-                                             hasz && hh == 0, gL, acc, accz);
+                                             hasz && hh == 0, gL, w0, acc, accz);
                     if (hh == 0) accz_e = accz;
                     float4 *slot = lb_slot<DK>(sb, a, h0, hh);
 #pragma unroll
@@ -1122,33 +1169,37 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                                                         acc[4 * e + 2], acc[4 * e + 3]);
                 }
             }
-            j += it.c1 - it.c0;  // the phase-A jobs (released by the MMA issuer)
+        }
+        if (it.hasA) {
+            j += it.a1 - it.a0;  // the phase-A jobs (released by the MMA issuer)
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
             tc_fence_after();
-            // publish the segment's local state at once
+            if (it.pub) {
+                // publish the predecessor's local state at once
 #pragma unroll
-            for (int hh = 0; hh < SM::NH; ++hh) {
-                const int h = h0 + hh;
-                uint32_t v[32];
-                tmem_ld32(lb + TM_S + 32 * h, v);
-                tmem_wait_ld();
-                reg_fence(v);
-                float4 *dst = reinterpret_cast<float4 *>(agg + a * DV + 32 * h);
+                for (int hh = 0; hh < SM::NH; ++hh) {
+                    const int h = h0 + hh;
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_S + 32 * h, v);
+                    tmem_wait_ld();
+                    reg_fence(v);
+                    float4 *dst = reinterpret_cast<float4 *>(agg + a * DV + 32 * h);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
-                                         u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
+                                             u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+                }
+                if (hasz) {
+                    uint32_t zl = tmem_ld1(lb + TM_S + DV);
+                    tmem_wait_ld();
+                    reg_fence(zl);
+                    agg[DK * DV + a] = u2f(zl);
+                }
+                __threadfence();
+                named_bar_sync(BAR_E2, 128);
+                if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
             }
-            if (hasz) {
-                uint32_t zl = tmem_ld1(lb + TM_S + DV);
-                tmem_wait_ld();
-                reg_fence(zl);
-                agg[DK * DV + a] = u2f(zl);
-            }
-            __threadfence();
-            named_bar_sync(BAR_E2, 128);
-            if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
         }
         if (kMode == 2) {
             // the first chunk's product of gates (its transform wrote the
@@ -1174,8 +1225,11 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                     acc[4 * e + 2] = u.z;
                     acc[4 * e + 3] = u.w;
                 }
+                float accz = zh ? accz_e : 0.f;
+                add_own_state(lb, h, zh, acc, accz);
+                if (zh) accz_e = accz;
                 uint32_t v[32];
-                if (zh) tmem_put_z(lb + TM_S + DV, f0 * accz_e);
+                if (zh) tmem_put_z(lb + TM_S + DV, f0 * accz);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(f0 * acc[e]);
                 tmem_st32(lb + TM_S + 32 * h, v);
@@ -1185,16 +1239,20 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             }
             if (hasz) store_zrow(sbz, a, accz_e);
         } else {
-            // look-back, waiting for the predecessors
-            if (warp == kWarpE2) resolve_lookback(sm, p, it, cx, lane, true);
-            named_bar_sync(BAR_E2, 128);
-            const int nlb = sm.lb_n;
+            // look-back, waiting for segments 1 .. seg-1
+            int nlb = 0;
+            if (lbk) {
+                if (warp == kWarpE2) resolve_lookback(sm, p, it, cx, lane, true);
+                named_bar_sync(BAR_E2, 128);
+                nlb = sm.lb_n;
+            }
 #pragma unroll 1
             for (int hh = 0; hh < SM::NH; ++hh) {
                 const int h = h0 + hh;
                 const bool zh = hasz && hh == 0;
                 float acc[32], accz;
-                lookback_sum<DK, kMode>(sm, p, it, nlb, a, h, zh, gL, acc, accz);
+                lookback_sum<DK, kMode>(sm, p, it, nlb, a, h, zh, gL, w0, acc, accz);
+                if (it.hasA) add_own_state(lb, h, zh, acc, accz);
                 // phase-B start: TMEM [S | z] = g^n0 [S_start | z_start], and
                 // the bf16 [S_start | z_start] operand
                 uint32_t v[32];
@@ -1429,7 +1487,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Work decomposition and workspace layout of one causal launch.
 struct CausalPlan {
-    int seg_chunks, nseg, nchunks, nhalf;
+    int seg_chunks, seg0, nseg, nchunks, nhalf;
     long long items;
     size_t off_flags, off_agg, off_gprod, total;
 };
@@ -1441,11 +1499,24 @@ CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms, bool folds =
     CausalPlan pl{};
     pl.nchunks = (sh.N + C - 1) / C;
     pl.nhalf = DK / DV;
-    if (seg_chunks <= 0)
+    const bool automatic = seg_chunks <= 0;
+    if (automatic)
         seg_chunks = folds ? auto_segment_chunks<false>(sh.BH() * pl.nhalf, pl.nchunks, sms)
                            : auto_segment_chunks<kMode != 0>(sh.BH() * pl.nhalf, pl.nchunks, sms);
+    if (seg_chunks > pl.nchunks) seg_chunks = pl.nchunks;
+    int seg0 = seg_chunks;
+    // Two segments per head: segment 0 runs phase B from the start while
+    // segment 1 first reduces segment 0's chunks (phase A, about 0.42 of a
+    // phase-B chunk's time), so segment 0 takes three fifths of the chunks
+    // (B4 H16 N4096 d64: 19 of 32 chunks, 50.7 us a step; 21: 52.7 us; 22:
+    // 54.8 us; equal halves with segment 0 running a phase A: 56.5 us).
+    if (automatic && (pl.nchunks + seg_chunks - 1) / seg_chunks == 2) {
+        seg0 = 3 * pl.nchunks / 5;
+        seg_chunks = pl.nchunks - seg0;
+    }
+    pl.seg0 = seg0;
     pl.seg_chunks = seg_chunks;
-    pl.nseg = (pl.nchunks + seg_chunks - 1) / seg_chunks;
+    pl.nseg = pl.nchunks <= seg0 ? 1 : 1 + (pl.nchunks - seg0 + seg_chunks - 1) / seg_chunks;
     pl.items = sh.BH() * pl.nseg * pl.nhalf;
     // workspace: control words, flags, published states
     pl.off_flags = 256;
@@ -1484,6 +1555,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.nchunks = pl.nchunks;
     p.nhalf = pl.nhalf;
     p.seg_chunks = pl.seg_chunks;
+    p.seg0 = pl.seg0;
     p.nseg = pl.nseg;
     p.items = (int)pl.items;
     p.timeout = 1LL << 32;
@@ -1651,6 +1723,7 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
                 "la_forward_causal_noalloc: the problem needs more workspace "
                 "than the 16 MiB static scratch holds (too many heads)"};
     p.seg_chunks = seg;
+    p.seg0 = seg;
     p.nseg = (p.nchunks + seg - 1) / seg;
     p.items = (int)items;
     p.timeout = 1LL << 32;
