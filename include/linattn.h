@@ -381,8 +381,11 @@ unsigned long long la_kernel_launch_count(void);
  * la_debug_inject_timeout -- the next d = 128 causal tensor-core launch
  * (la_forward and friends with bf16, d = 128, no gates) bounds every wait by
  * `wait_cycles` clock cycles (>= 4096) instead of about two seconds, and
- * segment `hold_segment` of every head never publishes its local state
- * (-1: all publish).  Its successors' waits then run out: the launch records
+ * segment `hold_segment` of every head never publishes the state it holds
+ * (-1: all publish).  Segment s >= 1 holds the local state of segment s - 1
+ * and publishes it when a segment after s needs it (s = 1 .. nseg - 2;
+ * segment 0 and the last segment publish nothing).  The segments after
+ * `hold_segment` then wait in vain and their waits run out: the launch records
  * LA_ERR_TIMEOUT in the device status word, every later wait of the launch
  * passes through, it finishes (outputs invalid) and la_check_device_status
  * reports LA_ERR_TIMEOUT.  LA_ERR_INVALID_ARG for wait_cycles < 4096.

@@ -38,15 +38,19 @@
 //
 // Sequence parallelism: a head's chunks are cut into segments; persistent
 // CTAs (one per SM) take (head, segment) items from a ticket counter in
-// segment-major order.  A segment with successors first reduces its own
-// K and V to its local state (phase A: Khat^T [V | 1] with weights relative
-// to the segment end) and publishes it at once; its start state is the
-// decayed sum of all its predecessors' local states,
-//   start(s) = sum_{m = 1..s} g^(L (m - 1)) local(s - m),
+// segment-major order.  Segment 0 starts from the zero state and runs the
+// chunk loop (phase B) at once.  A later segment s first reduces its
+// predecessor's K and V to that segment's local state (phase A:
+// Khat^T [V | 1] with weights relative to the end of that range, its own
+// start), keeps it in TMEM as the first term of its start state, and
+// publishes it when a later segment needs it.  The other terms are the
+// states published by segments 1 .. s-1 (the local states of segments
+// s-2 .. 0):
+//   start(s) = local(s-1) + sum_{m = 2..s} g^(L (m - 1)) local(s - m),
 // added in this fixed order, so results do not depend on timing (repeated
 // calls are bit-identical) and no segment waits on another's look-back.
-// The score warps, idle in phase A, form the sum while phase A runs when the
-// predecessors have already published.
+// The score warps, idle in phase A, form the published part while phase A
+// runs when its segments have already published.
 //
 // Warp roles (576 threads): warp 0 TMA producer (with L2 prefetch ahead),
 // warp 1 MMA issuer and TMEM owner, warps 2-9 feature map (phi(K) in place,
@@ -107,6 +111,7 @@ __host__ __device__ constexpr int v_lbo(int st) { return st ? LBO_V1 : LBO_V0; }
 
 struct Params {
     int BH, N, nchunks, seg_chunks, nseg, items;
+    int seg0;               // chunks of segment 0 (later segments: seg_chunks)
     float *agg;             // [items][STATE] each segment's local state
     int *flags;             // [items]
     float *S_out, *z_out;   // final state [BH][D][D] / [BH][D], or NULL
@@ -134,18 +139,27 @@ struct Small {
     uint32_t tmem_base;
 };
 
+// A work item: segment `seg` of head `bh`, chunks [c0, c1) (segment 0
+// spans seg0 chunks, later ones seg_chunks).  Phase A of segment s >= 1
+// reduces its predecessor's chunks [a0, a1 = c0) to that segment's local
+// state, weighted relative to c0: the first term of its own start state,
+// kept in TMEM, published (pub) when a later segment needs it too.
+// Segment 0 starts from zero and runs phase B at once.
 struct Item {
-    int bh, seg, c0, c1;
-    bool hasA;
+    int bh, seg, c0, c1, a0, a1;
+    bool hasA, pub;
 };
 
 __device__ __forceinline__ Item decode_item(int t, const Params &p) {
     Item it;
     it.bh = t % p.BH;
     it.seg = t / p.BH;
-    it.c0 = it.seg * p.seg_chunks;
-    it.c1 = min(it.c0 + p.seg_chunks, p.nchunks);
-    it.hasA = it.seg < p.nseg - 1;
+    it.c0 = it.seg == 0 ? 0 : p.seg0 + (it.seg - 1) * p.seg_chunks;
+    it.c1 = min(it.seg == 0 ? p.seg0 : it.c0 + p.seg_chunks, p.nchunks);
+    it.a0 = it.seg <= 1 ? 0 : p.seg0 + (it.seg - 2) * p.seg_chunks;
+    it.a1 = it.c0;
+    it.hasA = it.seg > 0;
+    it.pub = it.seg > 0 && it.seg < p.nseg - 1;
     return it;
 }
 
@@ -167,14 +181,15 @@ __device__ __forceinline__ int pop_item(Small &sm, int &tl, const Ctx &cx,
 
 // ---------------------------------------------------------------- look-back
 
-// True once segments 0 .. seg-1 of head bh have all published their local
-// states (one warp; 32 flags per look).  Without `wait` it looks once.
+// True once segments 1 .. seg-1 of head bh (which hold the local states of
+// segments 0 .. seg-2) have all published (one warp; 32 flags per look).
+// Without `wait` it looks once.
 __device__ __forceinline__ bool preds_published(const Params &p, const Ctx &cx, int bh,
                                                 int seg, int lane, bool wait) {
     long long dl = 0;
-    for (int base = 0; base < seg; base += 32) {
+    for (int base = 1; base < seg; base += 32) {
         const int s = base + lane;
-        const int *fp = p.flags + item_index(bh, s < seg ? s : 0, p);
+        const int *fp = p.flags + item_index(bh, s < seg ? s : 1, p);
         for (;;) {
             const int f = s < seg ? load_flag(fp) : FLAG_AGG;
             if (__all_sync(~0u, f >= FLAG_AGG)) break;
@@ -194,15 +209,17 @@ __device__ __forceinline__ bool preds_published(const Params &p, const Ctx &cx, 
     return true;
 }
 
-// Row r of the start state, columns [32 g, 32 g + 32) (g < 4) or z[r] in
-// acc[0] (g = 4): sum_{m = 1..seg} gL^(m - 1) local(seg - m), in this order.
+// Row r of the published part of the start state, columns [32 g, 32 g + 32)
+// (g < 4) or z[r] in acc[0] (g = 4): sum_{m = 2..seg} gL^(m - 1)
+// local(seg - m), in this order; local(j) sits in segment j + 1's slot.  The
+// first term, m = 1, is the item's own phase-A result.
 __device__ __forceinline__ void start_sum(const Params &p, int bh, int seg, int r, int g,
                                           float gL, float (&acc)[32]) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-    float w = 1.f;
-    for (int m = 1; m <= seg; ++m) {
-        const float *src = p.agg + (size_t)item_index(bh, seg - m, p) * STATE;
+    float w = gL;
+    for (int m = 2; m <= seg; ++m) {
+        const float *src = p.agg + (size_t)item_index(bh, seg - m + 1, p) * STATE;
         if (g < 4) {
             const float4 *s4 = reinterpret_cast<const float4 *>(src);
 #pragma unroll
@@ -254,13 +271,13 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
         ++tl;
         if (t < 0) break;
         const Item it = decode_item(t, p);
-        const int nc = it.c1 - it.c0, nA = it.hasA ? nc : 0, nJ = nA + nc;
+        const int nc = it.c1 - it.c0, nA = it.hasA ? it.a1 - it.a0 : 0, nJ = nA + nc;
         if (*cx.abort) continue;  // issue nothing more once a wait gave up
         bool stop = false;
         for (int x = 0; x < nJ + kPrefetch && !stop; ++x) {
             if (x < nJ) {  // prefetch of job x, then the loads of job x - kPrefetch
                 const int pass = x < nA ? 0 : 1;
-                const int c = it.c0 + (pass == 0 ? x : x - nA);
+                const int c = pass == 0 ? it.a0 + x : it.c0 + (x - nA);
                 if (pass == 0) {
                     for (int kb = 0; kb < 2; ++kb) {
                         tma_prefetch_3d(tk, 64 * kb, c * C, it.bh, keep);
@@ -271,7 +288,7 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
             const int y = x - kPrefetch;
             if (y < 0) continue;
             const int pass = y < nA ? 0 : 1;
-            const int c = it.c0 + (pass == 0 ? y : y - nA);
+            const int c = pass == 0 ? it.a0 + y : it.c0 + (y - nA);
             const int st = j % STAGES;
             const uint32_t par = ((j / STAGES) & 1) ^ 1;
             if (!wait_bar_spin(&sm.k_empty[st], par, cx)) break;
@@ -344,8 +361,8 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         if (it.hasA) {
-            // phase A: the segment's local state Khat^T [V | 1] into S | z
-            for (int c = it.c0; c < it.c1; ++c, ++j) {
+            // phase A: the predecessor's local state Khat^T [V | 1] into S | z
+            for (int c = it.a0; c < it.a1; ++c, ++j) {
                 const int st = j % STAGES;
                 wait_bar_spin(&sm.xfk[st], (j / STAGES) & 1, cx);
                 wait_bar_spin(&sm.v_full[st], (j / STAGES) & 1, cx);
@@ -356,8 +373,8 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_ss(tmem + TM_S, sdesc_sw128(kb + ks * 2048, BLK, 1024),
                            sdesc_sw128(vb + ks * 2048, v_lbo(st), 1024), idSU,
-                           (c > it.c0 || ks > 0) ? 1u : 0u);
-                if (c == it.c1 - 1) mma_commit(&sm.s_full);
+                           (c > it.a0 || ks > 0) ? 1u : 0u);
+                if (c == it.a1 - 1) mma_commit(&sm.s_full);
                 mma_commit(&sm.k_empty[st]);
                 mma_commit(&sm.v_empty[st]);
             }
@@ -471,9 +488,11 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         if (it.hasA) {
-            // phase A: Khat_t = g^(L-1-t) phi(k_t), t relative to the segment end
-            const int seg_end = min(it.c1 * C, p.N);
-            for (int c = it.c0; c < it.c1; ++c, ++j) {
+            // phase A over the predecessor's chunks [a0, a1): Khat_t =
+            // g^(a1 C - 1 - t) phi(k_t), t relative to the item's own start
+            // (every chunk of the range is full)
+            const int seg_end = it.a1 * C;
+            for (int c = it.a0; c < it.a1; ++c, ++j) {
                 const int st = j % STAGES;
                 wait_bar(&sm.k_full[st], (j / STAGES) & 1, cx);
                 uint8_t *kt = smem + k_off(st);
@@ -657,12 +676,12 @@ __device__ void score_output(uint8_t *smem, Small &sm, const Params &p, const Ct
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
         if (kMode == 1 && et < 32) sm.gtab[et] = gpow(lg, et);
-        // The start state, if every predecessor has already published its
-        // local state, summed now (phase A runs meanwhile) into TMEM O (row
-        // `row` of S, and z in column D); the state warps take it from there.
+        // The published part of the start state (segments 1 .. seg-1), if
+        // they have all published already, summed now (phase A runs
+        // meanwhile) into TMEM O (row `row` of S, and z in column D); the
+        // state warps take it from there.
         if (et < 32) {
-            const bool e = it.hasA && it.seg > 0 &&
-                           preds_published(p, cx, it.bh, it.seg, lane, false);
+            const bool e = it.seg >= 2 && preds_published(p, cx, it.bh, it.seg, lane, false);
             if (lane == 0) sm.lb_early = e ? 1 : 0;
         }
         named_bar_sync(BAR_E1, 128);
@@ -692,7 +711,7 @@ __device__ void score_output(uint8_t *smem, Small &sm, const Params &p, const Ct
         if (et == 0) mbar_arrive(&sm.lb_done);
         // phase B: the output of chunk c - 1 (its O completes before P of
         // chunk c, issued after it), then the scores of chunk c
-        if (it.hasA) j += it.c1 - it.c0;
+        if (it.hasA) j += it.a1 - it.a0;
         for (int c = it.c0; c < it.c1; ++c, ++nb, ++j) {
             if (c > it.c0)
                 output_chunk(smem, sm, cx, lb, row, et, nb - 1, (j - 1) % STAGES, norm);
@@ -751,47 +770,53 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
         const float gL = gpow(lg, p.seg_chunks * C);
         const float f0 = gpow(lg, min(C, p.N - it.c0 * C));
         if (it.hasA) {
-            // publish the segment's local state (phase A) at once
+            // phase A done: its result (the predecessor's local state) is in
+            // TMEM S; publish it at once if a later segment needs it
             wait_bar(&sm.s_full, ns & 1, cx);
             ++ns;
             tc_fence_after();
-            float4 *d4 = reinterpret_cast<float4 *>(p.agg + (size_t)t * STATE);
+            if (it.pub) {
+                float4 *d4 = reinterpret_cast<float4 *>(p.agg + (size_t)t * STATE);
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-                uint32_t v[32];
-                tmem_ld32(lb + TM_S + 32 * g, v);
-                tmem_wait_ld();
-                reg_fence(v);
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_S + 32 * g, v);
+                    tmem_wait_ld();
+                    reg_fence(v);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    d4[(8 * g + u) * 128 + a] = make_float4(u2f(v[4 * u]), u2f(v[4 * u + 1]),
-                                                            u2f(v[4 * u + 2]), u2f(v[4 * u + 3]));
+                    for (int u = 0; u < 8; ++u)
+                        d4[(8 * g + u) * 128 + a] =
+                            make_float4(u2f(v[4 * u]), u2f(v[4 * u + 1]), u2f(v[4 * u + 2]),
+                                        u2f(v[4 * u + 3]));
+                }
+                uint32_t zl = tmem_ld1(lb + TM_S + D);
+                tmem_wait_ld();
+                reg_fence(zl);
+                p.agg[(size_t)t * STATE + D * D + a] = u2f(zl);
+                __threadfence();
+                named_bar_sync(BAR_E2, 128);
+                if (et == 0 && it.seg != p.hold_seg) publish_flag(p.flags + t, FLAG_AGG);
             }
-            uint32_t zl = tmem_ld1(lb + TM_S + D);
-            tmem_wait_ld();
-            reg_fence(zl);
-            p.agg[(size_t)t * STATE + D * D + a] = u2f(zl);
-            __threadfence();
-            named_bar_sync(BAR_E2, 128);
-            if (et == 0 && it.seg != p.hold_seg) publish_flag(p.flags + t, FLAG_AGG);
         }
-        // The start state: summed by the score warps during phase A (parked
-        // in TMEM O), or here once every predecessor has published.
+        // The start state: the own phase-A result (TMEM S) plus the part
+        // that segments 1 .. seg-1 published, summed by the score warps
+        // during phase A (parked in TMEM O), or here once they have all
+        // published.
         wait_bar(&sm.lb_done, nl & 1, cx);
         ++nl;
         tc_fence_after();
-        const bool pred = it.seg > 0;
+        const bool lbk = it.seg >= 2;
         // one value per warp; the barrier below is passed whatever it is, so
         // that the role's barrier count follows from the item alone
         const bool early = __shfl_sync(~0u, sm.lb_early, 0) != 0;
-        if (pred && !early && warp == kWarpE2)
+        if (lbk && !early && warp == kWarpE2)
             preds_published(p, cx, it.bh, it.seg, lane, true);
         named_bar_sync(BAR_E2, 128);
 #pragma unroll 1
         for (int g = 0; g < 5; ++g) {
             // g = 4: the z column
             float pv[32];
-            if (!pred) {
+            if (!lbk) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) pv[e] = 0.f;
             } else if (early) {
@@ -810,6 +835,21 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
                 }
             } else {
                 start_sum(p, it.bh, it.seg, a, g, gL, pv);
+            }
+            if (it.hasA) {  // + the own phase-A result, the first term
+                if (g < 4) {
+                    uint32_t v[32];
+                    tmem_ld32(lb + TM_S + 32 * g, v);
+                    tmem_wait_ld();
+                    reg_fence(v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pv[e] = u2f(v[e]) + pv[e];
+                } else {
+                    uint32_t zl = tmem_ld1(lb + TM_S + D);
+                    tmem_wait_ld();
+                    reg_fence(zl);
+                    pv[0] = u2f(zl) + pv[0];
+                }
             }
             if (g == 4) {
                 store_zb(sb, a, kMode == 2 ? f0 * pv[0] : pv[0]);
@@ -1005,7 +1045,7 @@ inline size_t align_up_w(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Work decomposition and workspace layout of one launch.
 struct WidePlan {
-    int seg_chunks, nseg, nchunks;
+    int seg_chunks, seg0, nseg, nchunks;
     long long items;
     size_t off_flags, off_agg, total;
 };
@@ -1014,10 +1054,20 @@ WidePlan plan_wide(const FwdShape &sh, int seg_chunks, int sms) {
     using namespace causal_wide;
     WidePlan pl{};
     pl.nchunks = (sh.N + C - 1) / C;
-    if (seg_chunks <= 0) seg_chunks = wide_segment_chunks(sh.BH(), pl.nchunks, sms);
+    const bool automatic = seg_chunks <= 0;
+    if (automatic) seg_chunks = wide_segment_chunks(sh.BH(), pl.nchunks, sms);
     if (seg_chunks > pl.nchunks) seg_chunks = pl.nchunks;
+    int seg0 = seg_chunks;
+    // Two segments per head: segment 0 runs phase B from the start while
+    // segment 1 first reduces segment 0's chunks, so segment 0 takes three
+    // fifths of them.
+    if (automatic && (pl.nchunks + seg_chunks - 1) / seg_chunks == 2) {
+        seg0 = 3 * pl.nchunks / 5;
+        seg_chunks = pl.nchunks - seg0;
+    }
+    pl.seg0 = seg0;
     pl.seg_chunks = seg_chunks;
-    pl.nseg = (pl.nchunks + seg_chunks - 1) / seg_chunks;
+    pl.nseg = pl.nchunks <= seg0 ? 1 : 1 + (pl.nchunks - seg0 + seg_chunks - 1) / seg_chunks;
     pl.items = sh.BH() * pl.nseg;
     pl.off_flags = 256;
     pl.off_agg = align_up_w(pl.off_flags + sizeof(int) * (size_t)pl.items, 256);
@@ -1044,6 +1094,7 @@ TcResult launch_wide_with(const void *q, const void *k, const void *v, void *out
     p.N = N;
     p.nchunks = pl.nchunks;
     p.seg_chunks = pl.seg_chunks;
+    p.seg0 = pl.seg0;
     p.nseg = pl.nseg;
     p.items = (int)pl.items;
     p.timeout = 1LL << 32;

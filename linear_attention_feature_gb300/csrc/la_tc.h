@@ -63,8 +63,8 @@ cudaError_t tc_workspace_alloc(void **ws, size_t bytes, cudaStream_t stream);
 
 // Test hooks, per calling thread, each consumed by the next launch that
 // reads it (set through la_debug_inject_timeout / la_debug_fail_next_allocs):
-// the next d = 128 causal launch bounds every wait by `wait_cycles` and never
-// publishes segment `hold_segment`'s state (-1: every segment publishes);
+// the next d = 128 causal launch bounds every wait by `wait_cycles` and
+// segment `hold_segment` never publishes the state it holds (-1: all do);
 // the next `n` workspace allocations fail.
 void tc_debug_set_timeout(long long wait_cycles, int hold_segment);
 bool tc_debug_take_timeout(long long *wait_cycles, int *hold_segment);

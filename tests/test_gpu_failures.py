@@ -30,12 +30,13 @@ def ordinary_call_matches_oracle(q, k, v):
     assert wl.max_row_rel_err(y.cpu(), ref) <= wl.TOL["bf16"]
 
 
-@pytest.mark.parametrize("hold", [0, 1])
+@pytest.mark.parametrize("hold", [1, 2])
 def test_wait_that_runs_out_is_reported(lib, hold):
-    # three segments per head (the last publishes nothing anyway): the
-    # successors of segment `hold` wait for a state that is never published,
-    # with a wait bound of 2^20 cycles
-    q, k, v = (t.cuda() for t in wl.make_qkv(1, 4, 6 * 128, 128, "bf16", seed=17))
+    # four segments per head: segments 1 and 2 publish the states of
+    # segments 0 and 1 (their phase A), which the segments after them need;
+    # those wait for a state that is never published, with a wait bound of
+    # 2^20 cycles
+    q, k, v = (t.cuda() for t in wl.make_qkv(1, 4, 8 * 128, 128, "bf16", seed=17))
     assert lib.la_debug_inject_timeout(1 << 20, hold) == 0
     la.forward(q, k, v, causal=True, path=2, segment_chunks=2)
     with pytest.raises(la.LinAttnError) as ei:
