@@ -219,11 +219,11 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "91c7d553a111171c", "bytes": 1182873600 + 218743296},
+        {"sources": "5c4b75b1ddd8dd1b", "bytes": 1159911424 + 216881152},
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "91c7d553a111171c", "bytes": 577628416 + 83308032},
+        {"sources": "5c4b75b1ddd8dd1b", "bytes": 552412928 + 82489600},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "86beacb004dd8e61", "bytes": 100760832 + 5021696},
+        {"sources": "b129464587918fa8", "bytes": 100752128 + 5222912},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
         {"sources": "dbac54d2b2bcf2fd", "bytes": 100719104 + 3564800},
 }

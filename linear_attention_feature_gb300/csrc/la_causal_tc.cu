@@ -783,7 +783,9 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
             const bool fold = chunk_folds<kMode>(lg, gs, n, p.phi);
             float F = 1.f;
             if (fold) F = kMode == 2 ? fast_exp2(-gs.lg2[n - 1]) : exp2f(-lg * (float)n);
-#pragma unroll
+            // not unrolled: the gated paths make four copies of this body
+            // too much code for the instruction cache the roles share
+#pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
                 uint32_t pk[16];
                 if (blk > q) {
