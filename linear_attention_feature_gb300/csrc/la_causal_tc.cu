@@ -71,6 +71,7 @@ using namespace la::tcc;
 
 constexpr int C = 128;           // chunk length (tokens) = MMA M
 constexpr int DV = 64;           // value columns per work item
+constexpr int kGateSlotBytes = 2048;  // a chunk's gate slot (mode 2)
 constexpr int kWarpT = 2, kNumT = 8, kWarpE1 = 10, kWarpE2 = 14;
 constexpr int kThreads = (kWarpE2 + 4) * 32;  // 576
 constexpr int kTThreads = kNumT * 32;
@@ -93,6 +94,7 @@ struct Params {
     float *S_out, *z_out;  // final state [BH][DK][DK] / [BH][DK], or NULL
     int phi, norm;         // elu(x) + 1 on q, k (else identity); divide by den
     const float *gates;    // mode 2: alpha [BH][N], a gate per token
+    const uint8_t *slots;  // mode 2: [BH][nchunks] gate slots (GateSlot, 2 KB each)
     float *gprod;          // mode 2: [items] each segment's product of gates
     int *ctrl;          // [0] ticket counter, [1] abort flag
     int *status;        // device status word
@@ -231,9 +233,13 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
                 if (j >= L::STAGES) settle_wait(&sm.full[st], par);
                 uint8_t *base = smem + st * L::STAGE;
                 const uint64_t pol = pass == 0 ? keep : stream;
-                mbar_arrive_expect_tx(&sm.full[st], pass == 0
-                                                        ? L::TILE + L::VTILE
-                                                        : 2 * L::TILE + L::VTILE);
+                mbar_arrive_expect_tx(&sm.full[st], (pass == 0 ? L::TILE + L::VTILE
+                                                               : 2 * L::TILE + L::VTILE) +
+                                                        (kMode == 2 ? kGateSlotBytes : 0));
+                if (kMode == 2)  // the chunk's gate slot, computed ahead
+                    bulk_load(base + L::OFF_GS,
+                              p.slots + ((size_t)it.bh * p.nchunks + c) * kGateSlotBytes,
+                              kGateSlotBytes, &sm.full[st]);
                 if (pass == 1)
                     for (int kb = 0; kb < L::KB; ++kb)
                         tma_load_3d(base + L::OFF_Q + kb * 16384, tq, &sm.full[st],
@@ -448,8 +454,8 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
 // before j's block, serves the diagonal block (row and column in one block)
 // where that block has no zero gate and a log2 span within kGateSpan: the
 // product is then 2^(lg2[i] - lg2[s]) colg[j], both factors normal floats.
-// The transform warps write the slot of each stage before its xf arrival;
-// readers wait on that barrier.
+// Every chunk's slot is computed ahead of the forward (gate_slots_kernel);
+// the producer copies it into the chunk's stage with its tiles.
 struct GateSlot {
     float lg2[C];
     int nz[C];
@@ -468,7 +474,7 @@ constexpr float kGateSpan = 100.f;
 // with P.
 constexpr float kFoldLog2 = -0.3770f;  // log2(0.77)
 constexpr float kFoldGateLog2 = -48.f;
-static_assert(sizeof(GateSlot) <= 2048, "GateSlot outgrows its stage slot");
+static_assert(sizeof(GateSlot) == kGateSlotBytes, "a gate slot is copied whole");
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -507,51 +513,50 @@ __device__ __forceinline__ void gate_terms(float a, float &l, int &z) {
     }
 }
 
-// Gate of token et of chunk c (1 past N); transform threads et >= C get 1.
-__device__ __forceinline__ float gate_load(const Params &p, int bh, int c, int et) {
+// The gate slot of chunk c of head bh (block bh * nchunks + c), one thread
+// per token (tokens past N count as gate 1), for every chunk at once ahead
+// of the forward kernel: the chunk-local inclusive prefixes of the log2 of
+// the nonzero gates and of the zero-gate count, then the column factors
+// (see GateSlot).
+__global__ void __launch_bounds__(C) gate_slots_kernel(const float *gates, int N, int nchunks,
+                                                       GateSlot *slots) {
+    __shared__ float wl[C / 32], s_l[C];
+    __shared__ int wz[C / 32], s_z[C];
+    const int c = (int)(blockIdx.x % (unsigned)nchunks), bh = (int)(blockIdx.x / (unsigned)nchunks);
+    const int et = threadIdx.x, lane = et & 31, w = et >> 5;
     const int tok = c * C + et;
-    return et < C && tok < p.N ? __ldg(p.gates + (size_t)bh * p.N + tok) : 1.f;
-}
-
-// The chunk's prefixes and column factors into `g` from the gates `a` the
-// calling threads loaded (all transform threads call; the first 128, one
-// per token, compute).
-__device__ __forceinline__ void gate_scan(GateSlot &g, Small &sm, float a, int et) {
-    const int lane = et & 31, w = et >> 5;
-    float l = 0.f;
-    int z = 0;
-    if (et < C) {
-        gate_terms(a, l, z);
+    const float a = tok < N ? __ldg(gates + (size_t)bh * N + tok) : 1.f;
+    float l;
+    int z;
+    gate_terms(a, l, z);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float lo = __shfl_up_sync(~0u, l, o);
-            const int zo = __shfl_up_sync(~0u, z, o);
-            if (lane >= o) {
-                l += lo;
-                z += zo;
-            }
-        }
-        if (lane == 31) {
-            sm.tg_l[w] = l;
-            sm.tg_z[w] = z;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float lo = __shfl_up_sync(~0u, l, o);
+        const int zo = __shfl_up_sync(~0u, z, o);
+        if (lane >= o) {
+            l += lo;
+            z += zo;
         }
     }
-    named_bar_sync(BAR_T, kTThreads);
-    if (et < C) {
-        for (int w2 = 0; w2 < w; ++w2) {
-            l += sm.tg_l[w2];
-            z += sm.tg_z[w2];
-        }
-        g.lg2[et] = l;
-        g.nz[et] = z;
+    if (lane == 31) {
+        wl[w] = l;
+        wz[w] = z;
     }
-    named_bar_sync(BAR_T, kTThreads);
-    if (et < C) {
-        const int e = et | 31, s = (et & ~31) - 1;
-        g.colf[et] = g.nz[e] == z ? fast_exp2(g.lg2[e] - l) : 0.f;
-        // >= 1; clamped, as blocks past the span never read it
-        g.colg[et] = fast_exp2(fminf((s < 0 ? 0.f : g.lg2[s]) - l, kGateSpan + 1.f));
+    __syncthreads();
+    for (int w2 = 0; w2 < w; ++w2) {
+        l += wl[w2];
+        z += wz[w2];
     }
+    s_l[et] = l;
+    s_z[et] = z;
+    __syncthreads();
+    GateSlot &g = slots[(size_t)bh * nchunks + c];
+    const int e = et | 31, s = (et & ~31) - 1;
+    g.lg2[et] = l;
+    g.nz[et] = z;
+    g.colf[et] = s_z[e] == z ? fast_exp2(s_l[e] - l) : 0.f;
+    // >= 1; clamped, as blocks past the span never read it
+    g.colg[et] = fast_exp2(fminf((s < 0 ? 0.f : s_l[s]) - l, kGateSpan + 1.f));
 }
 
 // Totals over tokens [t0, t1) of head bh: sum of log2 of the nonzero gates
@@ -643,7 +648,6 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         if (t < 0) break;
         const Item it = decode_item(t, p);
         const float lg = head_log2g(dk, it.bh);
-        float gnext = 1.f;  // mode 2: gates of the next chunk this role transforms
         if (it.hasA) {
             // phase A over the predecessor's chunks [a0, a1): Khat_t =
             // g^(a1 C - 1 - t) phi(k_t), t relative to the end of that range
@@ -652,24 +656,19 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             const int seg_end = it.a1 * C;
             float L2 = 0.f, off2 = 0.f;
             int Z = 0, offz = 0;
-            if (kMode == 2) {
-                gnext = gate_load(p, it.bh, it.a0, et);
+            if (kMode == 2)
                 gate_totals(L2, Z, p, it.bh, it.a0 * C, seg_end, et, kTThreads,
                             sm.tg_l, sm.tg_z, BAR_T);
-            }
             for (int c = it.a0; c < it.a1; ++c, ++j) {
                 const int st = j % L::STAGES;
-                // the next chunk's gates (after the range: phase B's first, c0 = a1)
-                const float gcur = gnext;
-                if (kMode == 2) gnext = gate_load(p, it.bh, c + 1, et);
                 wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
                 uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
                 const int tok = c * C + row;
                 if (kMode || tok >= p.N) {
                     float w;
                     if (kMode == 2) {
-                        GateSlot &g = *reinterpret_cast<GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
-                        gate_scan(g, sm, gcur, et);
+                        const GateSlot &g =
+                            *reinterpret_cast<const GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
                         w = tok < p.N && Z == offz + g.nz[row]
                                 ? fast_exp2(L2 - (off2 + g.lg2[row])) : 0.f;
                         const int nv = min(C, p.N - c * C);
@@ -687,7 +686,6 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
                 if (et == 0) mbar_arrive(&sm.xf[st]);
             }
         }
-        if (kMode == 2 && !it.hasA) gnext = gate_load(p, it.bh, it.c0, et);
         // With weights, chunk c's Q and K rows are weighted in place once
         // P(c) has read them.  With three or more stages that step runs
         // after the feature map of chunk c + 1, so the feature map overlaps
@@ -698,14 +696,12 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         bool pfold = false;
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % L::STAGES;
-            const float gcur = gnext;
-            if (kMode == 2 && c + 1 < it.c1) gnext = gate_load(p, it.bh, c + 1, et);
             wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
             uint8_t *qt = smem + st * L::STAGE + L::OFF_Q;
             uint8_t *kt = smem + st * L::STAGE + L::OFF_K;
             const int n = min(C, p.N - c * C);
-            GateSlot &g = *reinterpret_cast<GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
-            if (kMode == 2) gate_scan(g, sm, gcur, et);
+            const GateSlot &g =
+                *reinterpret_cast<const GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
             const bool fold = chunk_folds<kMode>(lg, g, n, p.phi);
             if (fold) {
                 // Qhat and Khat at once (rows past N -> 0)
@@ -1491,7 +1487,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct CausalPlan {
     int seg_chunks, seg0, nseg, nchunks, nhalf;
     long long items;
-    size_t off_flags, off_agg, off_gprod, total;
+    size_t off_flags, off_agg, off_gprod, off_slots, total;
 };
 
 template <int DK, int kMode>
@@ -1525,7 +1521,10 @@ CausalPlan plan_causal(const FwdShape &sh, int seg_chunks, int sms, bool folds =
     pl.off_agg = align_up(pl.off_flags + sizeof(int) * (size_t)pl.items, 256);
     const size_t state_bytes = (pl.nseg > 1) ? sizeof(float) * L::STATE * (size_t)pl.items : 0;
     pl.off_gprod = align_up(pl.off_agg + state_bytes, 256);
-    pl.total = pl.off_gprod + (kMode == 2 ? sizeof(float) * (size_t)pl.items : 0);
+    // mode 2: the gate slots of every chunk of every head
+    pl.off_slots = align_up(pl.off_gprod + (kMode == 2 ? sizeof(float) * (size_t)pl.items : 0), 256);
+    pl.total = pl.off_slots +
+               (kMode == 2 ? (size_t)kGateSlotBytes * (size_t)sh.BH() * (size_t)pl.nchunks : 0);
     return pl;
 }
 
@@ -1580,8 +1579,14 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.flags = reinterpret_cast<int *>(w8 + pl.off_flags);
     p.agg = reinterpret_cast<float *>(w8 + pl.off_agg);
     p.gprod = reinterpret_cast<float *>(w8 + pl.off_gprod);
+    p.slots = reinterpret_cast<const uint8_t *>(w8 + pl.off_slots);
     p.status = status;
     e = tc_zero_words(ws, pl.off_agg, stream);
+    if (e == cudaSuccess && kMode == 2) {
+        gate_slots_kernel<<<(unsigned)(sh.BH() * pl.nchunks), C, 0, stream>>>(
+            gates, N, pl.nchunks, reinterpret_cast<GateSlot *>(w8 + pl.off_slots));
+        e = cudaGetLastError();
+    }
     if (e == cudaSuccess) {
         const size_t smem = smem_bytes<DK, kMode>();
         auto kern = causal_kernel<DK, kMode>;
@@ -1596,7 +1601,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     cudaError_t ef = ws_in ? cudaSuccess : cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return {LA_ERR_CUDA, e, "la_forward: causal kernel launch"};
     if (ef != cudaSuccess) return {LA_ERR_CUDA, ef, "la_forward: workspace free"};
-    note_launches(2);  // workspace clear + forward
+    note_launches(kMode == 2 ? 3 : 2);  // workspace clear (+ gate slots) + forward
     return {LA_OK, cudaSuccess, ""};
 }
 

@@ -125,6 +125,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap,
 
 // L2 prefetch of the tile a 3-D tiled load with the same coordinates would
 // read (no shared-memory destination, no completion to wait for).
+// Bulk copy of `bytes` (a multiple of 16) from global to shared memory
+// (both 16-byte aligned), completing on `bar` (counted in its expect_tx).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1,
                                                 int c2, uint64_t policy) {
     asm volatile(
