@@ -257,6 +257,60 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
         if (x >= 0) settle_wait(&sm.full[x % L::STAGES], (x / L::STAGES) & 1);
 }
 
+// Mode 2, a data-dependent gate alpha_t per token ("Linear Attention", GLA:
+// S_t = G_t (.) S_{t-1} + k_t v_t^T, here with the scalar G_t = alpha_t).
+// For the tokens of one chunk, lg2[t] is the sum of log2(alpha_u) over the
+// nonzero gates u <= t and nz[t] the number of zero gates u <= t (chunk-local
+// inclusive prefixes), so that the product of the gates u = j+1..i is
+// (nz[i] == nz[j]) ? 2^(lg2[i] - lg2[j]) : 0 -- exact where a gate is 0.
+// Tokens past N count as gate 1.  colf[j] is the product of the gates
+// u = j+1 .. e(j), e(j) the last token of j's 32-token block, so that where
+// j's block lies wholly before row i's block the product u = j+1..i factors
+// into a per-row term (u = e(j)+1..i) times colf[j]; both factors lie in
+// [0, 1] and neither overflows.  colg[j] = 2^(lg2[s] - lg2[j]), s the token
+// before j's block, serves the diagonal block (row and column in one block)
+// where that block has no zero gate and a log2 span within kGateSpan: the
+// product is then 2^(lg2[i] - lg2[s]) colg[j], both factors normal floats.
+// Every chunk's slot is computed ahead of the forward (gate_slots_kernel);
+// the producer copies it into the chunk's stage with its tiles.
+struct GateSlot {
+    float lg2[C];
+    int nz[C];
+    float colf[C];
+    float colg[C];
+};
+constexpr float kGateSpan = 100.f;
+// Folded weights: a chunk whose weights all lie in range takes Qhat and
+// Khat as soon as they are mapped, P from them, and one factor per chunk in
+// the score epilogue (see chunk_folds).  Decay: g >= 0.77 (log2 below), so
+// that g^(2C-1) >= 2^-96; gates: no zero gate in the chunk and a product of
+// at least 2^-48, so that every power in P stays above 2^-96.  Only with
+// the elu + 1 feature map: its features are positive, so the bf16 rounding
+// of the weighted rows costs P a relative 2^-8 at most; with the identity
+// map the terms of q . k cancel and that rounding error would not shrink
+// with P.
+constexpr float kFoldLog2 = -0.3770f;  // log2(0.77)
+constexpr float kFoldGateLog2 = -48.f;
+static_assert(sizeof(GateSlot) == kGateSlotBytes, "a gate slot is copied whole");
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Whether chunk weights fold into Q and K (mode 1: per head; mode 2: per
+// chunk, from its gate slot), and the factor of P then: Qhat_i . Khat_j =
+// w(i) w'(j) phi(q_i) . phi(k_j) = G prod_{u=j+1..i}, with G = g^n or the
+// chunk's gate product, so Pt = P / G.
+template <int kMode>
+__device__ __forceinline__ bool chunk_folds(float lg, const GateSlot &g, int n, int phi) {
+    if (!phi) return false;
+    if (kMode == 1) return lg >= kFoldLog2;
+    if (kMode == 2) return g.nz[n - 1] == 0 && g.lg2[n - 1] >= kFoldGateLog2;
+    return false;
+}
+
 // ---------------------------------------------------------------- MMA issuer
 
 // P = phi(Q) phi(K)^T of job `jj` (stage jj % STAGES) into P buffer b of
@@ -303,7 +357,7 @@ __device__ __forceinline__ void try_issue_next_p(uint8_t *smem, Small &sm,
 
 template <int DK, int kMode>
 __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
-                           const Ctx &cx, uint32_t tmem) {
+                           const Ctx &cx, const DecayArgs &dk, uint32_t tmem) {
     using L = Layout<DK, kMode>;
     constexpr uint32_t idPV = idesc_bf16(128, NX, 0, 1);  // Pt [V | 1]
     constexpr uint32_t idQS = idesc_bf16(128, NX, 0, 1);  // phi(Q) [S | z]
@@ -315,11 +369,12 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
     constexpr bool kPVFirst = DK == 64;
     const uint32_t sb = smem_u32(smem + L::OFF_SB);
     const uint32_t onesx = smem_u32(smem + L::OFF_ONESX);
-    int j = 0, nb = 0, nsb = 0, tl = 0;
+    int j = 0, nb = 0, nsb = 0, nk = 0, tl = 0;  // nk: chunks weighted after P
     for (;;) {
         const int t = pop_item(sm, tl, cx, 0, 0, true);
         if (t < 0) break;
         const Item it = decode_item(t, p);
+        const float lg = head_log2g(dk, it.bh);
         if (it.hasA) {
             // phase A: the segment's local state.  S's columns are free: the
             // previous item read them before its last sb_ready.  Phase-A
@@ -375,7 +430,12 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 wait_bar(&sm.sb_ready, nsb & 1, cx);
                 ++nsb;
                 // with weights: Qhat, Khat in place (after P(j) read them)
-                if (kMode) wait_bar(&sm.khat_ready[nbq & 1], (nbq >> 1) & 1, cx);
+                if (kMode && !chunk_folds<kMode>(lg, *reinterpret_cast<const GateSlot *>(
+                                                         smem + st * L::STAGE + L::OFF_GS),
+                                                     min(C, p.N - (it.c0 + qi) * C), p.phi)) {
+                    wait_bar(&sm.khat_ready[nk & 1], (nk >> 1) & 1, cx);
+                    ++nk;
+                }
                 tc_fence_after();
                 for (int ks = 0; ks < DK / 16; ++ks)
                     mma_ss(tmem + tob, sdesc_sw128(qb + kmajor_off(ks, 16384), 16, 1024),
@@ -395,7 +455,12 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 // with weights: Qhat_i = g^(i+1) phi(q_i) and Khat_t =
                 // g^(n-1-t) phi(k_t) (or the products of gates) in place,
                 // once P(j) has read the unweighted rows
-                if (kMode) wait_bar(&sm.khat_ready[nbq & 1], (nbq >> 1) & 1, cx);
+                if (kMode && !chunk_folds<kMode>(lg, *reinterpret_cast<const GateSlot *>(
+                                                         smem + st * L::STAGE + L::OFF_GS),
+                                                     min(C, p.N - (it.c0 + qi) * C), p.phi)) {
+                    wait_bar(&sm.khat_ready[nk & 1], (nk >> 1) & 1, cx);
+                    ++nk;
+                }
                 tc_fence_after();
                 // inter-chunk read phi(Q) [S | z] (Qhat with weights)
                 for (int ks = 0; ks < DK / 16; ++ks)
@@ -439,60 +504,6 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
 }
 
 // ---------------------------------------------------------------- gates (mode 2)
-
-// Mode 2, a data-dependent gate alpha_t per token ("Linear Attention", GLA:
-// S_t = G_t (.) S_{t-1} + k_t v_t^T, here with the scalar G_t = alpha_t).
-// For the tokens of one chunk, lg2[t] is the sum of log2(alpha_u) over the
-// nonzero gates u <= t and nz[t] the number of zero gates u <= t (chunk-local
-// inclusive prefixes), so that the product of the gates u = j+1..i is
-// (nz[i] == nz[j]) ? 2^(lg2[i] - lg2[j]) : 0 -- exact where a gate is 0.
-// Tokens past N count as gate 1.  colf[j] is the product of the gates
-// u = j+1 .. e(j), e(j) the last token of j's 32-token block, so that where
-// j's block lies wholly before row i's block the product u = j+1..i factors
-// into a per-row term (u = e(j)+1..i) times colf[j]; both factors lie in
-// [0, 1] and neither overflows.  colg[j] = 2^(lg2[s] - lg2[j]), s the token
-// before j's block, serves the diagonal block (row and column in one block)
-// where that block has no zero gate and a log2 span within kGateSpan: the
-// product is then 2^(lg2[i] - lg2[s]) colg[j], both factors normal floats.
-// Every chunk's slot is computed ahead of the forward (gate_slots_kernel);
-// the producer copies it into the chunk's stage with its tiles.
-struct GateSlot {
-    float lg2[C];
-    int nz[C];
-    float colf[C];
-    float colg[C];
-};
-constexpr float kGateSpan = 100.f;
-// Folded weights: a chunk whose weights all lie in range takes Qhat and
-// Khat as soon as they are mapped, P from them, and one factor per chunk in
-// the score epilogue (see chunk_folds).  Decay: g >= 0.77 (log2 below), so
-// that g^(2C-1) >= 2^-96; gates: no zero gate in the chunk and a product of
-// at least 2^-48, so that every power in P stays above 2^-96.  Only with
-// the elu + 1 feature map: its features are positive, so the bf16 rounding
-// of the weighted rows costs P a relative 2^-8 at most; with the identity
-// map the terms of q . k cancel and that rounding error would not shrink
-// with P.
-constexpr float kFoldLog2 = -0.3770f;  // log2(0.77)
-constexpr float kFoldGateLog2 = -48.f;
-static_assert(sizeof(GateSlot) == kGateSlotBytes, "a gate slot is copied whole");
-
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Whether chunk weights fold into Q and K (mode 1: per head; mode 2: per
-// chunk, from its gate slot), and the factor of P then: Qhat_i . Khat_j =
-// w(i) w'(j) phi(q_i) . phi(k_j) = G prod_{u=j+1..i}, with G = g^n or the
-// chunk's gate product, so Pt = P / G.
-template <int kMode>
-__device__ __forceinline__ bool chunk_folds(float lg, const GateSlot &g, int n, int phi) {
-    if (!phi) return false;
-    if (kMode == 1) return lg >= kFoldLog2;
-    if (kMode == 2) return g.nz[n - 1] == 0 && g.lg2[n - 1] >= kFoldGateLog2;
-    return false;
-}
 
 // prod_{u=j+1..i} alpha_u within a chunk (j < i; j = -1: from the chunk's
 // first token, i.e. prod_{u<=i}).
@@ -613,27 +624,26 @@ __device__ __forceinline__ void gate_totals(float &L2, int &Z, const Params &p,
 // Qhat_i = g^(i+1) phi(q_i), the weight of the chunk's start state in row i;
 // with gates prod_{u=t+1..n-1} alpha_u and prod_{u<=i} alpha_u.  The
 // inter-chunk read Qhat [S | z] then accumulates onto P~ [V | 1] directly.
-// All transform threads call.
-// A folded chunk was weighted when it was mapped: only the hand-off remains
-// (its wait on P keeps the transform at most one chunk ahead of the MMA
-// issuer's khat_ready waits).
+// All transform threads call, for the chunks that do not fold only (a
+// folded chunk was weighted when it was mapped, and the MMA issuer does not
+// wait for it).  khat_ready is indexed by the count `nk` of such chunks; the
+// wait on P(nb) keeps the transform from arriving twice on one barrier
+// before the MMA issuer has observed the first arrival.
 template <int DK, int kMode>
 __device__ __forceinline__ void weight_qk(uint8_t *smem, Small &sm, const Ctx &cx,
-                                          float lg, int st, int n, int nb,
-                                          int row, int part, int et, bool folded) {
+                                          float lg, int st, int n, int nb, int nk,
+                                          int row, int part, int et) {
     using L = Layout<DK, kMode>;
     wait_bar(&sm.pfull[nb & 1], (nb >> 1) & 1, cx);
-    if (!folded) {
-        const GateSlot &g = *reinterpret_cast<const GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
-        const float wk = row >= n ? 0.f
-                                  : (kMode == 2 ? gate_prod(g, n - 1, row) : gpow(lg, n - 1 - row));
-        const float wq = kMode == 2 ? gate_prod(g, row, -1) : gpow(lg, row + 1);
-        scale_row<DK>(smem + st * L::STAGE + L::OFF_K, row, part, bf2_splat(wk));
-        scale_row<DK>(smem + st * L::STAGE + L::OFF_Q, row, part, bf2_splat(wq));
-        fence_async_shared();
-    }
+    const GateSlot &g = *reinterpret_cast<const GateSlot *>(smem + st * L::STAGE + L::OFF_GS);
+    const float wk = row >= n ? 0.f
+                              : (kMode == 2 ? gate_prod(g, n - 1, row) : gpow(lg, n - 1 - row));
+    const float wq = kMode == 2 ? gate_prod(g, row, -1) : gpow(lg, row + 1);
+    scale_row<DK>(smem + st * L::STAGE + L::OFF_K, row, part, bf2_splat(wk));
+    scale_row<DK>(smem + st * L::STAGE + L::OFF_Q, row, part, bf2_splat(wq));
+    fence_async_shared();
     named_bar_sync(BAR_T, kTThreads);
-    if (et == 0) mbar_arrive(&sm.khat_ready[nb & 1]);
+    if (et == 0) mbar_arrive(&sm.khat_ready[nk & 1]);
 }
 
 template <int DK, int kMode>
@@ -642,7 +652,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
     using L = Layout<DK, kMode>;
     const int et = threadIdx.x - kWarpT * 32;  // 0..255
     const int row = et & 127, part = et >> 7;
-    int j = 0, nb = 0, tl = 0;
+    int j = 0, nb = 0, nk = 0, tl = 0;  // nk: chunks weighted after P (not folded)
     for (;;) {
         const int t = pop_item(sm, tl, cx, BAR_T, kTThreads, et == 0);
         if (t < 0) break;
@@ -692,8 +702,7 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
         // P(c); with two, chunk c + 1's stage is chunk c - 1's, whose
         // release would then sit on the path, so it runs at once.
         constexpr bool kPipe = L::STAGES >= 3;
-        int pst = -1, pn = 0, pnb = 0;
-        bool pfold = false;
+        int pst = -1, pn = 0, pnb = 0, pnk = 0;
         for (int c = it.c0; c < it.c1; ++c, ++j, ++nb) {
             const int st = j % L::STAGES;
             wait_bar(&sm.full[st], (j / L::STAGES) & 1, cx);
@@ -718,19 +727,22 @@ __device__ void transform(uint8_t *smem, Small &sm, const Params &p,
             fence_async_shared();
             named_bar_sync(BAR_T, kTThreads);
             if (et == 0) mbar_arrive(&sm.xf[st]);
-            if (kMode && !kPipe)
-                weight_qk<DK, kMode>(smem, sm, cx, lg, st, n, nb, row, part, et, fold);
+            if (kMode && !kPipe && !fold)
+                weight_qk<DK, kMode>(smem, sm, cx, lg, st, n, nb, nk++, row, part, et);
             if (kMode && kPipe) {
                 if (pst >= 0)
-                    weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et, pfold);
-                pst = st;
-                pn = n;
-                pnb = nb;
-                pfold = fold;
+                    weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, pnk, row, part, et);
+                pst = -1;
+                if (!fold) {
+                    pst = st;
+                    pn = n;
+                    pnb = nb;
+                    pnk = nk++;
+                }
             }
         }
         if (kMode && pst >= 0)
-            weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, row, part, et, pfold);
+            weight_qk<DK, kMode>(smem, sm, cx, lg, pst, pn, pnb, pnk, row, part, et);
     }
 }
 
@@ -1428,7 +1440,7 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
     if (warp == 0) {
         if (lane == 0) producer<DK, kMode>(smem, sm, p, cx, &tq, &tk, &tv);
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer<DK, kMode>(smem, sm, p, cx, tmem);
+        if (lane == 0) mma_issuer<DK, kMode>(smem, sm, p, cx, dk, tmem);
     } else if (warp < kWarpE1) {
         transform<DK, kMode>(smem, sm, p, cx, dk);
     } else if (warp < kWarpE2) {
