@@ -889,8 +889,15 @@ def run_kernel_case(B, H, N, d, form):
     q, k, v = wl.make_qkv(B, H, N, d, "bf16", seed=0, device="cuda")
     out = torch.empty_like(q)
     decay = list(wl.decay_schedule(H)) if form == "decay" else None
+    gates = None
+    if form == "gated":  # a gate per token, uniform in [0.9, 1), as the gated leg
+        gen = torch.Generator(device="cpu").manual_seed(200)
+        gates = (0.9 + 0.1 * torch.rand(B, H, N, generator=gen)).to("cuda")
     for _ in range(4):
-        la.forward(q, k, v, causal=form != "noncausal", decay=decay, out=out)
+        if gates is not None:
+            la.forward_gated(q, k, v, gates, out=out)
+        else:
+            la.forward(q, k, v, causal=form != "noncausal", decay=decay, out=out)
     torch.cuda.synchronize()
     la.check_device_status()
 
@@ -910,7 +917,7 @@ def main():
                     help="timed decode steps (default: the workload's 1024)")
     ap.add_argument("--kernel-case", nargs=5,
                     metavar=("B", "H", "N", "D", "FORM"),
-                    help="run one forward (FORM: causal, noncausal or decay) "
+                    help="run one forward (FORM: causal, noncausal, decay or gated) "
                          "or decode step (FORM: decode or delta) four times "
                          "and exit; a driver for ncu captures")
     args = ap.parse_args()
