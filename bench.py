@@ -219,13 +219,13 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "5c4b75b1ddd8dd1b", "bytes": 1159911424 + 216881152},
+        {"sources": "ff743744ae8aa5a9", "bytes": 1160293632 + 217143296},
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "5c4b75b1ddd8dd1b", "bytes": 552412928 + 82489600},
+        {"sources": "ff743744ae8aa5a9", "bytes": 553779712 + 82348032},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "b129464587918fa8", "bytes": 100752128 + 5222912},
+        {"sources": "ae9465e0fafbe7eb", "bytes": 100759296 + 4972800},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
-        {"sources": "dbac54d2b2bcf2fd", "bytes": 100719104 + 3564800},
+        {"sources": "d59745ffa5a38e91", "bytes": 100719616 + 3770368},
 }
 
 
