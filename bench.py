@@ -215,7 +215,8 @@ def timed_steps(fn, K, W, world, flush=None):
 KNOWN_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
     #     -k regex:<kernel> -s 3 -c 1 python bench.py --kernel-case B H N D FORM
-    # (FORM causal, decay or noncausal; dram__bytes_read.sum +
+    # (FORM causal, decay, noncausal, gated, retention or state;
+    # dram__bytes_read.sum +
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
@@ -224,6 +225,12 @@ KNOWN_TRAFFIC = {
         {"sources": "ff743744ae8aa5a9", "bytes": 553779712 + 82348032},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
         {"sources": "ae9465e0fafbe7eb", "bytes": 100759296 + 4972800},
+    ("causal_kernel<64,2>", "bf16_b4h16_n4096_d64"):
+        {"sources": "ae9465e0fafbe7eb", "bytes": 111111936 + 13041920},
+    ("causal_kernel<64,0>+state", "bf16_b4h16_n4096_d64"):
+        {"sources": "ae9465e0fafbe7eb", "bytes": 100758016 + 5086208},
+    ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
+        {"sources": "ff743744ae8aa5a9", "bytes": 560054016 + 82019328},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
         {"sources": "d59745ffa5a38e91", "bytes": 100719616 + 3770368},
 }
@@ -485,10 +492,11 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
              decay=list(wd.decay), kernel="causal_wide_kernel<2>")
     fwd_path("fp32_causal_small causal", "fp32_causal_small", True, elem=4)
     fwd_path(f"{MID} causal with final state", MID, True, inputs=mid_inputs(),
-             state=True)
+             state=True, kernel="causal_kernel<64,0>+state")
     fwd_path("bf16_decay_b4h8_n16384_d128 retention", wd.name, True,
-             decay=list(wd.decay), retention=True)
-    fwd_path(f"{MID} gated", MID, True, inputs=mid_inputs(), gated=True)
+             decay=list(wd.decay), retention=True, kernel="causal_wide_kernel<1>")
+    fwd_path(f"{MID} gated", MID, True, inputs=mid_inputs(), gated=True,
+             kernel="causal_kernel<64,2>")
     # the same gated problem in fp32 (the CUDA-core kernels)
     fwd_path(f"{MID} gated fp32", MID, True, elem=4, gated=True,
              inputs=tuple(t.float() for t in mid_inputs()))
@@ -893,9 +901,20 @@ def run_kernel_case(B, H, N, d, form):
     if form == "gated":  # a gate per token, uniform in [0.9, 1), as the gated leg
         gen = torch.Generator(device="cpu").manual_seed(200)
         gates = (0.9 + 0.1 * torch.rand(B, H, N, generator=gen)).to("cuda")
+    if form == "retention":  # identity feature map, no normaliser, the decay schedule
+        decay = list(wl.decay_schedule(H))
+    S = z = None
+    if form == "state":  # the forward plus its final state
+        S = torch.empty(B, H, d, d, device="cuda")
+        z = torch.empty(B, H, d, device="cuda")
     for _ in range(4):
         if gates is not None:
             la.forward_gated(q, k, v, gates, out=out)
+        elif form == "retention":
+            la.forward_variant(q, k, v, causal=True, decay=decay, out=out,
+                               feature_map="identity", normalise=False)
+        elif form == "state":
+            la.forward_causal_state(q, k, v, out=out, S=S, z=z)
         else:
             la.forward(q, k, v, causal=form != "noncausal", decay=decay, out=out)
     torch.cuda.synchronize()
@@ -917,7 +936,8 @@ def main():
                     help="timed decode steps (default: the workload's 1024)")
     ap.add_argument("--kernel-case", nargs=5,
                     metavar=("B", "H", "N", "D", "FORM"),
-                    help="run one forward (FORM: causal, noncausal, decay or gated) "
+                    help="run one forward (FORM: causal, noncausal, decay, gated, "
+                         "retention or state) "
                          "or decode step (FORM: decode or delta) four times "
                          "and exit; a driver for ncu captures")
     args = ap.parse_args()
