@@ -220,19 +220,19 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "ff743744ae8aa5a9", "bytes": 1160293632 + 217143296},
+        {"sources": "be95c35f9aa72540", "bytes": 1160145152 + 216721664},
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "ff743744ae8aa5a9", "bytes": 553779712 + 82348032},
+        {"sources": "be95c35f9aa72540", "bytes": 552455168 + 82014976},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "ae9465e0fafbe7eb", "bytes": 100759296 + 4972800},
+        {"sources": "9e33a37a51ebf232", "bytes": 100757248 + 4908800},
     ("causal_kernel<64,2>", "bf16_b4h16_n4096_d64"):
-        {"sources": "ae9465e0fafbe7eb", "bytes": 111111936 + 13041920},
+        {"sources": "9e33a37a51ebf232", "bytes": 109958912 + 12057088},
     ("causal_kernel<64,0>+state", "bf16_b4h16_n4096_d64"):
-        {"sources": "ae9465e0fafbe7eb", "bytes": 100758016 + 5086208},
+        {"sources": "9e33a37a51ebf232", "bytes": 100757760 + 4956672},
     ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "ff743744ae8aa5a9", "bytes": 560054016 + 82019328},
+        {"sources": "be95c35f9aa72540", "bytes": 560132096 + 81980416},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
-        {"sources": "d59745ffa5a38e91", "bytes": 100719616 + 3770368},
+        {"sources": "f4b32ad6ea1b69a3", "bytes": 100719616 + 3992832},
 }
 
 

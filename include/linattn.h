@@ -53,7 +53,8 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run          */
     LA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed         */
     LA_ERR_NO_MEMORY = 4,    /* workspace allocation failed                  */
-    LA_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up           */
+    LA_ERR_TIMEOUT = 5,      /* a device-side bounded wait gave up           */
+    LA_ERR_INTERNAL = 6      /* a debug build's device-side index check failed */
 } la_status;
 
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
@@ -355,7 +356,9 @@ la_status la_forward_causal_noalloc(const void *q, const void *k,
  * la_check_device_status -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns LA_ERR_TIMEOUT if a kernel gave up
  * on a bounded wait since the last check (its outputs are then not valid),
- * LA_ERR_CUDA if the synchronisation itself failed, else LA_OK.
+ * LA_ERR_INTERNAL if, in a library built with LA_DEBUG, a device-side index
+ * check failed (la_last_error names the source line), LA_ERR_CUDA if the
+ * synchronisation itself failed, else LA_OK.
  */
 la_status la_check_device_status(la_stream_t stream);
 

@@ -25,7 +25,8 @@ __all__ = ["forward", "forward_variant", "forward_gated", "decode_step_gated",
 LA_F32 = 0
 LA_BF16 = 1
 STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED",
-          3: "LA_ERR_CUDA", 4: "LA_ERR_NO_MEMORY", 5: "LA_ERR_TIMEOUT"}
+          3: "LA_ERR_CUDA", 4: "LA_ERR_NO_MEMORY", 5: "LA_ERR_TIMEOUT",
+          6: "LA_ERR_INTERNAL"}
 EXPORTED = ("la_forward", "la_forward_ex", "la_decode_step",
             "la_check_device_status", "la_status_string", "la_last_error",
             "la_abi_version", "la_kernel_launch_count",

@@ -395,9 +395,14 @@ la_status la_check_device_status(la_stream_t stream) {
         e = cudaMemcpy(p, zero, sizeof(zero), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "la_check_device_status: clear");
         char msg[160];
-        std::snprintf(msg, sizeof(msg),
-                      "a kernel reported a device-side failure (block %d, wait 0x%05x)",
-                      (word[1] >> 20) & 0xFFF, word[1] & 0xFFFFF);
+        if (word[0] == (int)LA_ERR_INTERNAL)
+            std::snprintf(msg, sizeof(msg),
+                          "a device-side index check failed (debug build, source line %d)",
+                          word[1]);
+        else
+            std::snprintf(msg, sizeof(msg),
+                          "a kernel reported a device-side failure (block %d, wait 0x%05x)",
+                          (word[1] >> 20) & 0xFFF, word[1] & 0xFFFFF);
         return fail(static_cast<la_status>(word[0]), msg);
     }
     return LA_OK;
@@ -412,6 +417,7 @@ const char *la_status_string(la_status s) {
         case LA_ERR_CUDA: return "LA_ERR_CUDA";
         case LA_ERR_NO_MEMORY: return "LA_ERR_NO_MEMORY";
         case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+        case LA_ERR_INTERNAL: return "LA_ERR_INTERNAL";
     }
     return "LA_ERR_UNKNOWN";
 }

@@ -218,6 +218,9 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
         ++tl;
         if (t < 0) break;
         const Item it = decode_item(t, p);
+        LA_DCHECK(p.status, it.bh >= 0 && it.bh < p.BH && it.seg < p.nseg && it.a0 >= 0 &&
+                                it.a0 <= it.a1 && it.a1 == it.c0 && it.c0 < it.c1 &&
+                                it.c1 <= p.nchunks && it.half < p.nhalf);
         for (int pass = it.hasA ? 0 : 1; pass < 2 && !stop; ++pass) {
             const int cb = pass == 0 ? it.a0 : it.c0, ce = pass == 0 ? it.a1 : it.c1;
             for (int c = cb; c < ce; ++c, ++j) {
@@ -236,7 +239,8 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
                 mbar_arrive_expect_tx(&sm.full[st], (pass == 0 ? L::TILE + L::VTILE
                                                                : 2 * L::TILE + L::VTILE) +
                                                         (kMode == 2 ? kGateSlotBytes : 0));
-                if (kMode == 2)  // the chunk's gate slot, computed ahead
+                if (kMode == 2 &&  // the chunk's gate slot, computed ahead
+                    LA_DCHECK(p.status, c >= 0 && c < p.nchunks))
                     bulk_load(base + L::OFF_GS,
                               p.slots + ((size_t)it.bh * p.nchunks + c) * kGateSlotBytes,
                               kGateSlotBytes, &sm.full[st]);
@@ -1014,9 +1018,11 @@ __device__ __forceinline__ void resolve_lookback(Small &sm, const Params &p,
     long long dl = 0;
     for (int base = 1; base < it.seg && n >= 0; base += 32) {
         const int s = base + lane;
-        const int *fp = p.flags + item_index(it.bh, s < it.seg ? s : 1, it.half, p);
+        const int fi = item_index(it.bh, s < it.seg ? s : 1, it.half, p);
+        const bool ok = LA_DCHECK(p.status, fi >= 0 && fi < p.items);
+        const int *fp = p.flags + (ok ? fi : 0);
         for (;;) {
-            const int f = s < it.seg ? load_flag(fp) : FLAG_AGG;
+            const int f = s < it.seg && ok ? load_flag(fp) : FLAG_AGG;
             if (__all_sync(~0u, f >= FLAG_AGG)) break;
             if (!wait) {
                 n = -1;
@@ -1059,6 +1065,9 @@ __device__ __forceinline__ void lookback_sum(const Small &sm, const Params &p,
     float w = w0;
     for (int m = 0; m < nlb; ++m) {
         const int pi = item_index(it.bh, it.seg - 1 - m, it.half, p);
+        if (!LA_DCHECK(p.status, pi >= 0 && pi < p.items && a >= 0 && a < DK && h >= 0 &&
+                                     32 * h + 32 <= DV))
+            continue;
         const float *src = p.agg + (size_t)pi * L::STATE;
         const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV + 32 * h);
 #pragma unroll
@@ -1148,7 +1157,8 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             gate_totals(L2, Z, p, it.bh, it.a0 * C, it.a1 * C, et, 128,
                         sm.eg_l, sm.eg_z, BAR_E2);
             w0 = Z == 0 ? exp2f(L2) : 0.f;
-            if (et == 0 && it.pub) p.gprod[t] = w0;  // visible with the item's flags
+            if (et == 0 && it.pub && LA_DCHECK(p.status, t < p.items))
+                p.gprod[t] = w0;  // visible with the item's flags
         }
         float *agg = p.agg + (size_t)t * L::STATE;
         const int n0 = min(C, p.N - it.c0 * C);
@@ -1186,7 +1196,10 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             ++ns;
             tc_fence_after();
             if (it.pub) {
-                // publish the predecessor's local state at once
+                // publish the predecessor's local state at once (a debug
+                // check guards the stores only: every thread still reaches
+                // the barrier)
+                const bool okp = LA_DCHECK(p.status, t < p.items && a < DK);
 #pragma unroll
                 for (int hh = 0; hh < SM::NH; ++hh) {
                     const int h = h0 + hh;
@@ -1197,18 +1210,19 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                     float4 *dst = reinterpret_cast<float4 *>(agg + a * DV + 32 * h);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
-                                             u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+                        if (okp)
+                            dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
+                                                 u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
                 }
                 if (hasz) {
                     uint32_t zl = tmem_ld1(lb + TM_S + DV);
                     tmem_wait_ld();
                     reg_fence(zl);
-                    agg[DK * DV + a] = u2f(zl);
+                    if (okp) agg[DK * DV + a] = u2f(zl);
                 }
                 __threadfence();
                 named_bar_sync(BAR_E2, 128);
-                if (et == 0) publish_flag(p.flags + t, FLAG_AGG);
+                if (et == 0 && okp) publish_flag(p.flags + t, FLAG_AGG);
             }
         }
         if (kMode == 2) {
@@ -1351,16 +1365,20 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 reg_fence(v);
                 float4 *dst = reinterpret_cast<float4 *>(
                     p.S_out + ((size_t)it.bh * DK + a) * DK + 64 * it.half + 32 * h);
+                const bool oks = LA_DCHECK(p.status, it.bh < p.BH && a < DK &&
+                                                         64 * it.half + 32 * h + 32 <= DK);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
-                                         u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
+                    if (oks)
+                        dst[e] = make_float4(u2f(v[4 * e]), u2f(v[4 * e + 1]),
+                                             u2f(v[4 * e + 2]), u2f(v[4 * e + 3]));
             }
             if (hasz && it.half == 0) {
                 uint32_t zr = tmem_ld1(lb + TM_S + DV);
                 tmem_wait_ld();
                 reg_fence(zr);
-                p.z_out[(size_t)it.bh * DK + a] = u2f(zr);
+                if (LA_DCHECK(p.status, it.bh < p.BH && a < DK))
+                    p.z_out[(size_t)it.bh * DK + a] = u2f(zr);
             }
             tc_fence_before();
             named_bar_sync(BAR_E2, 128);

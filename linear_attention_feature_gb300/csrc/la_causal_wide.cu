@@ -189,9 +189,11 @@ __device__ __forceinline__ bool preds_published(const Params &p, const Ctx &cx, 
     long long dl = 0;
     for (int base = 1; base < seg; base += 32) {
         const int s = base + lane;
-        const int *fp = p.flags + item_index(bh, s < seg ? s : 1, p);
+        const int fi = item_index(bh, s < seg ? s : 1, p);
+        const bool ok = LA_DCHECK(p.status, fi >= 0 && fi < p.items);
+        const int *fp = p.flags + (ok ? fi : 0);
         for (;;) {
-            const int f = s < seg ? load_flag(fp) : FLAG_AGG;
+            const int f = s < seg && ok ? load_flag(fp) : FLAG_AGG;
             if (__all_sync(~0u, f >= FLAG_AGG)) break;
             if (!wait) return false;
             if (__any_sync(~0u, *cx.abort != 0)) return false;
@@ -219,7 +221,9 @@ __device__ __forceinline__ void start_sum(const Params &p, int bh, int seg, int 
     for (int e = 0; e < 32; ++e) acc[e] = 0.f;
     float w = gL;
     for (int m = 2; m <= seg; ++m) {
-        const float *src = p.agg + (size_t)item_index(bh, seg - m + 1, p) * STATE;
+        const int pi = item_index(bh, seg - m + 1, p);
+        if (!LA_DCHECK(p.status, pi >= 0 && pi < p.items && r >= 0 && r < D)) continue;
+        const float *src = p.agg + (size_t)pi * STATE;
         if (g < 4) {
             const float4 *s4 = reinterpret_cast<const float4 *>(src);
 #pragma unroll
@@ -271,6 +275,9 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
         ++tl;
         if (t < 0) break;
         const Item it = decode_item(t, p);
+        LA_DCHECK(p.status, it.bh >= 0 && it.bh < p.BH && it.seg < p.nseg && it.a0 >= 0 &&
+                                it.a0 <= it.a1 && it.a1 == it.c0 && it.c0 < it.c1 &&
+                                it.c1 <= p.nchunks);
         const int nc = it.c1 - it.c0, nA = it.hasA ? it.a1 - it.a0 : 0, nJ = nA + nc;
         if (*cx.abort) continue;  // issue nothing more once a wait gave up
         bool stop = false;
@@ -776,6 +783,9 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
             ++ns;
             tc_fence_after();
             if (it.pub) {
+                // (a debug check guards the stores only: every thread still
+                // reaches the barrier)
+                const bool okp = LA_DCHECK(p.status, t < p.items && a < D);
                 float4 *d4 = reinterpret_cast<float4 *>(p.agg + (size_t)t * STATE);
 #pragma unroll 1
                 for (int g = 0; g < 4; ++g) {
@@ -785,17 +795,18 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
                     reg_fence(v);
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
-                        d4[(8 * g + u) * 128 + a] =
-                            make_float4(u2f(v[4 * u]), u2f(v[4 * u + 1]), u2f(v[4 * u + 2]),
-                                        u2f(v[4 * u + 3]));
+                        if (okp)
+                            d4[(8 * g + u) * 128 + a] =
+                                make_float4(u2f(v[4 * u]), u2f(v[4 * u + 1]),
+                                            u2f(v[4 * u + 2]), u2f(v[4 * u + 3]));
                 }
                 uint32_t zl = tmem_ld1(lb + TM_S + D);
                 tmem_wait_ld();
                 reg_fence(zl);
-                p.agg[(size_t)t * STATE + D * D + a] = u2f(zl);
+                if (okp) p.agg[(size_t)t * STATE + D * D + a] = u2f(zl);
                 __threadfence();
                 named_bar_sync(BAR_E2, 128);
-                if (et == 0 && it.seg != p.hold_seg) publish_flag(p.flags + t, FLAG_AGG);
+                if (et == 0 && it.seg != p.hold_seg && okp) publish_flag(p.flags + t, FLAG_AGG);
             }
         }
         // The start state: the own phase-A result (TMEM S) plus the part
@@ -918,6 +929,7 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
             }
         }
         if (p.S_out && it.seg == p.nseg - 1) {
+            const bool oks = LA_DCHECK(p.status, it.bh < p.BH && a < D);
             // the state after the sequence's last token (a decode continues
             // from it); the last chunk's update ran
 #pragma unroll 1
@@ -929,13 +941,14 @@ __device__ void state_role(uint8_t *smem, Small &sm, const Params &p, const Ctx 
                 float4 *d4 = reinterpret_cast<float4 *>(p.S_out + ((size_t)it.bh * D + a) * D + 32 * g);
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    d4[u] = make_float4(u2f(v[4 * u]), u2f(v[4 * u + 1]), u2f(v[4 * u + 2]),
-                                        u2f(v[4 * u + 3]));
+                    if (oks)
+                        d4[u] = make_float4(u2f(v[4 * u]), u2f(v[4 * u + 1]), u2f(v[4 * u + 2]),
+                                            u2f(v[4 * u + 3]));
             }
             uint32_t zr = tmem_ld1(lb + TM_S + D);
             tmem_wait_ld();
             reg_fence(zr);
-            p.z_out[(size_t)it.bh * D + a] = u2f(zr);
+            if (oks) p.z_out[(size_t)it.bh * D + a] = u2f(zr);
             tc_fence_before();
             named_bar_sync(BAR_E2, 128);
             if (et == 0) mbar_arrive(&sm.sb_ready);

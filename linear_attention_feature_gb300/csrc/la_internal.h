@@ -9,6 +9,22 @@
 
 namespace la {
 
+// Debug builds (-DLA_DEBUG) check the computed indices of the tensor-core
+// kernels' global-memory accesses on the device.  A failed check records
+// LA_ERR_INTERNAL and the source line in the device status word (the first
+// failure wins; la_check_device_status reports it), and the guarded access
+// is skipped.  Release builds compile the checks away: LA_DCHECK is `true`
+// there and its condition is not evaluated.
+#if defined(__CUDACC__) && defined(LA_DEBUG)
+__device__ __forceinline__ bool dcheck_failed(int *status, int line) {
+    if (atomicCAS(status, 0, (int)LA_ERR_INTERNAL) == 0) atomicExch(status + 1, line);
+    return false;
+}
+#define LA_DCHECK(status, cond) ((cond) ? true : ::la::dcheck_failed((status), __LINE__))
+#else
+#define LA_DCHECK(status, cond) true
+#endif
+
 // Per-head decay, passed to kernels by value (kernel parameter space).
 // has == 0 means g = 1 for every head.
 struct DecayArgs {

@@ -283,7 +283,7 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
             ++n1;
             tc_fence_after();
             float *dst = p.part + (size_t)t * L::STATE;
-            if (act) {
+            if (act && LA_DCHECK(p.status, t >= 0 && t < p.items1 && row < DK)) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t v[32];
@@ -330,6 +330,7 @@ __device__ void epilogue(uint8_t *smem, Small &sm, const Params &p,
 #pragma unroll 2
                 for (int s2 = 0; s2 < p.nseg1; ++s2) {
                     const int pi = (s2 * p.BH + it.bh) * p.nhalf + it.half;
+                    if (!LA_DCHECK(p.status, pi >= 0 && pi < p.items1 && a < DK)) continue;
                     const float *src = p.part + (size_t)pi * L::STATE;
                     const float4 *s4 = reinterpret_cast<const float4 *>(src + a * DV + 32 * h);
 #pragma unroll

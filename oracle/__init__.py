@@ -50,7 +50,10 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    path = build()
+    # LA_ORACLE_LIB: a separately built copy of la_oracle.c (the tests run
+    # the oracle's pins against a copy built with address and
+    # undefined-behaviour sanitizers)
+    path = os.environ.get("LA_ORACLE_LIB") or build()
     lib = ctypes.CDLL(path)
     P = ctypes.c_void_p
     L = ctypes.c_long
