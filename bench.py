@@ -220,19 +220,19 @@ KNOWN_TRAFFIC = {
     # dram__bytes_write.sum of the captured launch; "sources":
     # kernel_sources_digest(kernel) at capture time)
     ("causal_wide_kernel<0>", "bf16_b2h16_n32768_d128"):
-        {"sources": "be95c35f9aa72540", "bytes": 1160145152 + 216721664},
+        {"sources": "02c3fbb34c6aedd3", "bytes": 1160498176 + 216706560},
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "be95c35f9aa72540", "bytes": 552455168 + 82014976},
+        {"sources": "02c3fbb34c6aedd3", "bytes": 552040704 + 82226688},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "9e33a37a51ebf232", "bytes": 100757248 + 4908800},
+        {"sources": "a3a789308229d9b7", "bytes": 100764416 + 5440768},
     ("causal_kernel<64,2>", "bf16_b4h16_n4096_d64"):
-        {"sources": "9e33a37a51ebf232", "bytes": 109958912 + 12057088},
+        {"sources": "a3a789308229d9b7", "bytes": 111546368 + 13187840},
     ("causal_kernel<64,0>+state", "bf16_b4h16_n4096_d64"):
-        {"sources": "9e33a37a51ebf232", "bytes": 100757760 + 4956672},
+        {"sources": "a3a789308229d9b7", "bytes": 100761600 + 5300480},
     ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
-        {"sources": "be95c35f9aa72540", "bytes": 560132096 + 81980416},
+        {"sources": "02c3fbb34c6aedd3", "bytes": 559557120 + 81642496},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
-        {"sources": "f4b32ad6ea1b69a3", "bytes": 100719616 + 3992832},
+        {"sources": "c99e10d20fed1e5d", "bytes": 100719104 + 3817984},
 }
 
 

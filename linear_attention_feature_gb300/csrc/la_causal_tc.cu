@@ -532,13 +532,19 @@ __device__ __forceinline__ void gate_terms(float a, float &l, int &z) {
 // per token (tokens past N count as gate 1), for every chunk at once ahead
 // of the forward kernel: the chunk-local inclusive prefixes of the log2 of
 // the nonzero gates and of the zero-gate count, then the column factors
-// (see GateSlot).
+// (see GateSlot).  The blocks also clear the forward's ticket counter and
+// flags (nclr 16-byte words at clr), and let the forward kernel start its
+// prologue early: it waits for this kernel's completion before it reads
+// anything.
 __global__ void __launch_bounds__(C) gate_slots_kernel(const float *gates, int N, int nchunks,
-                                                       GateSlot *slots) {
+                                                       GateSlot *slots, uint4 *clr, size_t nclr) {
+    grid_dep_launch();
     __shared__ float wl[C / 32], s_l[C];
     __shared__ int wz[C / 32], s_z[C];
     const int c = (int)(blockIdx.x % (unsigned)nchunks), bh = (int)(blockIdx.x / (unsigned)nchunks);
     const int et = threadIdx.x, lane = et & 31, w = et >> 5;
+    for (size_t i = (size_t)blockIdx.x * C + et; i < nclr; i += (size_t)gridDim.x * C)
+        clr[i] = make_uint4(0u, 0u, 0u, 0u);
     const int tok = c * C + et;
     const float a = tok < N ? __ldg(gates + (size_t)bh * N + tok) : 1.f;
     float l;
@@ -1453,6 +1459,8 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the workspace clear before this kernel has completed (dependent launch)
+    grid_dep_wait();
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
@@ -1611,11 +1619,15 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.gprod = reinterpret_cast<float *>(w8 + pl.off_gprod);
     p.slots = reinterpret_cast<const uint8_t *>(w8 + pl.off_slots);
     p.status = status;
-    e = tc_zero_words(ws, pl.off_agg, stream);
-    if (e == cudaSuccess && kMode == 2) {
+    // the ticket counter, abort flag and segment flags start at zero (cleared
+    // by the gate-slot kernel in the gated mode); the states need no clearing
+    if (kMode == 2) {
         gate_slots_kernel<<<(unsigned)(sh.BH() * pl.nchunks), C, 0, stream>>>(
-            gates, N, pl.nchunks, reinterpret_cast<GateSlot *>(w8 + pl.off_slots));
+            gates, N, pl.nchunks, reinterpret_cast<GateSlot *>(w8 + pl.off_slots),
+            static_cast<uint4 *>(ws), pl.off_agg / 16);
         e = cudaGetLastError();
+    } else {
+        e = tc_zero_words(ws, pl.off_agg, stream);
     }
     if (e == cudaSuccess) {
         const size_t smem = smem_bytes<DK, kMode>();
@@ -1624,14 +1636,15 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
                                  (int)smem);
         if (e == cudaSuccess) {
             const int grid = (int)(pl.items < sms ? pl.items : sms);
-            kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p, dk);
-            e = cudaGetLastError();
+            e = tchost::launch_dependent(kern, (unsigned)grid, kThreads, smem, stream, tq, tk,
+                                         tv, to, p, dk);
+            if (e == cudaSuccess) e = cudaGetLastError();
         }
     }
     cudaError_t ef = ws_in ? cudaSuccess : cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return {LA_ERR_CUDA, e, "la_forward: causal kernel launch"};
     if (ef != cudaSuccess) return {LA_ERR_CUDA, ef, "la_forward: workspace free"};
-    note_launches(kMode == 2 ? 3 : 2);  // workspace clear (+ gate slots) + forward
+    note_launches(2);  // workspace clear (with the gate slots when gated) + forward
     return {LA_OK, cudaSuccess, ""};
 }
 
@@ -1779,8 +1792,9 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
                                   (int)smem)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel attribute"};
     const int grid = (int)(items < sms ? items : sms);
-    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p, dk);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+    e = tchost::launch_dependent(kern, (unsigned)grid, kThreads, smem, stream, tq, tk, tv, to,
+                                 p, dk);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel launch"};
     note_launches(2);  // flag clear + forward
     return {LA_OK, cudaSuccess, ""};

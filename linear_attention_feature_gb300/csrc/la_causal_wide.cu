@@ -1023,6 +1023,8 @@ causal_wide_kernel(const __grid_constant__ CUtensorMap tq,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the workspace clear before this kernel has completed (dependent launch)
+    grid_dep_wait();
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
@@ -1138,8 +1140,9 @@ TcResult launch_wide_with(const void *q, const void *k, const void *v, void *out
                                   (int)kSmemBytes)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: kernel attribute"};
     const int grid = (int)(pl.items < sms ? pl.items : sms);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, to, p, dk);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+    e = tchost::launch_dependent(kern, (unsigned)grid, kThreads, kSmemBytes, stream, tq, tk, tv,
+                                 to, p, dk);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: causal kernel launch"};
     note_launches(2);  // workspace clear + forward
     return {LA_OK, cudaSuccess, ""};

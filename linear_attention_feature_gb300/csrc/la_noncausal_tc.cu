@@ -465,6 +465,8 @@ noncausal_kernel(const __grid_constant__ CUtensorMap tq,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the workspace clear before this kernel has completed (dependent launch)
+    grid_dep_wait();
     const uint32_t tmem = sm.tmem_base;
     if (warp == 0) {
         if (lane == 0) producer<DK>(smem, sm, p, cx, &tq, &tk, &tv);
@@ -575,8 +577,9 @@ TcResult launch_noncausal_t(const void *q, const void *k, const void *v,
         if (e == cudaSuccess) {
             const long long all = 2 * pl.items;
             const int grid = (int)(all < sms ? all : sms);
-            kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p);
-            e = cudaGetLastError();
+            e = tchost::launch_dependent(kern, (unsigned)grid, kThreads, smem, stream, tq, tk,
+                                         tv, to, p);
+            if (e == cudaSuccess) e = cudaGetLastError();
         }
     }
     cudaError_t ef = ws_in ? cudaSuccess : cudaFreeAsync(ws, stream);

@@ -40,6 +40,9 @@ size_t tc_workspace_bytes(const FwdShape &sh, int causal, bool decay,
 namespace {
 
 __global__ void zero_words_kernel(uint4 *p, size_t n) {
+    // the forward kernel after this one may start its prologue now; it waits
+    // for this kernel's completion before it reads the cleared words
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_uint4(0u, 0u, 0u, 0u);

@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <utility>
 
 namespace la {
 namespace tchost {
@@ -65,6 +66,26 @@ inline cudaError_t sm_count(int *out) {
     }
     *out = cache[dev];
     return cudaSuccess;
+}
+
+// Launches `kern` on `stream` with programmatic stream serialisation: its
+// CTAs may start (barrier set-up, TMEM allocation, descriptor prefetch)
+// while the kernel before it in the stream, the workspace clear, still runs.
+// The kernel calls griddepcontrol.wait before it touches any global memory.
+template <typename... P, typename... A>
+inline cudaError_t launch_dependent(void (*kern)(P...), unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t stream, A &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
 }
 
 // Chunks per sequence segment for the persistent tensor-core kernels.  A

@@ -105,6 +105,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     return true;
 }
 
+// ------------------------------------------------------- dependent launch
+
+// A kernel launched with programmatic stream serialisation may start while
+// the kernel before it in the stream still runs.  grid_dep_wait() holds the
+// calling thread until that kernel has completed and its writes are visible;
+// grid_dep_launch() lets the kernel after this one start early.
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
