@@ -47,7 +47,7 @@
 // Warp roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-9 feature-map transform, warps 10-13 score epilogue (mask,
 // decay, bf16 P~ in TMEM), warps 14-17 state and output epilogue (bf16
-// [S | z] operand, look-back; O / den, TMA store).  P and (without decay) O
+// [S | z] operand, look-back; O / den stored from registers).  P and O
 // have two TMEM buffers, and the MMA issuer issues P of chunk j+1 ahead of
 // P~V of chunk j when it is ready, so the tensor pipe can run
 // ... SU(j) P(j+1) P~V(j) QS(j+1) SU(j+1) ... without waiting for an
@@ -98,6 +98,7 @@ struct Params {
     float *gprod;          // mode 2: [items] each segment's product of gates
     int *ctrl;          // [0] ticket counter, [1] abort flag
     int *status;        // device status word
+    uint16_t *out;      // [BH][N][DK] bf16 output
     long long timeout;  // clock cycles per bounded wait
 };
 
@@ -123,13 +124,7 @@ struct Layout {
     // second N block of the V operand (reached through the descriptor LBO)
     static constexpr int OFF_ONESX = OFF_SB + SB;
     static constexpr int ONESX = 16384;
-    // output staging: a buffer of its own where shared memory allows (a
-    // stage is then free once its last product completes), else the stage's
-    // Q slot, dead by the time the chunk's output is ready
-    static constexpr bool OWN_OST = DK == 128 && kMode != 2;
-    static constexpr int OFF_OST = OFF_ONESX + ONESX;
-    static constexpr int OST = OWN_OST ? C * DV * 2 : 0;
-    static constexpr int OFF_SMALL = OFF_OST + OST;
+    static constexpr int OFF_SMALL = OFF_ONESX + ONESX;
     static constexpr int STATE = DK * DV + DK;
 };
 
@@ -218,9 +213,9 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p,
         ++tl;
         if (t < 0) break;
         const Item it = decode_item(t, p);
-        LA_DCHECK(p.status, it.bh >= 0 && it.bh < p.BH && it.seg < p.nseg && it.a0 >= 0 &&
-                                it.a0 <= it.a1 && it.a1 == it.c0 && it.c0 < it.c1 &&
-                                it.c1 <= p.nchunks && it.half < p.nhalf);
+        (void)LA_DCHECK(p.status, it.bh >= 0 && it.bh < p.BH && it.seg < p.nseg && it.a0 >= 0 &&
+                                      it.a0 <= it.a1 && it.a1 == it.c0 && it.c0 < it.c1 &&
+                                      it.c1 <= p.nchunks && it.half < p.nhalf);
         for (int pass = it.hasA ? 0 : 1; pass < 2 && !stop; ++pass) {
             const int cb = pass == 0 ? it.a0 : it.c0, ce = pass == 0 ? it.a1 : it.c1;
             for (int c = cb; c < ce; ++c, ++j) {
@@ -489,9 +484,8 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 mma_commit(&sm.pv_done[b]);
             }
             // the stage: one release per consumer (the output epilogue
-            // releases it itself when the output is staged in its Q slot)
+            // gives the second)
             mma_commit(&sm.empty[st]);
-            if (L::OWN_OST) mma_commit(&sm.empty[st]);
         }
         if (final_state) {
             // S's columns are reused by the next item: wait until the
@@ -899,29 +893,28 @@ __device__ void score_epilogue(uint8_t *smem, Small &sm, const Params &p,
     }
 }
 
-// One chunk's output: O / den (O alone without the normaliser), bf16 into
-// the stage's (dead) Q slot, TMA store.  With several stages the
-// stage is released when the next store is issued (the store has read it by
-// then), so the store never stalls this warpgroup.
+// One chunk's output: O / den (O alone without the normaliser) in bf16,
+// stored to global memory from registers, one token row per thread in
+// 16-byte streaming stores (rows past N dropped).  Nothing is staged in
+// shared memory, so the chunk's stage goes back to the producer as soon as
+// its products have completed.
 template <int DK, int kMode>
-__device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
-                                             const Ctx &cx, uint32_t lb,
-                                             int row, int et,
-                                             const Item &it, int c, int j,
-                                             int nb, int &pend, bool norm,
-                                             const CUtensorMap *to) {
+__device__ __forceinline__ void output_chunk(Small &sm, const Params &p, const Ctx &cx,
+                                             uint32_t lb, int row, int et, const Item &it,
+                                             int c, int j, int nb) {
     using L = Layout<DK, kMode>;
-    constexpr bool kDefer = !L::OWN_OST && L::STAGES >= 3;
     const int st = j % L::STAGES;
     const int ob = nb & 1;
     const uint32_t tob = TM_O + 80u * ob;
-    uint8_t *stage_o = L::OWN_OST ? smem + L::OFF_OST : smem + st * L::STAGE + L::OFF_Q;
-    if (L::OWN_OST) {  // the previous chunk's store must have read the buffer
-        if (et == 0) tma_store_wait_read<0>();
-        named_bar_sync(BAR_E2, 128);
-    }
     wait_bar(&sm.o_full[ob], (nb >> 1) & 1, cx);
     tc_fence_after();
+    // the output needs nothing from the stage: its second release (the MMA
+    // issuer's commit is the first, once the chunk's products completed)
+    if (et == 0) mbar_arrive(&sm.empty[st]);
+    const int tok = c * C + row;
+    const bool live = tok < p.N && LA_DCHECK(p.status, it.bh < p.BH && 64 * it.half < DK);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out) +
+                 (((size_t)it.bh * p.N + (live ? tok : 0)) * DK + 64 * it.half) / 8;
     uint32_t dreg = tmem_ld1(lb + tob + DV);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -930,42 +923,26 @@ __device__ __forceinline__ void output_chunk(uint8_t *smem, Small &sm,
         tmem_wait_ld();
         reg_fence(o);
         reg_fence(dreg);
-        const float inv = norm ? 1.f / u2f(dreg) : 1.f;
+        const float inv = p.norm ? 1.f / u2f(dreg) : 1.f;
         if (h == 1) {
             tc_fence_before();
             mbar_arrive(&sm.o_empty[ob]);  // 128 arrivals: O has been read
         }
+        if (live) {
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-            *reinterpret_cast<uint4 *>(stage_o + sw128_offset(row, 32 * h + ch * 8)) =
-                make_uint4(pack_bf16x2(u2f(o[8 * ch]) * inv, u2f(o[8 * ch + 1]) * inv),
-                           pack_bf16x2(u2f(o[8 * ch + 2]) * inv, u2f(o[8 * ch + 3]) * inv),
-                           pack_bf16x2(u2f(o[8 * ch + 4]) * inv, u2f(o[8 * ch + 5]) * inv),
-                           pack_bf16x2(u2f(o[8 * ch + 6]) * inv, u2f(o[8 * ch + 7]) * inv));
-    }
-    fence_async_shared();
-    named_bar_sync(BAR_E2, 128);
-    if (et == 0) {
-        tma_store_3d(to, stage_o, 64 * it.half, c * C, it.bh);
-        tma_store_commit();
-        if (L::OWN_OST) {
-            // the stage was released by the MMA issuer
-        } else if (kDefer) {
-            if (pend >= 0) {
-                tma_store_wait_read<1>();
-                mbar_arrive(&sm.empty[pend]);
-            }
-            pend = st;
-        } else {
-            tma_store_wait_read<0>();
-            mbar_arrive(&sm.empty[st]);
+            for (int ch = 0; ch < 4; ++ch)
+                __stcs(dst + 4 * h + ch,
+                       make_uint4(pack_bf16x2(u2f(o[8 * ch]) * inv, u2f(o[8 * ch + 1]) * inv),
+                                  pack_bf16x2(u2f(o[8 * ch + 2]) * inv, u2f(o[8 * ch + 3]) * inv),
+                                  pack_bf16x2(u2f(o[8 * ch + 4]) * inv, u2f(o[8 * ch + 5]) * inv),
+                                  pack_bf16x2(u2f(o[8 * ch + 6]) * inv, u2f(o[8 * ch + 7]) * inv)));
         }
     }
 }
 
 // ---------------------------------------------------------------- output + state
 
-// Output epilogue (O / den, bf16, TMA store) and state epilogue (bf16 [S | z]
+// Output epilogue (O / den, bf16, stored from registers) and state epilogue (bf16 [S | z]
 // operand of the next chunk, decay rescale, segment publication and
 // look-back) on one warpgroup.  Per chunk j the state of chunk j+1 is
 // prepared first (it gates the next phi(Q) [S | z]), then chunk j's output.
@@ -1130,8 +1107,7 @@ __device__ __forceinline__ void store_zrow(uint8_t *sb_z, int a, float z) {
 
 template <int DK, int kMode>
 __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
-                             const Ctx &cx, const DecayArgs &dk, uint32_t tmem,
-                             const CUtensorMap *to) {
+                             const Ctx &cx, const DecayArgs &dk, uint32_t tmem) {
     using L = Layout<DK, kMode>;
     using SM = SMap<DK>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1145,7 +1121,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
     uint8_t *sb = smem + L::OFF_SB;
     uint8_t *sbz = sb + L::SBLK;
     const int row = ln;  // output row i
-    int tl = 0, ns = 0, j = 0, nb = 0, pend = -1;
+    int tl = 0, ns = 0, j = 0, nb = 0;
     for (;;) {
         const int t = pop_item(sm, tl, cx, BAR_E2, 128, et == 0);
         if (t < 0) break;
@@ -1348,13 +1324,7 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 named_bar_sync(BAR_E2, 128);
                 if (et == 0) mbar_arrive(&sm.sb_ready);
             }
-            output_chunk<DK, kMode>(smem, sm, cx, lb, row, et, it, c, j, nb,
-                                     pend, p.norm != 0, to);
-        }
-        if (et == 0 && pend >= 0) {  // the item's last store: release its stage
-            tma_store_wait_read<0>();
-            mbar_arrive(&sm.empty[pend]);
-            pend = -1;
+            output_chunk<DK, kMode>(sm, p, cx, lb, row, et, it, c, j, nb);
         }
         if (p.S_out && it.seg == p.nseg - 1) {
             // the state after the sequence's last token (a decode continues
@@ -1391,7 +1361,6 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             if (et == 0) mbar_arrive(&sm.sb_ready);
         }
     }
-    if (et == 0) tma_store_wait_all<0>();
 }
 
 // ---------------------------------------------------------------- kernel
@@ -1400,8 +1369,7 @@ template <int DK, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_kernel(const __grid_constant__ CUtensorMap tq,
               const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv,
-              const __grid_constant__ CUtensorMap to, const Params p,
+              const __grid_constant__ CUtensorMap tv, const Params p,
               const DecayArgs dk) {
     using L = Layout<DK, kMode>;
     extern __shared__ uint8_t smem_raw[];
@@ -1454,7 +1422,6 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
-        tma_prefetch_desc(&to);
     }
     tc_fence_before();
     __syncthreads();
@@ -1472,7 +1439,7 @@ causal_kernel(const __grid_constant__ CUtensorMap tq,
     } else if (warp < kWarpE2) {
         score_epilogue<DK, kMode>(smem, sm, p, cx, dk, tmem);
     } else {
-        output_state<DK, kMode>(smem, sm, p, cx, dk, tmem, &to);
+        output_state<DK, kMode>(smem, sm, p, cx, dk, tmem);
     }
 
     tc_fence_before();
@@ -1573,12 +1540,11 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
                          float *z_out, const float *gates, cudaStream_t stream) {
     using namespace causal_tc;
     const int BH = (int)sh.BH(), N = sh.N;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     cudaError_t e;
     if ((e = tchost::make_seq_map(&tq, q, BH, N, DK, C)) != cudaSuccess ||
         (e = tchost::make_seq_map(&tk, k, BH, N, DK, C)) != cudaSuccess ||
-        (e = tchost::make_seq_map(&tv, v, BH, N, DK, C)) != cudaSuccess ||
-        (e = tchost::make_seq_map(&to, out, BH, N, DK, C)) != cudaSuccess)
+        (e = tchost::make_seq_map(&tv, v, BH, N, DK, C)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward: TMA descriptor"};
     int sms = 0;
     if ((e = tchost::sm_count(&sms)) != cudaSuccess)
@@ -1619,6 +1585,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
     p.gprod = reinterpret_cast<float *>(w8 + pl.off_gprod);
     p.slots = reinterpret_cast<const uint8_t *>(w8 + pl.off_slots);
     p.status = status;
+    p.out = static_cast<uint16_t *>(out);
     // the ticket counter, abort flag and segment flags start at zero (cleared
     // by the gate-slot kernel in the gated mode); the states need no clearing
     if (kMode == 2) {
@@ -1637,7 +1604,7 @@ TcResult launch_causal_t(const void *q, const void *k, const void *v, void *out,
         if (e == cudaSuccess) {
             const int grid = (int)(pl.items < sms ? pl.items : sms);
             e = tchost::launch_dependent(kern, (unsigned)grid, kThreads, smem, stream, tq, tk,
-                                         tv, to, p, dk);
+                                         tv, p, dk);
             if (e == cudaSuccess) e = cudaGetLastError();
         }
     }
@@ -1734,12 +1701,11 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     using namespace causal_tc;
     using L = Layout<DK, kMode>;
     const int BH = (int)sh.BH(), N = sh.N;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     cudaError_t e;
     if ((e = tchost::make_seq_map(&tq, q, BH, N, DK, C)) != cudaSuccess ||
         (e = tchost::make_seq_map(&tk, k, BH, N, DK, C)) != cudaSuccess ||
-        (e = tchost::make_seq_map(&tv, v, BH, N, DK, C)) != cudaSuccess ||
-        (e = tchost::make_seq_map(&to, out, BH, N, DK, C)) != cudaSuccess)
+        (e = tchost::make_seq_map(&tv, v, BH, N, DK, C)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: TMA descriptor"};
     int sms = 0;
     if ((e = tchost::sm_count(&sms)) != cudaSuccess)
@@ -1783,6 +1749,7 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
     p.flags = reinterpret_cast<int *>(scratch + 256);
     p.agg = reinterpret_cast<float *>(scratch + off_agg);
     p.status = status;
+    p.out = static_cast<uint16_t *>(out);
     // the counter and flags must start at zero; the states need no clearing
     if ((e = tc_zero_words(scratch, off_agg, stream)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: clearing flags"};
@@ -1792,8 +1759,8 @@ TcResult launch_causal_noalloc_t(const void *q, const void *k, const void *v,
                                   (int)smem)) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel attribute"};
     const int grid = (int)(items < sms ? items : sms);
-    e = tchost::launch_dependent(kern, (unsigned)grid, kThreads, smem, stream, tq, tk, tv, to,
-                                 p, dk);
+    e = tchost::launch_dependent(kern, (unsigned)grid, kThreads, smem, stream, tq, tk, tv, p,
+                                 dk);
     if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess)
         return {LA_ERR_CUDA, e, "la_forward_causal_noalloc: kernel launch"};
     note_launches(2);  // flag clear + forward

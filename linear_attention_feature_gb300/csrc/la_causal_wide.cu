@@ -275,9 +275,9 @@ __device__ void producer(uint8_t *smem, Small &sm, const Params &p, const Ctx &c
         ++tl;
         if (t < 0) break;
         const Item it = decode_item(t, p);
-        LA_DCHECK(p.status, it.bh >= 0 && it.bh < p.BH && it.seg < p.nseg && it.a0 >= 0 &&
-                                it.a0 <= it.a1 && it.a1 == it.c0 && it.c0 < it.c1 &&
-                                it.c1 <= p.nchunks);
+        (void)LA_DCHECK(p.status, it.bh >= 0 && it.bh < p.BH && it.seg < p.nseg && it.a0 >= 0 &&
+                                      it.a0 <= it.a1 && it.a1 == it.c0 && it.c0 < it.c1 &&
+                                      it.c1 <= p.nchunks);
         const int nc = it.c1 - it.c0, nA = it.hasA ? it.a1 - it.a0 : 0, nJ = nA + nc;
         if (*cx.abort) continue;  // issue nothing more once a wait gave up
         bool stop = false;
