@@ -224,11 +224,11 @@ KNOWN_TRAFFIC = {
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
         {"sources": "02c3fbb34c6aedd3", "bytes": 552040704 + 82226688},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "a3a789308229d9b7", "bytes": 100764416 + 5440768},
+        {"sources": "cc7d12846f4e3b11", "bytes": 100766720 + 4931328},
     ("causal_kernel<64,2>", "bf16_b4h16_n4096_d64"):
-        {"sources": "a3a789308229d9b7", "bytes": 111546368 + 13187840},
+        {"sources": "cc7d12846f4e3b11", "bytes": 109208320 + 9956864},
     ("causal_kernel<64,0>+state", "bf16_b4h16_n4096_d64"):
-        {"sources": "a3a789308229d9b7", "bytes": 100761600 + 5300480},
+        {"sources": "cc7d12846f4e3b11", "bytes": 100805376 + 4865792},
     ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
         {"sources": "02c3fbb34c6aedd3", "bytes": 559557120 + 81642496},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
