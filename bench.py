@@ -226,7 +226,7 @@ KNOWN_TRAFFIC = {
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
         {"sources": "cc7d12846f4e3b11", "bytes": 100766720 + 4931328},
     ("causal_kernel<64,2>", "bf16_b4h16_n4096_d64"):
-        {"sources": "cc7d12846f4e3b11", "bytes": 109208320 + 9956864},
+        {"sources": "4abcad99685fb400", "bytes": 105626112 + 5544192},
     ("causal_kernel<64,0>+state", "bf16_b4h16_n4096_d64"):
         {"sources": "cc7d12846f4e3b11", "bytes": 100805376 + 4865792},
     ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
