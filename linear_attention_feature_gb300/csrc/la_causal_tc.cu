@@ -408,6 +408,13 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 issue_p<DK, kMode>(smem, sm, cx, tmem, jj, nbq);
                 ++p_next;
             }
+            // whether the chunk's weights fold, read now (its gate slot has
+            // landed: P of the chunk is issued) and used after the waits
+            // below, so that the load's latency stays off the issue path
+            const bool wait_khat =
+                kMode && !chunk_folds<kMode>(lg, *reinterpret_cast<const GateSlot *>(
+                                                     smem + st * L::STAGE + L::OFF_GS),
+                                             min(C, p.N - (it.c0 + qi) * C), p.phi);
             const uint32_t qb = smem_u32(smem + st * L::STAGE + L::OFF_Q);
             const uint32_t kb = smem_u32(smem + st * L::STAGE + L::OFF_K);
             const uint32_t vb = smem_u32(smem + st * L::STAGE + L::OFF_V);
@@ -429,9 +436,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 wait_bar(&sm.sb_ready, nsb & 1, cx);
                 ++nsb;
                 // with weights: Qhat, Khat in place (after P(j) read them)
-                if (kMode && !chunk_folds<kMode>(lg, *reinterpret_cast<const GateSlot *>(
-                                                         smem + st * L::STAGE + L::OFF_GS),
-                                                     min(C, p.N - (it.c0 + qi) * C), p.phi)) {
+                if (wait_khat) {
                     wait_bar(&sm.khat_ready[nk & 1], (nk >> 1) & 1, cx);
                     ++nk;
                 }
@@ -454,9 +459,7 @@ __device__ void mma_issuer(uint8_t *smem, Small &sm, const Params &p,
                 // with weights: Qhat_i = g^(i+1) phi(q_i) and Khat_t =
                 // g^(n-1-t) phi(k_t) (or the products of gates) in place,
                 // once P(j) has read the unweighted rows
-                if (kMode && !chunk_folds<kMode>(lg, *reinterpret_cast<const GateSlot *>(
-                                                         smem + st * L::STAGE + L::OFF_GS),
-                                                     min(C, p.N - (it.c0 + qi) * C), p.phi)) {
+                if (wait_khat) {
                     wait_bar(&sm.khat_ready[nk & 1], (nk >> 1) & 1, cx);
                     ++nk;
                 }
@@ -1208,9 +1211,9 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
             }
         }
         if (kMode == 2) {
-            // the first chunk's product of gates (its transform wrote the
-            // prefix before the stage's xf)
-            wait_bar(&sm.xf[j % L::STAGES], (j / L::STAGES) & 1, cx);
+            // the first chunk's product of gates, from its gate slot (copied
+            // in with the chunk's tiles)
+            wait_bar(&sm.full[j % L::STAGES], (j / L::STAGES) & 1, cx);
             f0 = gate_prod(*reinterpret_cast<const GateSlot *>(
                                smem + (j % L::STAGES) * L::STAGE + L::OFF_GS),
                            n0 - 1, -1);
@@ -1288,7 +1291,9 @@ __device__ void output_state(uint8_t *smem, Small &sm, const Params &p,
                 float f = gpow(lg, n);
                 if (kMode == 2) {
                     const int j1 = j + 1;
-                    wait_bar(&sm.xf[j1 % L::STAGES], (j1 / L::STAGES) & 1, cx);
+                    // the gate slot has landed with the tiles (no need to
+                    // wait for the chunk's feature map)
+                    wait_bar(&sm.full[j1 % L::STAGES], (j1 / L::STAGES) & 1, cx);
                     f = gate_prod(*reinterpret_cast<const GateSlot *>(
                                       smem + (j1 % L::STAGES) * L::STAGE + L::OFF_GS),
                                   n - 1, -1);
