@@ -224,11 +224,11 @@ KNOWN_TRAFFIC = {
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
         {"sources": "a3c2a2e658e48689", "bytes": 552642304 + 82396160},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "cc7d12846f4e3b11", "bytes": 100766720 + 4931328},
+        {"sources": "8bb38ad5cd466e29", "bytes": 100783104 + 5150464},
     ("causal_kernel<64,2>", "bf16_b4h16_n4096_d64"):
-        {"sources": "4abcad99685fb400", "bytes": 105626112 + 5544192},
+        {"sources": "8bb38ad5cd466e29", "bytes": 105599232 + 5204736},
     ("causal_kernel<64,0>+state", "bf16_b4h16_n4096_d64"):
-        {"sources": "cc7d12846f4e3b11", "bytes": 100805376 + 4865792},
+        {"sources": "8bb38ad5cd466e29", "bytes": 100782592 + 5165824},
     ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
         {"sources": "a3c2a2e658e48689", "bytes": 559840512 + 82061824},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
