@@ -186,8 +186,16 @@ def capture(fn):
     return g.replay, launches
 
 
-def timed_steps(fn, K, W, world, flush=None):
-    """Per-step CUDA-event durations (ms) of K steps after W warm-ups."""
+def timed_steps(fn, K, W, world, flush=None, name="timed"):
+    """Per-step CUDA-event durations (ms) of K steps after W warm-ups, the
+    warm-ups and the timed steps inside one NVTX range `la/<name>` (so that
+    a profiler can select a leg's launches by range)."""
+    import torch
+    with torch.cuda.nvtx.range("la/" + name):
+        return _timed_steps(fn, K, W, world, flush)
+
+
+def _timed_steps(fn, K, W, world, flush):
     import torch
     for _ in range(W):
         fn()
@@ -341,7 +349,7 @@ def run_ours(args):
     out = torch.empty_like(q)
     main_fn = lambda: la.forward(q, k, v, causal=True, out=out)  # noqa: E731
     replay, per_call = capture(main_fn)
-    steps_ms = timed_steps(replay, K, W, world, flush)
+    steps_ms = timed_steps(replay, K, W, world, flush, name=MAIN)
     launches = per_call * K  # library kernels inside the timed region
     la.check_device_status()
     ms = max_over_ranks(sum(steps_ms) / K, world)
@@ -366,7 +374,7 @@ def run_ours(args):
 
     def e2e_fn():
         la.forward_host(qh, kh, vh, causal=True, out=oh, workspace=ws)
-    e2e_ms = timed_steps(e2e_fn, K, W, world)
+    e2e_ms = timed_steps(e2e_fn, K, W, world, name=MAIN + " e2e")
     e2e_t = max_over_ranks(sum(e2e_ms) / K, world)
     e2e = {"value": round(tokens_step * world / (e2e_t * 1e-3), 1),
            "unit": "tokens/s", "h2d_bytes_per_step": 3 * q.numel() * 2,
@@ -461,7 +469,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
                 extra = 4 * w.B * w.H * (w.d * w.d + w.d)
                 form = "state"
             replay, _ = capture(fn)
-            steps = timed_steps(replay, Kx, Wx, world, flush)
+            steps = timed_steps(replay, Kx, Wx, world, flush, name=f"{wkey} {form}")
             la.check_device_status()
             ms = max_over_ranks(sum(steps) / Kx, world)
             r = {"tokens_per_s": round(w.B * w.N * world / (ms * 1e-3), 1),
@@ -513,7 +521,7 @@ def run_other_paths(args, la, wl, dev, flush, peaks, world, rank, keep):
         alpha = alpha.view(1, w.H, 1).expand(w.B, w.H, w.N).contiguous()
         oo = torch.empty_like(qq)
         replay, _ = capture(lambda: la.forward_delta(qq, kn, vv, beta, alpha, out=oo))
-        steps = timed_steps(replay, Kx, Wx, world, flush)
+        steps = timed_steps(replay, Kx, Wx, world, flush, name=name)
         la.check_device_status()
         ms = max_over_ranks(sum(steps) / Kx, world)
         res[name] = {"tokens_per_s": round(w.B * w.N * world / (ms * 1e-3), 1),
@@ -605,10 +613,11 @@ def run_delta_decode(la, wl, dev, peaks, world, rank, args, keep=None, name=None
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    replay()
-    e1.record(st)
-    torch.cuda.synchronize()
+    with torch.cuda.nvtx.range("la/" + (name or "decode")):
+        e0.record(st)
+        replay()
+        e1.record(st)
+        torch.cuda.synchronize()
     barrier(world)
     la.check_device_status()
     ms_total = max_over_ranks(e0.elapsed_time(e1), world)
@@ -657,10 +666,11 @@ def run_decode(la, wl, dev, peaks, world, rank, args, decay=None, keep=None,
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    replay()
-    e1.record(st)
-    torch.cuda.synchronize()
+    with torch.cuda.nvtx.range("la/" + (name or "decode")):
+        e0.record(st)
+        replay()
+        e1.record(st)
+        torch.cuda.synchronize()
     barrier(world)
     la.check_device_status()
     ms_total = max_over_ranks(e0.elapsed_time(e1), world)
