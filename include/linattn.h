@@ -334,7 +334,11 @@ la_status la_forward_delta(const void *q, const void *k, const void *v, void *ou
  * causal kernels keeps until the process exits.  The call makes no
  * cudaMalloc/cudaFree or other allocating call.  It enqueues two kernels on
  * `stream`: a small zeroing kernel that clears the part of the scratch that
- * must start at zero (ticket counter and segment flags), then the forward.
+ * must start at zero (ticket counter and segment flags), then the forward,
+ * launched with programmatic stream serialisation: it may run its set-up
+ * while the zeroing kernel finishes and waits for it (griddepcontrol.wait)
+ * before touching memory; stream capture records a programmatic edge
+ * between the two kernel nodes.
  *   - Sequence segments are lengthened until the workspace fits the
  *     scratch; if it cannot fit even with one segment per head the call
  *     returns LA_ERR_UNSUPPORTED ("needs more workspace than ...") and
