@@ -232,11 +232,11 @@ KNOWN_TRAFFIC = {
     ("causal_wide_kernel<2>", "bf16_decay_b4h8_n16384_d128"):
         {"sources": "a3c2a2e658e48689", "bytes": 552642304 + 82396160},
     ("causal_kernel<64,0>", "bf16_b4h16_n4096_d64"):
-        {"sources": "8bb38ad5cd466e29", "bytes": 100783104 + 5150464},
+        {"sources": "ddb510b143bbb274", "bytes": 100765696 + 4827392},
     ("causal_kernel<64,2>", "bf16_b4h16_n4096_d64"):
-        {"sources": "8bb38ad5cd466e29", "bytes": 105599232 + 5204736},
+        {"sources": "ddb510b143bbb274", "bytes": 105593600 + 5026816},
     ("causal_kernel<64,0>+state", "bf16_b4h16_n4096_d64"):
-        {"sources": "8bb38ad5cd466e29", "bytes": 100782592 + 5165824},
+        {"sources": "ddb510b143bbb274", "bytes": 100765952 + 4875008},
     ("causal_wide_kernel<1>", "bf16_decay_b4h8_n16384_d128"):
         {"sources": "a3c2a2e658e48689", "bytes": 559840512 + 82061824},
     ("noncausal_kernel<64>", "bf16_b4h16_n4096_d64"):
